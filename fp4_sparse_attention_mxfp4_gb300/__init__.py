@@ -1,0 +1,34 @@
+"""MXFP4 DSA lightning indexer for GB300 (sm_103a).
+
+The compute lives in the CUDA library ``libidxfp4.so`` (C ABI in ``include/idx_fp4.h``);
+this package is its Python binding plus the build step. Calls take CUDA tensors and run
+asynchronously on the current (or given) stream:
+
+    idx_fp4_quant_and_cache        bf16 keys -> paged MXFP4 cache (and q -> plain MXFP4)
+    idx_fp4_build_decode_schedule  once per decode step: the persistent-grid work table
+    idx_fp4_decode_logits_topk     decode: score every cached key of each sequence, top-k
+    idx_fp4_prefill_logits_topk    causal prefill: score keys [0, row_end) per row, top-k
+"""
+from ._lib import (  # noqa: F401
+    DEV_BAD_CTX,
+    DEV_BAD_PAGE,
+    DEV_BAD_ROWS,
+    DEV_BAD_SCHEDULE,
+    DEV_BAD_SLOT,
+    DEV_TIMEOUT,
+    IDX_FP4_MAX_TOPK,
+    IdxFp4Error,
+    idx_fp4_build_decode_schedule,
+    idx_fp4_decode_logits_topk,
+    idx_fp4_decode_schedule_bytes,
+    idx_fp4_decode_workspace_bytes,
+    idx_fp4_prefill_logits_topk,
+    idx_fp4_prefill_workspace_bytes,
+    idx_fp4_quant_and_cache,
+    lib,
+    library_path,
+)
+from .build import build as build_library  # noqa: F401
+
+PAGE = 64
+HEAD_DIM = 128

@@ -1,0 +1,175 @@
+/*
+ * idx_fp4 — MXFP4 DSA lightning indexer for GB300 (sm_103a): C ABI.
+ *
+ * The indexer keeps index keys as MXFP4 in a paged cache and, for each query row q,
+ * scores every visible key t as
+ *
+ *     logit[q, t] = sum_h w[q, h] * relu(q_h . k_t)
+ *
+ * then returns the top-k keys by logit. Sources, by page and section:
+ *   "Score a DSA sparse indexer in FP4" (ROCm/ATOM pull 2216)
+ *     - squashed commit message: keys stored as packed E2M1 plus e8m0 scales; one index
+ *       region declared in two planes, read in place by prefill and decode; decode and
+ *       prefill scorers driven by a persistent-grid CTA schedule built once per step at a
+ *       CUDA-graph-stable address; index_head_dim 128; page block size 64;
+ *     - review finding 2 and the sub-commit "Use the index scale plane's own row order
+ *       when staging FP4 prefill under DCP": the packed plane's in-page rows are flat, the
+ *       scale plane stores them as a 16x4 transpose, slot (row % 16) * 4 + row / 16;
+ *     - sub-commit "Schedule, refuse and document the FP4 indexer paths the review found":
+ *       the fused writer skips slots < 0; a schedule that under-covers rows is an error,
+ *       never a silent truncation; the prefill top-k takes per-row key bounds; padding
+ *       rows carry zero weights.
+ *   "PCP correctness fixes" (ROCm/ATOM pull 2125), Technical Details section 3: padding
+ *       rows are folded into the last request's group at position 0 and read no key.
+ *
+ * Conventions for every call
+ *   - Pointers marked "device" are device pointers owned by the caller; the library
+ *     keeps no global state and allocates no memory. Host sizing functions say how large
+ *     the caller's schedule and workspace buffers must be.
+ *   - Every call is asynchronous on `stream`, launches only kernels, and may be captured
+ *     into a CUDA graph. Nothing is sized from device data, so a captured graph may be
+ *     replayed after the device-side inputs (context lengths, row ends, tables) change.
+ *   - Return value: IDX_FP4_OK, or an IDX_FP4_ERR_* code from host-side argument checks
+ *     (nothing is launched then), or IDX_FP4_ERR_CUDA if a launch failed.
+ *   - `status_dev` (device int32, nullable): kernels OR IDX_FP4_DEV_* bits into it when
+ *     they meet invalid device data (a slot past the pool, a page id outside the pool, a
+ *     context longer than the table, row ends past the context, an inconsistent
+ *     schedule). The offending work is skipped or clamped to safe addresses; no kernel
+ *     traps. The caller clears the word; the library only sets bits.
+ *   - Shape gate (mirrors the structural gate on the pages; there is no fallback):
+ *     head_dim 128 and page 64 are fixed by the layout; num_heads in {16, 32, 64, 128};
+ *     1 <= topk <= IDX_FP4_MAX_TOPK. A mismatch returns IDX_FP4_ERR_SHAPE.
+ *
+ * Data layout
+ *   kv_packed  uint8 [num_pages][4][64][16]  group g holds dims 32g..32g+31 of the key in
+ *              row `row` of page `page`, two E2M1 codes per byte, even dim in the low nibble.
+ *   kv_scale   uint8 [num_pages][4][64]      e8m0 scale of (page, group g, row) at index
+ *              [page][g][(row % 16) * 4 + row / 16].
+ *   q_packed   uint8 [rows][num_heads][64]   plain, dims in order, even dim in the low nibble.
+ *   q_scale    uint8 [rows][num_heads][4]    plain e8m0 scale per 32 dims.
+ *   weights    float [rows][num_heads]
+ *   block_tables int32 [tables][block_table_stride]: logical page i of table b is
+ *              block_tables[b * block_table_stride + i]; entries past the last page a row
+ *              reads are never read.
+ *   topk_idx   int32 [rows][topk]: selected logical token indices in ascending order, then
+ *              -1; topk_val float [rows][topk] (nullable): their logits, then -inf.
+ *   Selection is exact: the min(topk, n) keys with the largest logits, ties going to the
+ *   lower token index.
+ */
+#ifndef IDX_FP4_H
+#define IDX_FP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IDX_FP4_OK 0
+#define IDX_FP4_ERR_ARG 1      /* null pointer where one is required, negative size, bad stride */
+#define IDX_FP4_ERR_SHAPE 2    /* unsupported num_heads or topk */
+#define IDX_FP4_ERR_CAPACITY 3 /* a caller buffer is smaller than the sizing function requires */
+#define IDX_FP4_ERR_CUDA 4     /* a CUDA launch or device query failed */
+
+#define IDX_FP4_DEV_BAD_SLOT 0x01     /* writer: slot >= num_pages * 64 (token skipped) */
+#define IDX_FP4_DEV_BAD_PAGE 0x02     /* scorer: page id outside [0, num_pages) (page 0 read instead) */
+#define IDX_FP4_DEV_BAD_CTX 0x04      /* context < 0, > max_ctx, or past the block-table width */
+#define IDX_FP4_DEV_BAD_ROWS 0x08     /* prefill: cu_seqlens not monotone / not ending at num_rows, or a
+                                         row end past its request's context (clamped) */
+#define IDX_FP4_DEV_BAD_SCHEDULE 0x10 /* decode: schedule built for another batch or grid, or ctx_lens
+                                         changed since it was built (call skipped) */
+#define IDX_FP4_DEV_TIMEOUT 0x20      /* a bounded on-chip wait gave up (results undefined) */
+
+#define IDX_FP4_MAX_TOPK 2048
+
+/* Writer: quantise bf16 keys to MXFP4 and store them in the paged cache; optionally quantise
+ * query heads to the plain MXFP4 layout. ("Score a DSA sparse indexer in FP4", squashed commit
+ * message: the FP4 output mode of the fused writer; sub-commit "Schedule, refuse and document
+ * ...": slots < 0 are skipped.)
+ *   k_bf16        device uint16 [num_tokens][128], bf16 bit patterns (may be NULL if num_tokens == 0)
+ *   slot_mapping  device int32 [num_tokens]; token i goes to page slot/64, row slot%64; slot < 0
+ *                 is skipped; slot >= num_pages*64 sets IDX_FP4_DEV_BAD_SLOT and is skipped
+ *   kv_packed, kv_scale  device cache planes (layout above), written in place
+ *   q_bf16        device uint16 [num_q_rows][num_heads][128] or NULL (then q is not touched)
+ *   q_packed, q_scale    device outputs [num_q_rows][num_heads][64] / [..][4] (required iff q_bf16)
+ * Quantiser: per 32 dims, scale 2^e with e the smallest integer such that max|x| <= 6 * 2^e
+ * (byte e + 127; an all-zero block gets byte 0); each element rounds to the nearest E2M1 value,
+ * ties to the even code; the sign bit is set iff the input is negative. */
+int idx_fp4_quant_and_cache(const uint16_t *k_bf16, int64_t num_tokens, const int32_t *slot_mapping,
+                            uint8_t *kv_packed, uint8_t *kv_scale, int64_t num_pages, const uint16_t *q_bf16,
+                            int64_t num_q_rows, int num_heads, uint8_t *q_packed, uint8_t *q_scale,
+                            int32_t *status_dev, cudaStream_t stream);
+
+/* Bytes of the decode schedule buffer for up to `max_batch` sequences (host, no device work). */
+size_t idx_fp4_decode_schedule_bytes(int max_batch);
+
+/* Build the decode CTA schedule once per step, before the layers; every decode call of the
+ * step reads it. ("Score a DSA sparse indexer in FP4", squashed commit message and PR section
+ * "Decode grid floor": a persistent-grid schedule built once a step at a CUDA-graph-stable
+ * address; here the grid is sized to the work — each CTA gets an equal share of 128-key tiles
+ * — instead of to a fixed floor, and the count lives on the device.)
+ *   ctx_lens_dev  device int32 [batch]: keys visible to each sequence (0 allowed)
+ *   batch <= max_batch; max_ctx bounds every context (larger sets IDX_FP4_DEV_BAD_CTX and the
+ *   sequence is treated as empty)
+ *   sched_dev     device buffer of sched_bytes >= idx_fp4_decode_schedule_bytes(max_batch)
+ * The schedule targets the current device's SM count; use it on that device. */
+int idx_fp4_build_decode_schedule(const int32_t *ctx_lens_dev, int batch, int max_batch, int64_t max_ctx,
+                                  void *sched_dev, size_t sched_bytes, int32_t *status_dev, cudaStream_t stream);
+
+/* Bytes of the decode workspace (candidate lists of sequences split across CTAs). */
+size_t idx_fp4_decode_workspace_bytes(int max_batch, int topk);
+
+/* Decode: one query row per sequence b scores keys [0, ctx_lens[b]) through block_tables[b]
+ * and selects its top-k. ("Score a DSA sparse indexer in FP4": the decode scorer reads q,
+ * q_scale, the paged planes, the block table and the CTA schedule; the top-k of a row is
+ * bounded by its context.) Logits never leave the chip unless logits_debug is given.
+ *   q_packed [batch][H][64], q_scale [batch][H][4], weights [batch][H]   device
+ *   kv_packed, kv_scale, num_pages   the cache
+ *   block_tables, block_table_stride  device int32 [batch][stride]
+ *   ctx_lens_dev   the vector the schedule was built from (checked against it)
+ *   sched_dev/sched_bytes   from idx_fp4_build_decode_schedule for this batch
+ *   workspace      device, >= idx_fp4_decode_workspace_bytes(max_batch, topk)
+ *   topk_idx [batch][topk] (device, required), topk_val [batch][topk] (nullable)
+ *   logits_debug   nullable device float [batch][logits_stride]: every scored logit (testing) */
+int idx_fp4_decode_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
+                               const uint8_t *kv_packed, const uint8_t *kv_scale, int64_t num_pages,
+                               const int32_t *block_tables, int block_table_stride, const int32_t *ctx_lens_dev,
+                               int batch, int num_heads, int topk, const void *sched_dev, size_t sched_bytes,
+                               void *workspace, size_t workspace_bytes, int32_t *topk_idx, float *topk_val,
+                               float *logits_debug, int64_t logits_stride, int32_t *status_dev,
+                               cudaStream_t stream);
+
+/* Bytes of the prefill workspace (its per-call unit table). */
+size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_heads);
+
+/* Causal prefill: row r of request g (cu_seqlens[g] <= r < cu_seqlens[g+1]) scores keys
+ * [0, row_ends[r]) through block_tables[g] and selects its top-min(topk, row_ends[r]).
+ * ("Score a DSA sparse indexer in FP4": the prefill scorer finds a row's page table through
+ * its group and takes per-row key bounds; "PCP correctness fixes", section 3: padding rows sit
+ * at position 0 in the last request's group and read no key — here they carry row_end 0 and
+ * come out as all -1.)
+ *   q_packed [num_rows][H][64], q_scale [num_rows][H][4], weights [num_rows][H]   device
+ *   ctx_lens_dev [num_requests]: keys cached per request; row_ends[r] <= ctx_lens[g] is checked
+ *   cu_seqlens_dev [num_requests + 1], non-decreasing, cu_seqlens[0] = 0, cu_seqlens[G] = num_rows
+ *   row_ends_dev [num_rows]: a real row at 0-based position p carries p + 1
+ *   workspace  device, >= idx_fp4_prefill_workspace_bytes(num_requests, num_rows, num_heads)
+ *   topk_idx [num_rows][topk] (required), topk_val (nullable), logits_debug as for decode */
+int idx_fp4_prefill_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
+                                const uint8_t *kv_packed, const uint8_t *kv_scale, int64_t num_pages,
+                                const int32_t *block_tables, int block_table_stride, const int32_t *ctx_lens_dev,
+                                const int32_t *cu_seqlens_dev, const int32_t *row_ends_dev, int num_requests,
+                                int num_rows, int num_heads, int topk, void *workspace, size_t workspace_bytes,
+                                int32_t *topk_idx, float *topk_val, float *logits_debug, int64_t logits_stride,
+                                int32_t *status_dev, cudaStream_t stream);
+
+/* Human-readable name of a return code. */
+const char *idx_fp4_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDX_FP4_H */

@@ -1,0 +1,235 @@
+"""GPU parity of the writer, the decode schedule and the decode scorer against the oracle.
+
+Every call goes through the C ABI (via the ctypes binding). Floating-point outputs are held to
+|gpu - ref| <= 1e-4 * (1 + |ref|); quantised bytes and selected index sets are exact (the sets up
+to keys tied with the k-th value within that tolerance).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import fp4_sparse_attention_mxfp4_gb300 as fx
+from gpu_helpers import (DecodeRun, assert_cache_equal, assert_logits_close, assert_topk_match, bf16_dev, dev,
+                         new_cache, oracle_cache)
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_side(case):
+    kv_p, kv_s = oracle_cache(case.layout.num_pages, case.k_bf16, case.all_slots())
+    qp, qs = oracle.quantize_plain(case.q_bf16)
+    return kv_p, kv_s, qp, qs
+
+
+def _check_decode(run: DecodeRun, ref, rows=None, full_logits=True):
+    case = run.case
+    kv_p, kv_s, qp, qs = ref
+    idx = run.topk_idx.cpu().numpy()
+    val = run.topk_val.cpu().numpy()
+    lg = run.logits.cpu().numpy() if run.logits is not None else None
+    rows = range(case.batch) if rows is None else rows
+    for b in rows:
+        c = int(case.ctx_lens[b])
+        ref_lg = oracle.row_logits(qp, qs, case.w, b, kv_p, kv_s, case.layout.block_tables[b], 0, c)
+        if lg is not None and full_logits:
+            assert_logits_close(lg[b, :c], ref_lg, f"{case.name} seq {b} logits")
+        assert_topk_match(idx[b], val[b], ref_lg, case.topk, f"{case.name} seq {b}")
+    assert int(run.status.item()) == 0, f"status {int(run.status.item()):#x}"
+
+
+def test_writer_bytes_match_oracle():
+    case = synth.decode_config(1)
+    run = DecodeRun(case)
+    torch.cuda.synchronize()
+    kv_p, kv_s, qp, qs = _oracle_side(case)
+    assert_cache_equal(run.kv_p, run.kv_s, kv_p, kv_s)
+    assert np.array_equal(run.q_packed.cpu().numpy(), qp)
+    assert np.array_equal(run.q_scale.cpu().numpy(), qs)
+
+
+def test_writer_edge_values_and_skips():
+    # Hand-built rows: exact grid points, every rounding midpoint, zeros, tiny and huge
+    # magnitudes, subnormals, negative values rounding to -0; negative slots skipped.
+    rng = synth.Rng(91)
+    rows = []
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5.0,
+                     -6.0, 0.0, -0.0, 0.1, -0.1, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 4.5, 5.5, -5.9, 5.99, 0.2, -0.01],
+                    np.float32)
+    for scale in (1.0, 2.0 ** -20, 2.0 ** 40, 2.0 ** -130, 2.0 ** 120):
+        x = np.tile(mids, 4) * np.float32(scale)
+        rows.append(x)
+    rows.append(np.zeros(128, np.float32))
+    rows.append(rng.normal(128).astype(np.float32) * 1e-38)
+    for _ in range(9):
+        rows.append((rng.normal(128) * np.exp(rng.normal(128) * 3)).astype(np.float32))
+    x = synth.bf16_bits(np.stack(rows))
+    T = x.shape[0]
+    pages = 3
+    slots = np.array([(i * 37) % (pages * 64) for i in range(T)], np.int32)
+    slots[[2, 5, 11]] = -1
+    kv_p, kv_s = new_cache(pages)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fx.idx_fp4_quant_and_cache(bf16_dev(x), dev(slots), kv_p, kv_s, status=status)
+    torch.cuda.synchronize()
+    ref_p, ref_s = oracle_cache(pages, x, slots)
+    assert_cache_equal(kv_p, kv_s, ref_p, ref_s)
+    assert int(status.item()) == 0
+    # query path on the same rows, as one query row of 16 heads
+    assert T == 16
+    xq = x.reshape(1, 16, 128)
+    qp = torch.empty((xq.shape[0], 16, 64), dtype=torch.uint8, device="cuda")
+    qs = torch.empty((xq.shape[0], 16, 4), dtype=torch.uint8, device="cuda")
+    fx.idx_fp4_quant_and_cache(bf16_dev(x[:0]), dev(np.zeros(0, np.int32)), kv_p, kv_s, q_bf16=bf16_dev(xq),
+                               q_packed=qp, q_scale=qs)
+    torch.cuda.synchronize()
+    rp, rs = oracle.quantize_plain(xq)
+    assert np.array_equal(qp.cpu().numpy(), rp)
+    assert np.array_equal(qs.cpu().numpy(), rs)
+
+
+def test_writer_flags_slot_past_pool():
+    x = synth.qk_bf16(synth.Rng(92), (3,))
+    kv_p, kv_s = new_cache(1)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fx.idx_fp4_quant_and_cache(bf16_dev(x), dev(np.array([5, 64, 1000], np.int32)), kv_p, kv_s, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & fx.DEV_BAD_SLOT
+    ref_p, ref_s = oracle_cache(1, x[:1], np.array([5], np.int32))
+    assert_cache_equal(kv_p, kv_s, ref_p, ref_s)
+
+
+@pytest.mark.parametrize("config", [1, 2])
+def test_decode_small_configs(config):
+    case = synth.decode_config(config)
+    run = DecodeRun(case).run()
+    ref = _oracle_side(case)
+    assert_cache_equal(run.kv_p, run.kv_s, ref[0], ref[1])
+    _check_decode(run, ref)
+
+
+@pytest.mark.parametrize("heads", [16, 32, 64, 128])
+def test_decode_heads_and_ragged_contexts(heads):
+    ctx = [1, 63, 64, 65, 127, 128, 129, 300, 0, 1000, 2047, 2048, 2049, 5000]
+    case = synth.decode_case(f"ragged_h{heads}", 100 + heads, ctx, heads, 2048 if heads != 16 else 64)
+    run = DecodeRun(case).run()
+    ref = _oracle_side(case)
+    _check_decode(run, ref)
+
+
+def test_decode_split_sequences_merge():
+    # Enough keys that every sequence spans several CTAs and the candidate merge runs; topk
+    # small and large relative to the per-CTA share.
+    ctx = [200000, 3, 150001, 64, 99999]
+    for k in (16, 2048):
+        case = synth.decode_case(f"split_k{k}", 7 + k, ctx, 64, k)
+        run = DecodeRun(case).run()
+        ref = _oracle_side(case)
+        _check_decode(run, ref)
+
+
+def test_decode_config3_full():
+    case = synth.decode_config(3)
+    run = DecodeRun(case).run()
+    ref = _oracle_side(case)
+    assert_cache_equal(run.kv_p, run.kv_s, ref[0], ref[1])
+    _check_decode(run, ref)
+
+
+@pytest.mark.parametrize("config", [4, 5])
+def test_decode_full_size_sampled(config):
+    """The long-context workloads at full size, in the benchmark's launch configuration: every
+    logit of two sequences and of sampled keys of all sequences, and the top-k of two sequences."""
+    case = synth.decode_config(config)
+    run = DecodeRun(case).run()
+    kv_p, kv_s, qp, qs = _oracle_side(case)
+    lg = run.logits.cpu().numpy()
+    rng = synth.Rng(1000 + config)
+    for b in range(case.batch):
+        c = int(case.ctx_lens[b])
+        t = np.unique(np.concatenate([rng.integers(0, c - 1, 64), [0, c - 1]]))
+        for t0 in t[:16]:
+            ref = oracle.row_logits(qp, qs, case.w, b, kv_p, kv_s, case.layout.block_tables[b], int(t0), int(t0) + 1)
+            assert_logits_close(lg[b, t0:t0 + 1], ref, f"seq {b} key {t0}")
+    _check_decode(run, (kv_p, kv_s, qp, qs), rows=[0, case.batch - 1], full_logits=True)
+
+
+def test_decode_without_debug_buffer_matches():
+    case = synth.decode_config(2)
+    a = DecodeRun(case).run()
+    b = DecodeRun(case, debug_logits=False).run()
+    assert torch.equal(a.topk_idx, b.topk_idx)
+    assert torch.equal(a.topk_val, b.topk_val)
+
+
+def test_decode_status_bad_page_and_ctx():
+    case = synth.decode_case("badpage", 5, [300, 200], 16, 64)
+    run = DecodeRun(case)
+    run.bt[1, 1] = case.layout.num_pages + 5  # a page id outside the pool
+    run.run()
+    assert int(run.status.item()) & fx.DEV_BAD_PAGE
+    run2 = DecodeRun(case, max_ctx=250)
+    run2.run()
+    assert int(run2.status.item()) & fx.DEV_BAD_CTX  # 300 > max_ctx: that sequence is treated as empty
+    assert np.all(run2.topk_idx.cpu().numpy()[0] == -1)
+
+
+def test_decode_schedule_mismatch_flagged():
+    case = synth.decode_case("mismatch", 6, [300, 200, 100], 16, 64)
+    run = DecodeRun(case)
+    run.schedule()
+    run.ctx = run.ctx[:2].contiguous()
+    run.q_packed = run.q_packed[:2].contiguous()
+    run.q_scale = run.q_scale[:2].contiguous()
+    run.w = run.w[:2].contiguous()
+    run.topk_idx = run.topk_idx[:2].contiguous()
+    run.topk_val = run.topk_val[:2].contiguous()
+    run.logits = run.logits[:2].contiguous()
+    run.score()
+    torch.cuda.synchronize()
+    assert int(run.status.item()) & fx.DEV_BAD_SCHEDULE
+
+
+def test_decode_schedule_invariants():
+    """Units of every sequence partition [0, ctx) exactly, each CTA's share is at most the
+    per-CTA tile count, and no CTA exists past the work."""
+    from fp4_sparse_attention_mxfp4_gb300 import _lib  # noqa: F401
+    ctx = np.array([131072, 5, 0, 70000, 128, 129, 1, 262144], np.int32)
+    t = dev(ctx)
+    sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(16), dtype=torch.uint8, device="cuda")
+    fx.idx_fp4_build_decode_schedule(t, 16, 262144, sched)
+    torch.cuda.synchronize()
+    s = sched.cpu().numpy().view(np.int32)
+    magic, ctas, batch, max_batch, num_units, total_tiles, per = s[:7]
+    assert batch == 8 and max_batch == 16
+    assert ctas == torch.cuda.get_device_properties(0).multi_processor_count
+    cta_first = s[8:8 + 1024]
+    cta_count = s[8 + 1024:8 + 2048]
+    off = 8 + 2048
+    seq_first, seq_units, seq_ctx = s[off:off + 16], s[off + 16:off + 32], s[off + 32:off + 48]
+    uoff = ((off + 48) * 4 + 31) // 32 * 32 // 4
+    units = s[uoff:uoff + 8 * num_units].reshape(num_units, 8)
+    assert total_tiles == sum(-(-int(c) // 128) for c in ctx)
+    assert np.array_equal(seq_ctx[:8], ctx)
+    covered = {b: [] for b in range(8)}
+    for c in range(ctas):
+        tiles = 0
+        for ui in range(cta_first[c], cta_first[c] + cta_count[c]):
+            row, table, kb, ke, nq, slot = units[ui][:6]
+            covered[row].append((kb, ke, ui))
+            tiles += -(-(ke - kb) // 128)
+            assert kb % 128 == 0 and nq == 1 and table == row
+            assert (slot == -1) == (seq_units[row] == 1)
+        assert tiles <= per
+    assert cta_first[ctas - 1] + cta_count[ctas - 1] == num_units
+    for b in range(8):
+        r = sorted(covered[b])
+        assert len(r) == seq_units[b]
+        if ctx[b] == 0:
+            assert r == []
+            continue
+        assert r[0][0] == 0 and r[-1][1] == ctx[b]
+        assert all(r[i][1] == r[i + 1][0] for i in range(len(r) - 1))
+        assert seq_first[b] == r[0][2]
+        assert [x[2] for x in r] == list(range(seq_first[b], seq_first[b] + seq_units[b]))
