@@ -11,6 +11,7 @@ asynchronously on the current (or given) stream:
 """
 from ._lib import (  # noqa: F401
     DEV_BAD_CTX,
+    DEV_CAPACITY,
     DEV_BAD_PAGE,
     DEV_BAD_ROWS,
     DEV_BAD_SCHEDULE,

@@ -28,6 +28,7 @@ DEV_BAD_CTX = 0x04
 DEV_BAD_ROWS = 0x08
 DEV_BAD_SCHEDULE = 0x10
 DEV_TIMEOUT = 0x20
+DEV_CAPACITY = 0x40
 
 _lock = threading.Lock()
 _lib = None
@@ -39,14 +40,14 @@ _SZ = ctypes.c_size_t
 
 SIGNATURES = {
     "idx_fp4_quant_and_cache": (_I32, [_P, _I64, _P, _P, _P, _I64, _P, _I64, _I32, _P, _P, _P, _P]),
-    "idx_fp4_decode_schedule_bytes": (_SZ, [_I32]),
+    "idx_fp4_decode_schedule_bytes": (_SZ, [_I32, _I64]),
     "idx_fp4_build_decode_schedule": (_I32, [_P, _I32, _I32, _I64, _P, _SZ, _P, _P]),
-    "idx_fp4_decode_workspace_bytes": (_SZ, [_I32, _I32]),
+    "idx_fp4_decode_workspace_bytes": (_SZ, [_I32, _I64, _I32]),
     "idx_fp4_decode_logits_topk": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _P, _SZ, _P,
                                           _SZ, _P, _P, _P, _I64, _P, _P]),
-    "idx_fp4_prefill_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
+    "idx_fp4_prefill_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I64, _I32]),
     "idx_fp4_prefill_logits_topk": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _P, _P, _I32, _I32, _I32, _I32,
-                                           _P, _SZ, _P, _P, _P, _I64, _P, _P]),
+                                           _I64, _P, _SZ, _P, _P, _P, _I64, _P, _P]),
     "idx_fp4_error_string": (ctypes.c_char_p, [_I32]),
 }
 
@@ -140,8 +141,8 @@ def idx_fp4_quant_and_cache(k_bf16, slot_mapping, kv_packed, kv_scale, q_bf16=No
     _check("idx_fp4_quant_and_cache", code)
 
 
-def idx_fp4_decode_schedule_bytes(max_batch: int) -> int:
-    return int(lib().idx_fp4_decode_schedule_bytes(int(max_batch)))
+def idx_fp4_decode_schedule_bytes(max_batch: int, max_ctx: int) -> int:
+    return int(lib().idx_fp4_decode_schedule_bytes(int(max_batch), int(max_ctx)))
 
 
 def idx_fp4_build_decode_schedule(ctx_lens, max_batch: int, max_ctx: int, sched, status=None, stream=None):
@@ -155,8 +156,8 @@ def idx_fp4_build_decode_schedule(ctx_lens, max_batch: int, max_ctx: int, sched,
     _check("idx_fp4_build_decode_schedule", code)
 
 
-def idx_fp4_decode_workspace_bytes(max_batch: int, topk: int) -> int:
-    return int(lib().idx_fp4_decode_workspace_bytes(int(max_batch), int(topk)))
+def idx_fp4_decode_workspace_bytes(max_batch: int, max_ctx: int, topk: int) -> int:
+    return int(lib().idx_fp4_decode_workspace_bytes(int(max_batch), int(max_ctx), int(topk)))
 
 
 def idx_fp4_decode_logits_topk(q_packed, q_scale, weights, kv_packed, kv_scale, block_tables, ctx_lens, topk: int,
@@ -196,14 +197,17 @@ def idx_fp4_decode_logits_topk(q_packed, q_scale, weights, kv_packed, kv_scale, 
     _check("idx_fp4_decode_logits_topk", code)
 
 
-def idx_fp4_prefill_workspace_bytes(num_requests: int, num_rows: int, num_heads: int) -> int:
-    return int(lib().idx_fp4_prefill_workspace_bytes(int(num_requests), int(num_rows), int(num_heads)))
+def idx_fp4_prefill_workspace_bytes(num_requests: int, num_rows: int, num_heads: int, max_ctx: int,
+                                    topk: int) -> int:
+    return int(lib().idx_fp4_prefill_workspace_bytes(int(num_requests), int(num_rows), int(num_heads), int(max_ctx),
+                                                     int(topk)))
 
 
 def idx_fp4_prefill_logits_topk(q_packed, q_scale, weights, kv_packed, kv_scale, block_tables, ctx_lens, cu_seqlens,
-                                row_ends, topk: int, workspace, topk_idx, topk_val=None, logits_debug=None,
-                                status=None, stream=None):
-    """Causal prefill scoring + top-k per row; padding rows (row_end 0) come out all -1."""
+                                row_ends, topk: int, max_ctx: int, workspace, topk_idx, topk_val=None,
+                                logits_debug=None, status=None, stream=None):
+    """Causal prefill scoring + top-k per row; padding rows (row_end 0) come out all -1. `max_ctx`
+    bounds every row end and is the value the workspace was sized with."""
     _need(q_packed, "q_packed", torch.uint8, 3)
     R, H = q_packed.shape[0], q_packed.shape[1]
     _need(q_scale, "q_scale", torch.uint8, 3)
@@ -235,6 +239,6 @@ def idx_fp4_prefill_logits_topk(q_packed, q_scale, weights, kv_packed, kv_scale,
     code = lib().idx_fp4_prefill_logits_topk(
         _ptr(q_packed), _ptr(q_scale), _ptr(weights), _ptr(kv_packed), _ptr(kv_scale), kv_packed.shape[0],
         _ptr(block_tables), block_tables.shape[1], _ptr(ctx_lens), _ptr(cu_seqlens), _ptr(row_ends), G, R, H,
-        int(topk), _ptr(workspace), workspace.numel(), _ptr(topk_idx), _ptr(topk_val), _ptr(logits_debug), stride,
+        int(topk), int(max_ctx), _ptr(workspace), workspace.numel(), _ptr(topk_idx), _ptr(topk_val), _ptr(logits_debug), stride,
         _ptr(status), _stream(stream))
     _check("idx_fp4_prefill_logits_topk", code)

@@ -14,29 +14,32 @@ cudaError_t launch_quant_and_cache(const uint16_t* k, int64_t num_tokens, const 
                                    uint8_t* q_packed, uint8_t* q_scale, int32_t* status, int num_sms,
                                    cudaStream_t stream);
 cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, int batch, int max_batch, int64_t max_ctx, int ctas,
-                                         int min_tiles, void* sched, int32_t* status, cudaStream_t stream);
+                                         int min_tiles, int64_t units_cap, void* sched, int32_t* status,
+                                         cudaStream_t stream);
 cudaError_t launch_build_prefill_schedule(const int32_t* cu_seqlens, const int32_t* row_ends, const int32_t* ctx_lens,
                                           int num_requests, int num_rows, int rows_per_unit, int table_width,
-                                          void* workspace, int32_t* status, cudaStream_t stream);
+                                          int64_t units_cap, int64_t slots_cap, void* workspace, int32_t* status,
+                                          cudaStream_t stream);
 cudaError_t launch_decode(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
                           const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
                           const int32_t* block_tables, int bt_stride, const int32_t* ctx_lens, int batch, int H,
-                          int topk, const void* sched, size_t sched_bytes, void* workspace, int slots,
+                          int topk, const void* sched, size_t sched_bytes, void* workspace, int64_t cand_slots,
                           int32_t* topk_idx, float* topk_val, float* logits_debug, int64_t logits_stride,
                           int32_t* status, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
                            const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
-                           const int32_t* block_tables, int bt_stride, const int32_t* row_ends, int H, int topk,
-                           void* workspace, int32_t* topk_idx, float* topk_val, float* logits_debug,
-                           int64_t logits_stride, int32_t* status, int grid, cudaStream_t stream);
-int max_batch_supported();
+                           const int32_t* block_tables, int bt_stride, const int32_t* row_ends, int num_rows, int H,
+                           int topk, void* workspace, int64_t units_cap, int64_t slots_cap, int32_t* topk_idx,
+                           float* topk_val, float* logits_debug, int64_t logits_stride, int32_t* status, int grid,
+                           cudaStream_t stream);
 }  // namespace idxfp4
 
 namespace {
 
 using namespace idxfp4;
 
-constexpr int kMinTilesPerCta = 8;  // a CTA's share is at least 1024 keys
+constexpr int kMinTilesPerCta = 8;      // a CTA's share is at least 1024 keys
+constexpr int64_t kMaxCtx = 1ll << 30;   // keys per sequence / row the sizing formulas accept
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool heads_ok(int h) { return h == 16 || h == 32 || h == 64 || h == 128; }
@@ -90,28 +93,29 @@ int idx_fp4_quant_and_cache(const uint16_t* k_bf16, int64_t num_tokens, const in
                                         q_vec, q_packed, q_scale, status_dev, sms, stream));
 }
 
-size_t idx_fp4_decode_schedule_bytes(int max_batch) {
-  if (max_batch < 1 || max_batch > max_batch_supported()) return 0;
-  return decode_sched_bytes(max_batch);
+size_t idx_fp4_decode_schedule_bytes(int max_batch, int64_t max_ctx) {
+  if (max_batch < 1 || max_batch > kMaxBatch || max_ctx < 0 || max_ctx > kMaxCtx) return 0;
+  return decode_sched_bytes_for(max_batch, decode_units_cap(max_batch, max_ctx));
 }
 
 int idx_fp4_build_decode_schedule(const int32_t* ctx_lens_dev, int batch, int max_batch, int64_t max_ctx,
                                   void* sched_dev, size_t sched_bytes, int32_t* status_dev, cudaStream_t stream) {
-  if (max_batch < 1 || max_batch > max_batch_supported() || batch < 0 || batch > max_batch || max_ctx < 0)
+  if (max_batch < 1 || max_batch > kMaxBatch || batch < 0 || batch > max_batch || max_ctx < 0 || max_ctx > kMaxCtx)
     return IDX_FP4_ERR_ARG;
   if (sched_dev == nullptr || !aligned16(sched_dev) || (batch > 0 && ctx_lens_dev == nullptr)) return IDX_FP4_ERR_ARG;
-  if (sched_bytes < decode_sched_bytes(max_batch)) return IDX_FP4_ERR_CAPACITY;
+  const int64_t units_cap = decode_units_cap(max_batch, max_ctx);
+  if (sched_bytes < decode_sched_bytes_for(max_batch, units_cap)) return IDX_FP4_ERR_CAPACITY;
   const int ctas = device_ctas();
   if (ctas <= 0) return IDX_FP4_ERR_CUDA;
   return to_code(launch_build_decode_schedule(ctx_lens_dev, batch, max_batch, max_ctx, ctas, kMinTilesPerCta,
-                                              sched_dev, status_dev, stream));
+                                              units_cap, sched_dev, status_dev, stream));
 }
 
-size_t idx_fp4_decode_workspace_bytes(int max_batch, int topk) {
-  if (max_batch < 1 || max_batch > max_batch_supported() || topk < 1 || topk > IDX_FP4_MAX_TOPK) return 0;
-  const int ctas = device_ctas();
-  if (ctas <= 0) return 0;
-  return decode_workspace_bytes_for(ctas + max_batch, topk);
+size_t idx_fp4_decode_workspace_bytes(int max_batch, int64_t max_ctx, int topk) {
+  if (max_batch < 1 || max_batch > kMaxBatch || max_ctx < 0 || max_ctx > kMaxCtx || topk < 1 ||
+      topk > IDX_FP4_MAX_TOPK)
+    return 0;
+  return decode_workspace_bytes_for(decode_units_cap(max_batch, max_ctx), topk);
 }
 
 int idx_fp4_decode_logits_topk(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
@@ -122,7 +126,7 @@ int idx_fp4_decode_logits_topk(const uint8_t* q_packed, const uint8_t* q_scale, 
                                float* logits_debug, int64_t logits_stride, int32_t* status_dev,
                                cudaStream_t stream) {
   if (!heads_ok(num_heads) || topk < 1 || topk > IDX_FP4_MAX_TOPK) return IDX_FP4_ERR_SHAPE;
-  if (batch < 0 || batch > max_batch_supported()) return IDX_FP4_ERR_ARG;
+  if (batch < 0 || batch > kMaxBatch) return IDX_FP4_ERR_ARG;
   if (batch == 0) return IDX_FP4_OK;
   if (q_packed == nullptr || q_scale == nullptr || weights == nullptr || kv_packed == nullptr ||
       kv_scale == nullptr || block_tables == nullptr || ctx_lens_dev == nullptr || sched_dev == nullptr ||
@@ -133,30 +137,34 @@ int idx_fp4_decode_logits_topk(const uint8_t* q_packed, const uint8_t* q_scale, 
   if (!aligned16(q_packed) || !aligned16(q_scale) || !aligned16(weights) || !aligned16(kv_packed) ||
       !aligned16(kv_scale) || !aligned16(sched_dev) || !aligned16(workspace))
     return IDX_FP4_ERR_ARG;
+  if (sched_bytes < decode_sched_bytes_for(batch, 0)) return IDX_FP4_ERR_CAPACITY;
+  const int64_t cand_slots = static_cast<int64_t>(workspace_bytes / (sizeof(uint2) * cand_slot_entries(topk)));
   const int ctas = device_ctas();
   if (ctas <= 0) return IDX_FP4_ERR_CUDA;
-  const int slots = ctas + batch;
-  if (workspace_bytes < decode_workspace_bytes_for(slots, topk)) return IDX_FP4_ERR_CAPACITY;
   return to_code(launch_decode(q_packed, q_scale, weights, kv_packed, kv_scale, num_pages, block_tables,
                                block_table_stride, ctx_lens_dev, batch, num_heads, topk, sched_dev, sched_bytes,
-                               workspace, slots, topk_idx, topk_val, logits_debug, logits_stride, status_dev, ctas,
-                               stream));
+                               workspace, cand_slots, topk_idx, topk_val, logits_debug, logits_stride, status_dev,
+                               ctas, stream));
 }
 
-size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_heads) {
-  if (num_requests < 1 || num_requests > max_batch_supported() || num_rows < 0 || !heads_ok(num_heads)) return 0;
-  return prefill_workspace_bytes_for(num_requests, num_rows, prefill_rows_per_unit(num_heads));
+size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_heads, int64_t max_ctx, int topk) {
+  if (num_requests < 1 || num_requests > kMaxBatch || num_rows < 0 || num_rows > kMaxPrefillRows ||
+      !heads_ok(num_heads) || max_ctx < 0 || max_ctx > kMaxCtx || topk < 1 || topk > IDX_FP4_MAX_TOPK)
+    return 0;
+  return prefill_workspace_bytes_for(num_requests, num_rows, prefill_rows_per_unit(num_heads), max_ctx, topk);
 }
 
 int idx_fp4_prefill_logits_topk(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
                                 const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
                                 const int32_t* block_tables, int block_table_stride, const int32_t* ctx_lens_dev,
                                 const int32_t* cu_seqlens_dev, const int32_t* row_ends_dev, int num_requests,
-                                int num_rows, int num_heads, int topk, void* workspace, size_t workspace_bytes,
-                                int32_t* topk_idx, float* topk_val, float* logits_debug, int64_t logits_stride,
-                                int32_t* status_dev, cudaStream_t stream) {
+                                int num_rows, int num_heads, int topk, int64_t max_ctx, void* workspace,
+                                size_t workspace_bytes, int32_t* topk_idx, float* topk_val, float* logits_debug,
+                                int64_t logits_stride, int32_t* status_dev, cudaStream_t stream) {
   if (!heads_ok(num_heads) || topk < 1 || topk > IDX_FP4_MAX_TOPK) return IDX_FP4_ERR_SHAPE;
-  if (num_rows < 0 || num_requests < 0 || num_requests > max_batch_supported()) return IDX_FP4_ERR_ARG;
+  if (num_rows < 0 || num_rows > kMaxPrefillRows || num_requests < 0 || num_requests > kMaxBatch || max_ctx < 0 ||
+      max_ctx > kMaxCtx)
+    return IDX_FP4_ERR_ARG;
   if (num_rows == 0) return IDX_FP4_OK;
   if (num_requests < 1) return IDX_FP4_ERR_ARG;
   if (q_packed == nullptr || q_scale == nullptr || weights == nullptr || kv_packed == nullptr ||
@@ -169,17 +177,20 @@ int idx_fp4_prefill_logits_topk(const uint8_t* q_packed, const uint8_t* q_scale,
       !aligned16(kv_scale) || !aligned16(workspace))
     return IDX_FP4_ERR_ARG;
   const int q_rows = prefill_rows_per_unit(num_heads);
-  if (workspace_bytes < prefill_workspace_bytes_for(num_requests, num_rows, q_rows)) return IDX_FP4_ERR_CAPACITY;
+  if (workspace_bytes < prefill_workspace_bytes_for(num_requests, num_rows, q_rows, max_ctx, topk))
+    return IDX_FP4_ERR_CAPACITY;
+  const int64_t units_cap = prefill_units_cap(num_requests, num_rows, q_rows, max_ctx);
+  const int64_t slots_cap = max_ctx > unit_key_cap(q_rows) ? units_cap * q_rows : 0;
   const int ctas = device_ctas();
   if (ctas <= 0) return IDX_FP4_ERR_CUDA;
-  const int max_units = prefill_max_units(num_requests, num_rows, q_rows);
-  const int grid = max_units < ctas ? max_units : ctas;
+  const int grid = static_cast<int>(units_cap < ctas ? units_cap : ctas);
   cudaError_t e = launch_build_prefill_schedule(cu_seqlens_dev, row_ends_dev, ctx_lens_dev, num_requests, num_rows,
-                                                q_rows, block_table_stride, workspace, status_dev, stream);
+                                                q_rows, block_table_stride, units_cap, slots_cap, workspace,
+                                                status_dev, stream);
   if (e != cudaSuccess) return IDX_FP4_ERR_CUDA;
   return to_code(launch_prefill(q_packed, q_scale, weights, kv_packed, kv_scale, num_pages, block_tables,
-                                block_table_stride, row_ends_dev, num_heads, topk, workspace, topk_idx, topk_val,
-                                logits_debug, logits_stride, status_dev, grid, stream));
+                                block_table_stride, row_ends_dev, num_rows, num_heads, topk, workspace, units_cap,
+                                slots_cap, topk_idx, topk_val, logits_debug, logits_stride, status_dev, grid, stream));
 }
 
 }  // extern "C"

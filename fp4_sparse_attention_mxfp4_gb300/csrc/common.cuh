@@ -15,33 +15,42 @@ constexpr int kPageBytes = kGroups * kPage * 16;   // packed plane: [group][row]
 constexpr int kPageScaleBytes = kGroups * kPage;   // scale plane: [group][swizzled row] = 256
 constexpr int kTileKeys = 128;                     // keys per MMA tile (M = 128, two pages)
 constexpr int kMaxTopk = IDX_FP4_MAX_TOPK;
-constexpr int kCandCap = 2 * kMaxTopk + 256;       // per-row candidate buffer (entries)
 constexpr int kMaxCtas = 1024;                     // upper bound on the persistent grid
+constexpr int kMaxBatch = 4096;                    // sequences (decode) / requests (prefill) per call
+constexpr int kMaxPrefillRows = 8192;              // query rows per prefill call
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: a bound, never reached in normal runs
+
+// Keys one unit scores per query row: the unit's logits live in shared memory (4 B per key and
+// row). Decode units carry one row, prefill units up to two.
+__host__ __device__ constexpr int unit_key_cap(int rows) { return rows == 1 ? 16384 : 8192; }
 
 // Row permutation of the scale plane inside a page: the 64 rows viewed as 4 x 16 and
 // transposed ("Use the index scale plane's own row order when staging FP4 prefill under DCP").
 __host__ __device__ constexpr int scale_slot(int row) { return (row % 16) * 4 + row / 16; }
 
 // One unit of scorer work: `nq` query rows sharing one page table, scored against keys
-// [kb, ke). kb is a multiple of kTileKeys.
+// [kb, ke). kb is a multiple of kTileKeys and ke - kb <= unit_key_cap(rows per unit).
 struct Unit {
   int32_t row;    // first query row (decode: the sequence)
   int32_t table;  // row of block_tables
   int32_t kb, ke;
   int32_t nq;
   int32_t slot;   // -1: this unit covers its rows fully and writes the final top-k;
-                  // >= 0: candidate slot in the decode workspace (merged afterwards)
+                  // >= 0: candidate slot of its first row (row r uses slot + r), merged afterwards
   int32_t pad0, pad1;
 };
 static_assert(sizeof(Unit) == 32, "Unit is 32 bytes");
 
-constexpr uint32_t kDecodeMagic = 0x44534331u;   // "DSC1"
-constexpr uint32_t kPrefillMagic = 0x50465331u;  // "PFS1"
+constexpr uint32_t kDecodeMagic = 0x44534332u;   // "DSC2"
+constexpr uint32_t kPrefillMagic = 0x50465332u;  // "PFS2"
+
+__host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Decode schedule, at a fixed address the caller owns (CUDA-graph stable):
-//   header | cta_first[kMaxCtas] | cta_count[kMaxCtas] | seq_first[max_batch] |
-//   seq_units[max_batch] | seq_ctx[max_batch] | (pad to 32) | units[kMaxCtas + max_batch]
+//   header | cta_first[kMaxCtas] | cta_count[kMaxCtas] | seq_first[max_batch] | seq_units[max_batch] |
+//   seq_ctx[max_batch] | (pad to 32) | units[units_cap]
+// Units are stored in token order, so a sequence's units (and candidate slots) are consecutive
+// and so are each CTA's.
 struct DecodeSchedHeader {
   uint32_t magic;
   int32_t ctas;         // persistent grid the schedule was built for
@@ -49,8 +58,8 @@ struct DecodeSchedHeader {
   int32_t max_batch;
   int32_t num_units;
   int32_t total_tiles;
-  int32_t tiles_per_cta;
-  int32_t reserved;
+  int32_t tiles_per_range;
+  int32_t units_cap;
 };
 
 struct DecodeSchedView {
@@ -63,12 +72,20 @@ struct DecodeSchedView {
   Unit* units;
 };
 
-__host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+// Units a decode schedule can hold: tile ranges of at most unit_key_cap(1) keys (their number a
+// multiple of the grid), plus one more unit per sequence boundary inside a range.
+__host__ __device__ inline int64_t decode_units_cap(int max_batch, int64_t max_ctx) {
+  const int64_t tiles = static_cast<int64_t>(max_batch) * ((max_ctx + kTileKeys - 1) / kTileKeys);
+  const int64_t per = unit_key_cap(1) / kTileKeys;
+  return (tiles + per - 1) / per + kMaxCtas + max_batch;
+}
 
-__host__ __device__ inline size_t decode_sched_bytes(int max_batch) {
-  size_t b = sizeof(DecodeSchedHeader) + 2 * sizeof(int32_t) * kMaxCtas + 3 * sizeof(int32_t) * max_batch;
-  b = round_up(b, 32);
-  return b + sizeof(Unit) * (kMaxCtas + static_cast<size_t>(max_batch));
+__host__ __device__ inline size_t decode_units_offset(int max_batch) {
+  return round_up(sizeof(DecodeSchedHeader) + 2 * sizeof(int32_t) * kMaxCtas + 3 * sizeof(int32_t) * max_batch, 32);
+}
+
+__host__ __device__ inline size_t decode_sched_bytes_for(int max_batch, int64_t units_cap) {
+  return decode_units_offset(max_batch) + sizeof(Unit) * static_cast<size_t>(units_cap);
 }
 
 __host__ __device__ inline DecodeSchedView decode_sched_view(void* base, int max_batch) {
@@ -85,38 +102,64 @@ __host__ __device__ inline DecodeSchedView decode_sched_view(void* base, int max
   v.seq_units = reinterpret_cast<int32_t*>(p);
   p += sizeof(int32_t) * max_batch;
   v.seq_ctx = reinterpret_cast<int32_t*>(p);
-  size_t off = round_up(sizeof(DecodeSchedHeader) + 2 * sizeof(int32_t) * kMaxCtas + 3 * sizeof(int32_t) * max_batch,
-                        32);
-  v.units = reinterpret_cast<Unit*>(static_cast<char*>(base) + off);
+  v.units = reinterpret_cast<Unit*>(static_cast<char*>(base) + decode_units_offset(max_batch));
   return v;
 }
 
-// Decode workspace: candidates of split sequences, one slot per unit:
-//   cand_count[slots] (padded to 16 B) | cand[slots][topk] as (ordered key, token index)
-__host__ __device__ inline size_t decode_workspace_bytes_for(int slots, int topk) {
-  return round_up(sizeof(int32_t) * slots, 16) + sizeof(uint2) * static_cast<size_t>(slots) * topk;
+// Candidate slots (decode units of split sequences, prefill rows split into key chunks): slot s
+// is a 16-byte header whose first word is the entry count, then up to k (ordered key, token
+// index) entries in token order; an odd count is followed by one (0, -1) pad entry so each list
+// is a whole number of 16-byte pairs. Key 0 is below every logit's key and never selected.
+__host__ __device__ inline size_t cand_slot_entries(int topk) { return round_up(static_cast<size_t>(topk) + 2, 2); }
+
+__host__ __device__ inline size_t decode_workspace_bytes_for(int64_t units_cap, int topk) {
+  return sizeof(uint2) * cand_slot_entries(topk) * static_cast<size_t>(units_cap);
 }
 
-// Prefill workspace: header + unit table.
+// Prefill workspace: header | row_merge[num_rows] (first slot, number of lists, clamped row end,
+// 0) | (pad to 32) | units[units_cap] | candidate slots[slots_cap]. Row r of a split row group has
+// its lists at slots first, first + rows_per_unit, ...; an unsplit row has count 1 and is written
+// directly by the scorer.
 struct PrefillSchedHeader {
   uint32_t magic;
   int32_t num_units;
   int32_t rows_per_unit;
-  int32_t reserved[5];
+  int32_t units_cap;
+  int32_t num_rows;
+  int32_t slots_cap;
+  int32_t reserved[2];
 };
 
-__host__ __device__ inline int prefill_max_units(int num_requests, int num_rows, int rows_per_unit) {
-  return (num_rows + rows_per_unit - 1) / rows_per_unit + num_requests;
-}
-
-__host__ __device__ inline size_t prefill_workspace_bytes_for(int num_requests, int num_rows, int rows_per_unit) {
-  return sizeof(PrefillSchedHeader) + sizeof(Unit) * static_cast<size_t>(prefill_max_units(num_requests, num_rows,
-                                                                                             rows_per_unit));
-}
-
-// Query rows per prefill unit: the MMA N dimension is rows * heads, kept <= 128; each row
-// also needs its own candidate buffer in shared memory, which caps the count at 2.
+// Query rows per prefill unit: the MMA N dimension is rows * heads, kept <= 128; each row also
+// needs its own logit buffer in shared memory, which caps the count at 2.
 __host__ __device__ inline int prefill_rows_per_unit(int heads) { return heads <= 64 ? 2 : 1; }
+
+// Units of a prefill call: one per row group of each request, times the key chunks a row of up
+// to max_ctx keys needs.
+__host__ __device__ inline int64_t prefill_units_cap(int num_requests, int num_rows, int rows_per_unit,
+                                                     int64_t max_ctx) {
+  const int64_t groups = (num_rows + rows_per_unit - 1) / rows_per_unit + num_requests;
+  const int64_t cap = unit_key_cap(rows_per_unit);
+  const int64_t chunks = max_ctx > cap ? (max_ctx + cap - 1) / cap : 1;
+  return groups * chunks;
+}
+
+__host__ __device__ inline size_t prefill_units_offset(int num_rows) {
+  return round_up(sizeof(PrefillSchedHeader) + sizeof(int4) * static_cast<size_t>(num_rows), 32);
+}
+
+__host__ __device__ inline size_t prefill_slots_offset(int num_rows, int64_t units_cap) {
+  return round_up(prefill_units_offset(num_rows) + sizeof(Unit) * static_cast<size_t>(units_cap), 16);
+}
+
+// Candidate slots are only needed by units of split rows; sized for every unit and row.
+__host__ __device__ inline size_t prefill_workspace_bytes_for(int num_requests, int num_rows, int rows_per_unit,
+                                                               int64_t max_ctx, int topk) {
+  const int64_t units = prefill_units_cap(num_requests, num_rows, rows_per_unit, max_ctx);
+  const int64_t cap = unit_key_cap(rows_per_unit);
+  const int64_t slots = max_ctx > cap ? units * rows_per_unit : 0;
+  return prefill_slots_offset(num_rows, units) + sizeof(uint2) * cand_slot_entries(topk) * static_cast<size_t>(slots);
+}
 
 // Order-preserving map fp32 -> uint32 (a larger float maps to a larger integer). Adding
 // +0.0f first folds -0 into +0 so that equal values compare equal.

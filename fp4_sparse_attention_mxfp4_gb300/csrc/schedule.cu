@@ -4,16 +4,18 @@
 // grid floor": a persistent-grid CTA schedule built once per step at a CUDA-graph-stable
 // address, so a captured graph replays across changing context lengths; a schedule that
 // under-covers rows is an error, never silent). The pages size their grid with a fixed floor
-// (512 decode / 4096 prefill CTAs) and measure the cost of CTAs past the work. Here the grid
-// is the SM count and the work is cut to it: all sequences' 128-key tiles are laid end to end
-// and each CTA takes one contiguous, equal share, split at sequence boundaries into units.
-// A sequence spread over several units is merged from per-unit candidates afterwards.
+// (512 decode / 4096 prefill CTAs) and measure the cost of CTAs past the work. Here the grid is
+// the SM count and the work is cut to it: all sequences' 128-key tiles are laid end to end,
+// cut into ranges of at most unit_key_cap(1) keys whose number is a multiple of the grid, and
+// each CTA takes an equal block of consecutive ranges. Ranges split at sequence boundaries
+// into units. A sequence spread over several units is merged from per-unit candidates.
 //
 // Prefill ("Score a DSA sparse indexer in FP4": the prefill scorer finds a row's page table
 // through its group and takes per-row key bounds): rows of one request are grouped by
-// `rows_per_unit`; a group scores keys [0, max row end) once and masks per row. Groups are
-// listed per request from the last (longest) to the first so that a round-robin over CTAs
-// starts the longest work first.
+// `rows_per_unit`; a group scores keys [0, max row end) once and masks per row. A group whose
+// rows reach past unit_key_cap keys is cut into key chunks whose per-row candidates are merged.
+// Groups are listed per request from the last (longest) to the first, so a round-robin over
+// CTAs starts the longest work first.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -24,7 +26,7 @@ namespace idxfp4 {
 namespace {
 
 constexpr int kSchedThreads = 1024;
-constexpr int kMaxBatchSched = 4096;
+constexpr int kPer = kMaxBatch / kSchedThreads;  // sequences (requests) per thread in the scans
 
 // Exclusive scan of v over the block (kSchedThreads threads, one value each); returns the
 // exclusive prefix and writes the total to *total (shared).
@@ -39,7 +41,7 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   if (lane == 31) warp_sums[w] = incl;
   __syncthreads();
   if (w == 0) {
-    int s = lane < (kSchedThreads / 32) ? warp_sums[lane] : 0;
+    const int s = lane < (kSchedThreads / 32) ? warp_sums[lane] : 0;
     int si = s;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -58,15 +60,14 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 __global__ void __launch_bounds__(kSchedThreads) build_decode_schedule_kernel(const int32_t* __restrict__ ctx_lens,
                                                                               int batch, int max_batch,
                                                                               int64_t max_ctx, int ctas,
-                                                                              int min_tiles, void* sched,
-                                                                              int32_t* status) {
-  __shared__ int s_start[kMaxBatchSched + 1];  // exclusive prefix of tiles per sequence
-  __shared__ int s_ne[kMaxBatchSched + 1];     // exclusive prefix of non-empty sequences
+                                                                              int min_tiles, int64_t units_cap,
+                                                                              void* sched, int32_t* status) {
+  __shared__ int s_start[kMaxBatch + 1];  // exclusive prefix of tiles per sequence
+  __shared__ int s_ne[kMaxBatch + 1];     // exclusive prefix of non-empty sequences
   __shared__ int warp_sums[32];
   __shared__ int s_total, s_total_ne, s_scan;
   DecodeSchedView v = decode_sched_view(sched, max_batch);
   const int tid = threadIdx.x;
-  constexpr int kPer = kMaxBatchSched / kSchedThreads;  // sequences per thread in the scans
 
   // 1. tiles per sequence and their prefix sums
   int tiles[kPer], nonempty[kPer];
@@ -100,22 +101,27 @@ __global__ void __launch_bounds__(kSchedThreads) build_decode_schedule_kernel(co
     off_ne += nonempty[j];
   }
   if (tid == 0) {
-    s_start[kMaxBatchSched] = s_total;
-    s_ne[kMaxBatchSched] = s_total_ne;
+    s_start[kMaxBatch] = s_total;
+    s_ne[kMaxBatch] = s_total_ne;
   }
   __syncthreads();
   const int total = s_total;
-  int per = (total + ctas - 1) / ctas;
-  if (per < min_tiles) per = min_tiles;
-  if (per < 1) per = 1;
 
-  // 2. units per sequence (closed form) and per CTA
+  // 2. ranges: `m` per CTA, `per` tiles each (at most a unit's key cap)
+  const int cap_tiles = unit_key_cap(1) / kTileKeys;
+  const int64_t slab = static_cast<int64_t>(ctas) * cap_tiles;
+  const int m = total > 0 ? static_cast<int>((total + slab - 1) / slab) : 1;
+  int per = static_cast<int>((static_cast<int64_t>(total) + static_cast<int64_t>(ctas) * m - 1) /
+                             (static_cast<int64_t>(ctas) * m));
+  if (m == 1 && per < min_tiles) per = min_tiles;
+  if (per > cap_tiles) per = cap_tiles;
+  if (per < 1) per = 1;
   for (int b = tid; b < batch; b += kSchedThreads) {
     const int t = s_start[b + 1] - s_start[b];
     v.seq_units[b] = t > 0 ? ((s_start[b] + t - 1) / per - s_start[b] / per + 1) : 0;
     v.seq_first[b] = -1;
   }
-  // seq containing tile x: the last b with start[b] <= x (never an empty sequence)
+  // the sequence containing tile x: the last b with start[b] <= x (never an empty one)
   auto seq_of = [&](int x) {
     int lo = 0, hi = batch - 1;
     while (lo < hi) {
@@ -124,42 +130,56 @@ __global__ void __launch_bounds__(kSchedThreads) build_decode_schedule_kernel(co
     }
     return lo;
   };
-  int my_count = 0, b0 = 0, b1 = -1, lo_t = 0, hi_t = 0;
+  // 3. units per CTA
+  const int64_t cta_lo = static_cast<int64_t>(tid) * m * per;
+  int my_count = 0;
   if (tid < ctas) {
-    lo_t = tid * per;
-    hi_t = min(lo_t + per, total);
-    if (lo_t < hi_t) {
-      b0 = seq_of(lo_t);
-      b1 = seq_of(hi_t - 1);
-      my_count = s_ne[b1 + 1] - s_ne[b0];
+    for (int r = 0; r < m; ++r) {
+      const int64_t lo = cta_lo + static_cast<int64_t>(r) * per;
+      if (lo >= total) break;
+      const int hi = static_cast<int>(lo + per < total ? lo + per : total);
+      my_count += s_ne[seq_of(hi - 1) + 1] - s_ne[seq_of(static_cast<int>(lo))];
     }
   }
   __syncthreads();
   const int first = block_exclusive_scan(tid < ctas ? my_count : 0, warp_sums, &s_scan);
+  const bool fits = s_scan <= units_cap;
   if (tid < ctas) {
     v.cta_first[tid] = first;
-    v.cta_count[tid] = my_count;
+    v.cta_count[tid] = fits ? my_count : 0;
   }
   __syncthreads();
-  // 3. emit units
-  if (tid < ctas && my_count > 0) {
+  // 4. emit units in token order
+  if (fits && tid < ctas && my_count > 0) {
     int idx = first;
-    for (int b = b0; b <= b1; ++b) {
-      const int sb = s_start[b], tb = s_start[b + 1] - sb;
-      if (tb == 0) continue;
-      const int ulo = max(lo_t, sb), uhi = min(hi_t, sb + tb);
-      Unit u;
-      u.row = b;
-      u.table = b;
-      u.kb = (ulo - sb) * kTileKeys;
-      u.ke = min((uhi - sb) * kTileKeys, v.seq_ctx[b]);
-      u.nq = 1;
-      u.slot = v.seq_units[b] == 1 ? -1 : idx;
-      u.pad0 = u.pad1 = 0;
-      v.units[idx] = u;
-      if (ulo == sb) v.seq_first[b] = idx;
-      ++idx;
+    for (int r = 0; r < m; ++r) {
+      const int64_t lo64 = cta_lo + static_cast<int64_t>(r) * per;
+      if (lo64 >= total) break;
+      const int lo = static_cast<int>(lo64);
+      const int hi = lo + per < total ? lo + per : total;
+      const int b0 = seq_of(lo), b1 = seq_of(hi - 1);
+      for (int b = b0; b <= b1; ++b) {
+        const int sb = s_start[b], tb = s_start[b + 1] - sb;
+        if (tb == 0) continue;
+        const int ulo = max(lo, sb), uhi = min(hi, sb + tb);
+        Unit u;
+        u.row = b;
+        u.table = b;
+        u.kb = (ulo - sb) * kTileKeys;
+        u.ke = min((uhi - sb) * kTileKeys, v.seq_ctx[b]);
+        u.nq = 1;
+        u.slot = v.seq_units[b] == 1 ? -1 : idx;
+        u.pad0 = u.pad1 = 0;
+        v.units[idx] = u;
+        if (ulo == sb) v.seq_first[b] = idx;
+        ++idx;
+      }
     }
+  }
+  if (!fits) {
+    // cannot happen when the buffer was sized for (max_batch, max_ctx); report, schedule nothing
+    for (int b = tid; b < batch; b += kSchedThreads) v.seq_units[b] = 0;
+    if (tid == 0) set_status(status, IDX_FP4_DEV_CAPACITY);
   }
   if (tid == 0) {
     DecodeSchedHeader h;
@@ -167,36 +187,41 @@ __global__ void __launch_bounds__(kSchedThreads) build_decode_schedule_kernel(co
     h.ctas = ctas;
     h.batch = batch;
     h.max_batch = max_batch;
-    h.num_units = s_scan;
+    h.num_units = fits ? s_scan : 0;
     h.total_tiles = total;
-    h.tiles_per_cta = per;
-    h.reserved = 0;
+    h.tiles_per_range = per;
+    h.units_cap = static_cast<int32_t>(units_cap);
     *v.hdr = h;
   }
 }
 
+constexpr int kMaxPrefillGroups = kMaxPrefillRows + kMaxBatch;
+
 __global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ row_ends,
     const int32_t* __restrict__ ctx_lens, int num_requests, int num_rows, int rows_per_unit, int table_width,
-    void* workspace, int32_t* status) {
+    int64_t units_cap, int64_t slots_cap, void* workspace, int32_t* status) {
+  extern __shared__ int s_dyn[];
+  int* s_off = s_dyn;                   // [kMaxBatch + 1] groups before each request
+  int* s_n = s_dyn + kMaxBatch + 1;     // [kMaxPrefillGroups] chunks per group, then unit offsets
   __shared__ int warp_sums[32];
-  __shared__ int s_total, s_bad;
-  __shared__ int s_off[kMaxBatchSched + 1];
+  __shared__ int s_total, s_bad, s_units;
   const int tid = threadIdx.x;
   PrefillSchedHeader* hdr = static_cast<PrefillSchedHeader*>(workspace);
-  Unit* units = reinterpret_cast<Unit*>(hdr + 1);
+  int4* row_merge = reinterpret_cast<int4*>(hdr + 1);
+  Unit* units = reinterpret_cast<Unit*>(static_cast<char*>(workspace) + prefill_units_offset(num_rows));
   const int Q = rows_per_unit;
+  const int cap = unit_key_cap(Q);
   if (tid == 0) s_bad = 0;
   __syncthreads();
-  // validate cu_seqlens
   for (int g = tid; g < num_requests; g += kSchedThreads) {
     const int a = cu_seqlens[g], b = cu_seqlens[g + 1];
     if (a > b || (g == 0 && a != 0) || (g == num_requests - 1 && b != num_rows)) s_bad = 1;
   }
   __syncthreads();
   if (s_bad) {
-    // Rows cannot be mapped to requests: emit empty units over all rows so every row's
-    // output is written as "no key", and flag the call.
+    // Rows cannot be mapped to requests: emit empty units over all rows so every row's output is
+    // written as "no key", and flag the call.
     if (tid == 0) set_status(status, IDX_FP4_DEV_BAD_ROWS);
     const int n = (num_rows + Q - 1) / Q;
     for (int j = tid; j < n; j += kSchedThreads) {
@@ -210,17 +235,20 @@ __global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
       u.pad0 = u.pad1 = 0;
       units[j] = u;
     }
+    for (int r = tid; r < num_rows; r += kSchedThreads) row_merge[r] = make_int4(-1, 1, 0, 0);
     if (tid == 0) {
       PrefillSchedHeader h{};
       h.magic = kPrefillMagic;
       h.num_units = n;
       h.rows_per_unit = Q;
+      h.units_cap = static_cast<int32_t>(units_cap);
+      h.num_rows = num_rows;
+      h.slots_cap = static_cast<int32_t>(slots_cap);
       *hdr = h;
     }
     return;
   }
-  // groups per request and their offsets (requests handled kPer per thread)
-  constexpr int kPer = kMaxBatchSched / kSchedThreads;
+  // groups per request
   int cnt[kPer], my = 0;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
@@ -235,46 +263,87 @@ __global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
     off += cnt[j];
   }
   __syncthreads();
-  const int total = s_total;
-  for (int idx = tid; idx < total; idx += kSchedThreads) {
-    // request of unit idx: last g with s_off[g] <= idx and a non-zero count
+  const int ngroups = s_total;
+  // group idx -> request, first row, rows, and the clamped key end of its longest row
+  auto group_info = [&](int idx, int& g, int& r0, int& nq, int& kcap) {
     int lo = 0, hi = num_requests - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (s_off[mid] <= idx) lo = mid; else hi = mid - 1;
     }
-    const int g = lo;
+    g = lo;
     const int ng = (cu_seqlens[g + 1] - cu_seqlens[g] + Q - 1) / Q;
     const int j = ng - 1 - (idx - s_off[g]);  // last group first
-    const int r0 = cu_seqlens[g] + j * Q;
-    const int nq = min(Q, cu_seqlens[g + 1] - r0);
-    const int cap = min(ctx_lens[g], table_width * kPage);
-    if (ctx_lens[g] < 0) set_status(status, IDX_FP4_DEV_BAD_CTX);
-    if (ctx_lens[g] > table_width * kPage) set_status(status, IDX_FP4_DEV_BAD_CTX);
+    r0 = cu_seqlens[g] + j * Q;
+    nq = min(Q, cu_seqlens[g + 1] - r0);
+    kcap = min(max(ctx_lens[g], 0), table_width * kPage);
+  };
+  // pass 1: key chunks per group
+  for (int idx = tid; idx < ngroups; idx += kSchedThreads) {
+    int g, r0, nq, kcap;
+    group_info(idx, g, r0, nq, kcap);
+    if (ctx_lens[g] < 0 || ctx_lens[g] > table_width * kPage) set_status(status, IDX_FP4_DEV_BAD_CTX);
     int ke = 0;
     for (int i = 0; i < nq; ++i) {
       int e = row_ends[r0 + i];
-      if (e < 0 || e > cap) {
+      if (e < 0 || e > kcap) {
         set_status(status, IDX_FP4_DEV_BAD_ROWS);
-        e = e < 0 ? 0 : cap;
+        e = e < 0 ? 0 : kcap;
       }
       ke = max(ke, e);
     }
-    Unit u;
-    u.row = r0;
-    u.table = g;
-    u.kb = 0;
-    u.ke = max(ke, 0);
-    u.nq = nq;
-    u.slot = -1;
-    u.pad0 = u.pad1 = 0;
-    units[idx] = u;
+    s_n[idx] = ke > cap ? (ke + cap - 1) / cap : 1;
+  }
+  __syncthreads();
+  // pass 2: unit offsets (exclusive scan of the chunk counts, in blocks of the thread count)
+  int running = 0;
+  for (int base = 0; base < ngroups; base += kSchedThreads) {
+    const int idx = base + tid;
+    const int n = idx < ngroups ? s_n[idx] : 0;
+    const int ex = block_exclusive_scan(n, warp_sums, &s_units);
+    if (idx < ngroups) s_n[idx] = running + ex;
+    running += s_units;
+    __syncthreads();
+  }
+  const int total_units = running;
+  const bool fits = total_units <= units_cap;
+  // pass 3: units and the per-row merge table
+  for (int idx = tid; idx < ngroups; idx += kSchedThreads) {
+    int g, r0, nq, kcap;
+    group_info(idx, g, r0, nq, kcap);
+    int ends[4] = {0, 0, 0, 0}, ke = 0;
+    for (int i = 0; i < nq && i < 4; ++i) {
+      ends[i] = min(max(row_ends[r0 + i], 0), kcap);
+      ke = max(ke, ends[i]);
+    }
+    const int nch = ke > cap ? (ke + cap - 1) / cap : 1;
+    const int ub = s_n[idx];
+    const bool split = nch > 1 && static_cast<int64_t>(ub + nch) * Q <= slots_cap;
+    if (nch > 1 && !split) set_status(status, IDX_FP4_DEV_CAPACITY);
+    if (fits) {
+      for (int c = 0; c < nch; ++c) {
+        Unit u;
+        u.row = r0;
+        u.table = g;
+        u.kb = c * cap;
+        u.ke = split ? min((c + 1) * cap, ke) : (nch > 1 ? 0 : ke);
+        u.nq = nq;
+        u.slot = split ? (ub + c) * Q : -1;
+        u.pad0 = u.pad1 = 0;
+        units[ub + c] = u;
+      }
+    }
+    for (int i = 0; i < nq; ++i) row_merge[r0 + i] = make_int4(split ? ub * Q + i : -1, split ? nch : 1, ends[i], 0);
   }
   if (tid == 0) {
+    if (!fits) set_status(status, IDX_FP4_DEV_CAPACITY);
     PrefillSchedHeader h{};
     h.magic = kPrefillMagic;
-    h.num_units = total;
+    h.num_units = fits ? total_units : 0;
     h.rows_per_unit = Q;
+    h.units_cap = static_cast<int32_t>(units_cap);
+    h.num_rows = num_rows;
+    h.slots_cap = static_cast<int32_t>(slots_cap);
     *hdr = h;
   }
 }
@@ -282,21 +351,32 @@ __global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
 }  // namespace
 
 cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, int batch, int max_batch, int64_t max_ctx, int ctas,
-                                         int min_tiles, void* sched, int32_t* status, cudaStream_t stream) {
+                                         int min_tiles, int64_t units_cap, void* sched, int32_t* status,
+                                         cudaStream_t stream) {
   build_decode_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(ctx_lens, batch, max_batch, max_ctx, ctas, min_tiles,
-                                                                 sched, status);
+                                                                 units_cap, sched, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_build_prefill_schedule(const int32_t* cu_seqlens, const int32_t* row_ends, const int32_t* ctx_lens,
                                           int num_requests, int num_rows, int rows_per_unit, int table_width,
-                                          void* workspace, int32_t* status, cudaStream_t stream) {
-  build_prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(cu_seqlens, row_ends, ctx_lens, num_requests,
-                                                                  num_rows, rows_per_unit, table_width, workspace,
-                                                                  status);
+                                          int64_t units_cap, int64_t slots_cap, void* workspace, int32_t* status,
+                                          cudaStream_t stream) {
+  constexpr size_t smem = sizeof(int) * (kMaxBatch + 1 + kMaxPrefillGroups);
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(build_prefill_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  build_prefill_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(cu_seqlens, row_ends, ctx_lens, num_requests,
+                                                                     num_rows, rows_per_unit, table_width, units_cap,
+                                                                     slots_cap, workspace, status);
   return cudaGetLastError();
 }
-
-int max_batch_supported() { return kMaxBatchSched; }
 
 }  // namespace idxfp4

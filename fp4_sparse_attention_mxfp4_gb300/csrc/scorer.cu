@@ -1,6 +1,6 @@
 // Scorer: MXFP4 keys x MXFP4 query heads on tcgen05 block-scaled MMA, fused head-weighted
 // ReLU reduction, fused exact top-k. Shared by decode (one query row per unit) and prefill
-// (two rows of one request per unit).
+// (up to two rows of one request per unit).
 //
 // Method ("Score a DSA sparse indexer in FP4", squashed commit message and PR body):
 //   logit[q, t] = sum_h w[q, h] * relu(q_h . k_t), keys read in place from the paged two-plane
@@ -11,20 +11,23 @@
 //   * A 128-key tile (two pages) is the MMA M dimension, query rows x heads the N dimension:
 //     D[128 x N] = K[128 x 128] . Q^T, as two K=64 tcgen05.mma kind::mxf4 block-scaled MMAs
 //     accumulating fp32 in TMEM. TMEM lane = key, so the head sum is thread-local.
-//   * Warp 0 streams pages with 1-D bulk TMA copies (cp.async.bulk): each page's four 1 KB
-//     group chunks land interleaved with the tile's other page, which makes the stage a
-//     canonical no-swizzle K-major operand (LBO 2048 B between 32-dim chunks, SBO 128 B
-//     between 8-key groups) without any register pass.
-//   * Warp 1 rebuilds the stage's scale bytes from the cache's 16x4-transposed order into the
-//     tensor core's scale-factor layout (key m at lane m%32, column m/32), copies them to TMEM
-//     with tcgen05.cp, and issues the MMAs; tcgen05.commit frees the stage and hands the
+//   * Eight producer warps each own one stage of an 8-stage ring and fill it with 1-D bulk TMA
+//     copies (cp.async.bulk), the ten copies of a tile spread over ten lanes: a page's four 1 KB
+//     group chunks land interleaved with the tile's other page, which makes the stage a canonical
+//     no-swizzle K-major operand (LBO 2048 B between 32-dim chunks, SBO 128 B between 8-key
+//     groups). Bulk copies issued by one warp are processed one after another, so the stream
+//     rate grows with the number of issuing warps; eight reach the HBM copy rate.
+//   * One MMA warp rebuilds each stage's scale bytes from the cache's 16x4-transposed order into
+//     the tensor core's scale-factor layout (key m at lane m%32, column m/32), copies them to
+//     TMEM with tcgen05.cp and issues the MMAs; tcgen05.commit frees the stage and hands the
 //     accumulator to the epilogue.
-//   * Warps 2-5 (one per TMEM lane quarter) read the accumulator with tcgen05.ld, form the
-//     logit, and push it through a per-row threshold filter into a shared-memory candidate
-//     buffer; the buffer is cut back to k with an exact radix select when it fills. The full
-//     logit row never reaches global memory (unless a debug buffer is passed).
-//   * Persistent grid, one CTA per SM; every on-chip wait is bounded and reports a timeout in
-//     the status word instead of hanging.
+//   * Four epilogue warps (one per TMEM lane quarter) read the accumulator with tcgen05.ld, form
+//     each key's logit in a fixed order, store its order-preserving key in a shared-memory row
+//     buffer and count it in a per-warp histogram. At the end of a unit an exact radix select
+//     finds the k-th key and a stable pass writes the selected keys in token order. The logit
+//     row never reaches global memory (unless a debug buffer is passed).
+//   * Persistent grid, one CTA per SM; every on-chip wait is bounded and reports a timeout in the
+//     status word instead of hanging.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -42,12 +45,15 @@ template <int H, int Q>
 struct ScorerCfg {
   static constexpr int N = H * Q;
   static constexpr int ACC = N <= 64 ? 4 : 2;  // TMEM accumulator stages
-  static constexpr int STAGES = 8;             // key tiles in flight per CTA
-  static constexpr int THREADS = 192;
+  static constexpr int STAGES = 8;             // tiles in flight; one producer warp per stage
+  static constexpr int MMA_WARP = STAGES;
+  static constexpr int THREADS = (STAGES + 1 + 4) * 32;
+  static constexpr int UCAP = unit_key_cap(Q);   // keys per unit and row (row buffer size)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SFA_COL = 256;            // ACC chunks of 4 columns
   static constexpr uint32_t SFB_COL = 256 + 4 * 4;    // 2 chunks of 4 columns (unit parity)
   static_assert(ACC * N <= 256, "accumulators fit below the scale columns");
+  static_assert(UCAP % kTileKeys == 0, "whole tiles per unit");
   // shared memory map (offsets from a 1024-byte aligned base)
   static constexpr uint32_t OFF_PACKED = 0;                              // [STAGES][4][128][16]
   static constexpr uint32_t OFF_SCALE = OFF_PACKED + STAGES * 8192;      // [STAGES][2 pages][256]
@@ -57,12 +63,12 @@ struct ScorerCfg {
   static constexpr uint32_t OFF_UNIT = OFF_SFA + STAGES * 512;           // [2][UNIT_BYTES]
   static constexpr uint32_t OFF_QB = (OFF_UNIT + 2 * UNIT_BYTES + 1023) / 1024 * 1024;  // [2][4][N][16]
   static constexpr uint32_t OFF_SFB = OFF_QB + 2 * N * 64;               // [2][512]
-  static constexpr uint32_t OFF_CB = OFF_SFB + 2 * 512;                  // [Q][kCandCap] uint2
-  static constexpr uint32_t OFF_HIST = OFF_CB + Q * kCandCap * 8;        // [2048] u32
-  static constexpr uint32_t SCR_WORDS = 256;
-  static constexpr uint32_t OFF_SCR = OFF_HIST + 2048 * 4;
+  static constexpr uint32_t OFF_LG = OFF_SFB + 2 * 512;                  // [Q][UCAP] ordered keys
+  static constexpr uint32_t OFF_HW = OFF_LG + Q * UCAP * 4;              // [Q][4 warps][1024] packed counts
+  static constexpr uint32_t OFF_HIST = OFF_HW + Q * 4 * kHistWords * 4;  // [2048]
+  static constexpr uint32_t OFF_SCR = OFF_HIST + 2048 * 4;               // [64]
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * ACC + 6;
-  static constexpr uint32_t OFF_BAR = OFF_SCR + SCR_WORDS * 4;
+  static constexpr uint32_t OFF_BAR = OFF_SCR + 64 * 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM");
@@ -88,8 +94,8 @@ struct ScorerParams {
   int topk;
   int32_t* topk_idx;
   float* topk_val;
-  uint2* cand;
-  int32_t* cand_count;
+  uint2* cand;                   // candidate slots (see cand_slot_entries)
+  int64_t cand_slots;            // slots the caller's buffer holds
   float* logits_debug;
   int64_t logits_stride;
   int32_t* status;
@@ -100,6 +106,7 @@ struct UnitIter {
   const Unit* units;
   int first, count, stride;
   bool ok;
+  __device__ __forceinline__ Unit at(int i) const { return units[first + i * stride]; }
 };
 
 // This CTA's units; `ok` is false when the schedule does not belong to this call.
@@ -109,7 +116,7 @@ __device__ __forceinline__ UnitIter unit_range(const ScorerParams& p) {
   if (p.sched != nullptr) {
     const DecodeSchedHeader* h = static_cast<const DecodeSchedHeader*>(p.sched);
     it.ok = h->magic == kDecodeMagic && h->ctas == static_cast<int>(gridDim.x) && h->batch == p.expect_batch &&
-            h->max_batch >= h->batch && decode_sched_bytes(h->max_batch) <= p.sched_bytes;
+            h->max_batch >= h->batch && decode_sched_bytes_for(h->max_batch, h->units_cap) <= p.sched_bytes;
     if (!it.ok) return it;
     const DecodeSchedView v = decode_sched_view(const_cast<void*>(p.sched), h->max_batch);
     it.units = v.units;
@@ -120,7 +127,8 @@ __device__ __forceinline__ UnitIter unit_range(const ScorerParams& p) {
     it.ok = p.prefill->magic == kPrefillMagic;
     if (!it.ok) return it;
     const int n = p.prefill->num_units;
-    it.units = reinterpret_cast<const Unit*>(p.prefill + 1);
+    it.units = reinterpret_cast<const Unit*>(reinterpret_cast<const char*>(p.prefill) +
+                                             prefill_units_offset(p.prefill->num_rows));
     it.first = c;
     it.count = c < n ? (n - c + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 0;
     it.stride = gridDim.x;
@@ -132,6 +140,32 @@ __device__ __forceinline__ int unit_tiles(const Unit& u) {
   return u.ke > u.kb ? (u.ke - u.kb + kTileKeys - 1) / kTileKeys : 0;
 }
 
+// Position in this CTA's tile sequence: unit i (of the CTA's list), tile j of that unit.
+struct Cursor {
+  int i, j, nt;
+  Unit u;
+};
+
+// Move `steps` tiles forward (skipping units without tiles); false once past the last tile.
+__device__ __forceinline__ bool cursor_advance(Cursor& c, int steps, const UnitIter& it) {
+  while (c.i < it.count && (steps > 0 || c.j >= c.nt)) {
+    const int left = c.nt - c.j;
+    if (steps < left) {
+      c.j += steps;
+      steps = 0;
+    } else {
+      steps -= left;
+      ++c.i;
+      c.j = 0;
+      if (c.i < it.count) {
+        c.u = it.at(c.i);
+        c.nt = unit_tiles(c.u);
+      }
+    }
+  }
+  return c.i < it.count;
+}
+
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              int32_t* status) {
   if (*abort_flag) return false;
@@ -141,8 +175,18 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, vol
   return false;
 }
 
+// Page id of the tile at cursor c: lane 0 reads the tile's first page, lane 1 its second (or -1
+// if the tile has one page). A logical page past the table width reads nothing and gives -2.
+__device__ __forceinline__ int load_tile_page(const ScorerParams& p, const Cursor& c, int lane) {
+  const int lp = c.u.kb / kPage + 2 * c.j + lane;
+  const bool needed = lane == 0 || (lane == 1 && c.u.kb + c.j * kTileKeys + kPage < c.u.ke);
+  if (!needed) return -1;
+  if (lp >= p.bt_stride) return -2;
+  return p.block_tables[static_cast<int64_t>(c.u.table) * p.bt_stride + lp];
+}
+
 template <int H, int Q>
-__global__ void __launch_bounds__(192, 1) scorer_kernel(const __grid_constant__ ScorerParams p) {
+__global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(const __grid_constant__ ScorerParams p) {
   using C = ScorerCfg<H, Q>;
   constexpr int N = C::N, ACC = C::ACC, STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -184,103 +228,102 @@ __global__ void __launch_bounds__(192, 1) scorer_kernel(const __grid_constant__ 
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == C::MMA_WARP) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------- producer: bulk copies of key pages and unit inputs ----------------
+  if (warp < STAGES) {
+    // ---------------- producers: warp p fills stage p with tiles p, p+8, p+16, ... -----------
+    const int ps = warp;
     const uint64_t pol = policy_evict_first();
-    int f = 0;
-    for (int i = 0; i < it.count; ++i) {
-      const Unit u = it.units[it.first + i * it.stride];
+    Cursor c{0, 0, 0, Unit{}};
+    bool have = it.count > 0;
+    if (have) {
+      c.u = it.at(0);
+      c.nt = unit_tiles(c.u);
+      have = cursor_advance(c, ps, it);
+    }
+    int st = 0;  // warp 0 stages the unit inputs of every unit, in order
+    auto stage_unit = [&](int i) {
+      const Unit u = it.at(i);
       const int par = i & 1;
-      uint8_t* stage_unit = smem + C::OFF_UNIT + par * C::UNIT_BYTES;
+      uint8_t* dst = smem + C::OFF_UNIT + par * C::UNIT_BYTES;
+      if (i >= 2) bounded_wait(&unit_empty[par], ((i >> 1) - 1) & 1, abort_flag, p.status);
+      const uint32_t rq = u.nq * H * 64, rqs = u.nq * H * 4;
+      mbar_arrive_expect_tx(&unit_full[par], rq + 2 * rqs);
+      bulk_load(dst, p.q_packed + static_cast<int64_t>(u.row) * H * 64, rq, &unit_full[par]);
+      bulk_load(dst + C::RAW_Q, p.q_scale + static_cast<int64_t>(u.row) * H * 4, rqs, &unit_full[par]);
+      bulk_load(dst + C::RAW_Q + C::RAW_QS, p.weights + static_cast<int64_t>(u.row) * H, rqs, &unit_full[par]);
+    };
+    int entry = have ? load_tile_page(p, c, lane) : -1;
+    int f = ps;
+    while (have) {
+      if (ps == 0 && lane == 0)
+        while (st <= c.i) stage_unit(st++);
+      int pid0 = __shfl_sync(0xFFFFFFFFu, entry, 0);
+      int pid1 = __shfl_sync(0xFFFFFFFFu, entry, 1);
+      const bool has1 = pid1 != -1;
+      if ((pid0 == -2 || pid1 == -2) && lane == 0) set_status(p.status, IDX_FP4_DEV_BAD_CTX);
+      if (pid0 < 0 || pid0 >= p.num_pages) {
+        if (lane == 0 && pid0 != -2) set_status(p.status, IDX_FP4_DEV_BAD_PAGE);
+        pid0 = 0;
+      }
+      if (has1 && (pid1 < 0 || pid1 >= p.num_pages)) {
+        if (lane == 0 && pid1 != -2) set_status(p.status, IDX_FP4_DEV_BAD_PAGE);
+        pid1 = 0;
+      }
+      // the next tile of this stage: its page ids load while this one streams
+      Cursor nc = c;
+      const bool next = cursor_advance(nc, STAGES, it);
+      const int next_entry = next ? load_tile_page(p, nc, lane) : -1;
       if (lane == 0) {
-        if (i >= 2) bounded_wait(&unit_empty[par], ((i >> 1) - 1) & 1, abort_flag, p.status);
-        const uint32_t rq = u.nq * H * 64, rqs = u.nq * H * 4;
-        mbar_arrive_expect_tx(&unit_full[par], rq + 2 * rqs);
-        bulk_load(stage_unit, p.q_packed + static_cast<int64_t>(u.row) * H * 64, rq, &unit_full[par]);
-        bulk_load(stage_unit + C::RAW_Q, p.q_scale + static_cast<int64_t>(u.row) * H * 4, rqs, &unit_full[par]);
-        bulk_load(stage_unit + C::RAW_Q + C::RAW_QS, p.weights + static_cast<int64_t>(u.row) * H, rqs,
-                  &unit_full[par]);
+        bounded_wait(&empty_bar[ps], ((f / STAGES) & 1) ^ 1, abort_flag, p.status);
+        mbar_arrive_expect_tx(&full_bar[ps], (has1 ? 2u : 1u) * (kPageBytes + kPageScaleBytes));
       }
-      const int ntiles = unit_tiles(u);
-      const int32_t* table = p.block_tables + static_cast<int64_t>(u.table) * p.bt_stride;
-      const int lp_first = u.kb / kPage;
-      const int lp_end = (u.ke + kPage - 1) / kPage;  // one past the last logical page read
-      int wb = -64, entry = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int lp0 = lp_first + 2 * j;
-        const bool has1 = u.kb + j * kTileKeys + kPage < u.ke;
-        if (lp0 - wb >= 32) {
-          wb = lp0;
-          const int lp = wb + lane;
-          entry = (lp < lp_end && lp < p.bt_stride) ? table[lp] : 0;
+      __syncwarp();
+      // lanes 0..3: group chunks of page 0; lane 4: page 0 scales; lanes 5..9: the same for page 1
+      if (lane < 10 && (lane < 5 || has1)) {
+        const int pg = lane < 5 ? 0 : 1, k = lane < 5 ? lane : lane - 5;
+        const int64_t pid = pg == 0 ? pid0 : pid1;
+        uint8_t* dst;
+        const uint8_t* src;
+        uint32_t bytes;
+        if (k < 4) {
+          dst = smem + C::OFF_PACKED + ps * 8192 + k * 2048 + pg * 1024;
+          src = p.kv_packed + pid * kPageBytes + k * 1024;
+          bytes = 1024;
+        } else {
+          dst = smem + C::OFF_SCALE + ps * 512 + pg * 256;
+          src = p.kv_scale + pid * kPageScaleBytes;
+          bytes = 256;
         }
-        int pid0 = __shfl_sync(0xFFFFFFFFu, entry, lp0 - wb);
-        int pid1 = __shfl_sync(0xFFFFFFFFu, entry, (lp0 + 1 - wb) & 31);
-        if (lane == 0) {
-          if (lp0 >= p.bt_stride || (has1 && lp0 + 1 >= p.bt_stride)) {
-            set_status(p.status, IDX_FP4_DEV_BAD_CTX);
-            pid0 = lp0 >= p.bt_stride ? 0 : pid0;
-            pid1 = 0;
-          }
-          if (pid0 < 0 || pid0 >= p.num_pages) {
-            set_status(p.status, IDX_FP4_DEV_BAD_PAGE);
-            pid0 = 0;
-          }
-          if (has1 && (pid1 < 0 || pid1 >= p.num_pages)) {
-            set_status(p.status, IDX_FP4_DEV_BAD_PAGE);
-            pid1 = 0;
-          }
-          const int s = f % STAGES;
-          bounded_wait(&empty_bar[s], ((f / STAGES) & 1) ^ 1, abort_flag, p.status);
-          uint8_t* dst = smem + C::OFF_PACKED + s * 8192;
-          uint8_t* dsc = smem + C::OFF_SCALE + s * 512;
-          mbar_arrive_expect_tx(&full_bar[s], (has1 ? 2u : 1u) * (kPageBytes + kPageScaleBytes));
-          const uint8_t* src0 = p.kv_packed + static_cast<int64_t>(pid0) * kPageBytes;
-          const uint8_t* src1 = p.kv_packed + static_cast<int64_t>(pid1) * kPageBytes;
-          if (p.stream_once) {
-#pragma unroll
-            for (int g = 0; g < 4; ++g) bulk_load_evict_first(dst + g * 2048, src0 + g * 1024, 1024, &full_bar[s], pol);
-            bulk_load_evict_first(dsc, p.kv_scale + static_cast<int64_t>(pid0) * kPageScaleBytes, 256, &full_bar[s], pol);
-            if (has1) {
-#pragma unroll
-              for (int g = 0; g < 4; ++g)
-                bulk_load_evict_first(dst + g * 2048 + 1024, src1 + g * 1024, 1024, &full_bar[s], pol);
-              bulk_load_evict_first(dsc + 256, p.kv_scale + static_cast<int64_t>(pid1) * kPageScaleBytes, 256,
-                                    &full_bar[s], pol);
-            }
-          } else {
-#pragma unroll
-            for (int g = 0; g < 4; ++g) bulk_load(dst + g * 2048, src0 + g * 1024, 1024, &full_bar[s]);
-            bulk_load(dsc, p.kv_scale + static_cast<int64_t>(pid0) * kPageScaleBytes, 256, &full_bar[s]);
-            if (has1) {
-#pragma unroll
-              for (int g = 0; g < 4; ++g) bulk_load(dst + g * 2048 + 1024, src1 + g * 1024, 1024, &full_bar[s]);
-              bulk_load(dsc + 256, p.kv_scale + static_cast<int64_t>(pid1) * kPageScaleBytes, 256, &full_bar[s]);
-            }
-          }
-        }
-        __syncwarp();
-        ++f;
+        if (p.stream_once)
+          bulk_load_evict_first(dst, src, bytes, &full_bar[ps], pol);
+        else
+          bulk_load(dst, src, bytes, &full_bar[ps]);
       }
+      __syncwarp();
+      c = nc;
+      have = next;
+      entry = next_entry;
+      f += STAGES;
     }
-    // After an abort the consumers stop waiting; drain this CTA's copies before teardown.
+    if (ps == 0 && lane == 0)
+      while (st < it.count) stage_unit(st++);
+    // After an abort the consumers stop waiting; drain this warp's copies before teardown.
     if (lane == 0 && *abort_flag) {
-      for (int k = f - STAGES < 0 ? 0 : f - STAGES; k < f; ++k)
-        mbar_wait(&full_bar[k % STAGES], (k / STAGES) & 1, kWaitLimitNs);
-      for (int i = it.count - 2 < 0 ? 0 : it.count - 2; i < it.count; ++i)
-        mbar_wait(&unit_full[i & 1], (i >> 1) & 1, kWaitLimitNs);
+      if (f - STAGES >= 0) mbar_wait(&full_bar[ps], ((f - STAGES) / STAGES) & 1, kWaitLimitNs);
+      if (ps == 0)
+        for (int i = it.count - 2 < 0 ? 0 : it.count - 2; i < it.count; ++i)
+          mbar_wait(&unit_full[i & 1], (i >> 1) & 1, kWaitLimitNs);
     }
-  } else if (warp == 1) {
+  } else if (warp == C::MMA_WARP) {
     // ---------------- MMA issuer ----------------
     int f = 0, t = 0;
     for (int i = 0; i < it.count; ++i) {
-      const Unit u = it.units[it.first + i * it.stride];
+      const Unit u = it.at(i);
       const int par = i & 1;
       const uint8_t* raw = smem + C::OFF_UNIT + par * C::UNIT_BYTES;
       uint8_t* qb = smem + C::OFF_QB + par * (N * 64);
@@ -290,8 +333,8 @@ __global__ void __launch_bounds__(192, 1) scorer_kernel(const __grid_constant__ 
       __syncwarp();
       // Plain [rows*H][64 B] query -> canonical K-major [4 chunks][N][16 B]; missing rows zeroed.
       const int live = u.nq * H;
-      for (int c = lane; c < 4 * N; c += 32) {
-        const int g = c / N, n = c % N;
+      for (int cc = lane; cc < 4 * N; cc += 32) {
+        const int g = cc / N, n = cc % N;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (n < live) v = *reinterpret_cast<const uint4*>(raw + n * 64 + g * 16);
         *reinterpret_cast<uint4*>(qb + g * N * 16 + n * 16) = v;
@@ -356,33 +399,32 @@ __global__ void __launch_bounds__(192, 1) scorer_kernel(const __grid_constant__ 
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue: head-weighted ReLU sum + streaming top-k ----------------
+    // ---------------- epilogue: head-weighted ReLU sum, row buffer, exact top-k ----------------
     const int qtr = warp & 3;               // TMEM lane quarter of this warp
     const int etid = qtr * 32 + lane;       // key row within the tile, and rank in the group
     const uint32_t lane_base = static_cast<uint32_t>(qtr * 32) << 16;
-    uint2* cb_base = reinterpret_cast<uint2*>(smem + C::OFF_CB);
+    uint32_t* lg_base = reinterpret_cast<uint32_t*>(smem + C::OFF_LG);
+    uint32_t* hw_base = reinterpret_cast<uint32_t*>(smem + C::OFF_HW);
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);
     uint32_t* scr = reinterpret_cast<uint32_t*>(smem + C::OFF_SCR);
-    uint32_t* wc = scr + 64;  // block_append scratch, 2*Q*4 words
-    uint2* cb[Q];
-#pragma unroll
-    for (int r = 0; r < Q; ++r) cb[r] = cb_base + r * kCandCap;
-    int t = 0, par = 0;
+    int t = 0;
     for (int i = 0; i < it.count; ++i) {
-      const Unit u = it.units[it.first + i * it.stride];
+      const Unit u = it.at(i);
       const int upar = i & 1;
       const float* wsm = reinterpret_cast<const float*>(smem + C::OFF_UNIT + upar * C::UNIT_BYTES + C::RAW_Q +
                                                         C::RAW_QS);
+      // this warp's histograms start empty (the previous unit's selection ended with a barrier)
+#pragma unroll
+      for (int r = 0; r < Q; ++r)
+        for (int wd = lane; wd < kHistWords; wd += 32) hw_base[(r * 4 + qtr) * kHistWords + wd] = 0u;
+      __syncwarp();
       bounded_wait(&unit_full[upar], (i >> 1) & 1, abort_flag, p.status);
-      int end[Q], cnt[Q];
-      uint32_t tau[Q];
+      int end[Q];
 #pragma unroll
       for (int r = 0; r < Q; ++r) {
         int e = 0;
         if (r < u.nq) e = p.row_ends != nullptr ? min(max(p.row_ends[u.row + r], 0), u.ke) : u.ke;
         end[r] = e;
-        cnt[r] = 0;
-        tau[r] = 0u;
       }
       const int ntiles = unit_tiles(u);
       for (int j = 0; j < ntiles; ++j, ++t) {
@@ -392,158 +434,290 @@ __global__ void __launch_bounds__(192, 1) scorer_kernel(const __grid_constant__ 
         float logit[Q];
 #pragma unroll
         for (int r = 0; r < Q; ++r) {
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f, s5 = 0.f, s6 = 0.f, s7 = 0.f;
           const uint32_t col = tmem + lane_base + a * N + r * H;
           if constexpr (H == 16) {
             float v[16];
             tmem_load_x16(col, v);
 #pragma unroll
-            for (int h = 0; h < 16; h += 4) {
-              const float4 w = *reinterpret_cast<const float4*>(wsm + r * H + h);
-              s0 = fmaf(w.x, fmaxf(v[h], 0.f), s0);
-              s1 = fmaf(w.y, fmaxf(v[h + 1], 0.f), s1);
-              s2 = fmaf(w.z, fmaxf(v[h + 2], 0.f), s2);
-              s3 = fmaf(w.w, fmaxf(v[h + 3], 0.f), s3);
+            for (int h = 0; h < 16; h += 8) {
+              const float4 wa = *reinterpret_cast<const float4*>(wsm + r * H + h);
+              const float4 wb = *reinterpret_cast<const float4*>(wsm + r * H + h + 4);
+              s0 = fmaf(wa.x, fmaxf(v[h], 0.f), s0);
+              s1 = fmaf(wa.y, fmaxf(v[h + 1], 0.f), s1);
+              s2 = fmaf(wa.z, fmaxf(v[h + 2], 0.f), s2);
+              s3 = fmaf(wa.w, fmaxf(v[h + 3], 0.f), s3);
+              s4 = fmaf(wb.x, fmaxf(v[h + 4], 0.f), s4);
+              s5 = fmaf(wb.y, fmaxf(v[h + 5], 0.f), s5);
+              s6 = fmaf(wb.z, fmaxf(v[h + 6], 0.f), s6);
+              s7 = fmaf(wb.w, fmaxf(v[h + 7], 0.f), s7);
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < H; c += 32) {
+            for (int cc = 0; cc < H; cc += 32) {
               float v[32];
-              tmem_load_x32(col + c, v);
+              tmem_load_x32(col + cc, v);
 #pragma unroll
-              for (int h = 0; h < 32; h += 4) {
-                const float4 w = *reinterpret_cast<const float4*>(wsm + r * H + c + h);
-                s0 = fmaf(w.x, fmaxf(v[h], 0.f), s0);
-                s1 = fmaf(w.y, fmaxf(v[h + 1], 0.f), s1);
-                s2 = fmaf(w.z, fmaxf(v[h + 2], 0.f), s2);
-                s3 = fmaf(w.w, fmaxf(v[h + 3], 0.f), s3);
+              for (int h = 0; h < 32; h += 8) {
+                const float4 wa = *reinterpret_cast<const float4*>(wsm + r * H + cc + h);
+                const float4 wb = *reinterpret_cast<const float4*>(wsm + r * H + cc + h + 4);
+                s0 = fmaf(wa.x, fmaxf(v[h], 0.f), s0);
+                s1 = fmaf(wa.y, fmaxf(v[h + 1], 0.f), s1);
+                s2 = fmaf(wa.z, fmaxf(v[h + 2], 0.f), s2);
+                s3 = fmaf(wa.w, fmaxf(v[h + 3], 0.f), s3);
+                s4 = fmaf(wb.x, fmaxf(v[h + 4], 0.f), s4);
+                s5 = fmaf(wb.y, fmaxf(v[h + 5], 0.f), s5);
+                s6 = fmaf(wb.z, fmaxf(v[h + 6], 0.f), s6);
+                s7 = fmaf(wb.w, fmaxf(v[h + 7], 0.f), s7);
               }
             }
           }
-          logit[r] = (s0 + s1) + (s2 + s3);
+          logit[r] = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
         }
         tc_fence_before_sync();
         mbar_arrive(&acc_empty[a]);
-        const int key = u.kb + j * kTileKeys + etid;
-        bool keep[Q];
-        uint2 val[Q];
+        const int rel = j * kTileKeys + etid;  // < UCAP: a unit holds at most UCAP keys
+        const int key = u.kb + rel;
 #pragma unroll
         for (int r = 0; r < Q; ++r) {
           const bool valid = key < end[r];
           const uint32_t uk = valid ? ordered_key(logit[r]) : 0u;
-          keep[r] = valid && uk > tau[r];
-          val[r] = make_uint2(uk, static_cast<uint32_t>(key));
+          lg_base[r * C::UCAP + rel] = uk;
+          if (valid) hist16_add(hw_base + (r * 4 + qtr) * kHistWords, uk);
           if (valid && p.logits_debug != nullptr && key < p.logits_stride)
             p.logits_debug[static_cast<int64_t>(u.row + r) * p.logits_stride + key] = logit[r];
         }
-        block_append<Q, 4>(cb, cnt, keep, val, qtr, lane, wc, par, kEpiBarrier);
-#pragma unroll
-        for (int r = 0; r < Q; ++r) {
-          if (cnt[r] > kCandCap - kTileKeys) {
-            tau[r] = block_select<128>(cb[r], cnt[r], p.topk, hist, scr, etid, kEpiBarrier);
-            cnt[r] = p.topk;
-          }
-        }
       }
-      // unit inputs are no longer needed
-      mbar_arrive(&unit_empty[upar]);
-      // finalize each row: exactly min(k, valid keys) entries, in token order
-#pragma unroll
-      for (int r = 0; r < Q; ++r) {
-        if (r >= u.nq) continue;
+      mbar_arrive(&unit_empty[upar]);  // the unit's weights are no longer read
+      named_barrier_sync(kEpiBarrier, 128);
+      // select each row: exactly min(k, valid keys) keys, in token order
+      for (int r = 0; r < u.nq && r < Q; ++r) {
+        const uint32_t* keys = lg_base + r * C::UCAP;
         const int nvalid = max(0, end[r] - u.kb);
         const int kk = min(p.topk, nvalid);
-        if (cnt[r] > kk) {
-          block_select<128>(cb[r], cnt[r], kk, hist, scr, etid, kEpiBarrier);
-          cnt[r] = kk;
-        }
+        uint2 th = make_uint2(0u, 0u);  // (T, need): T = 0 keeps every valid key
+        auto key_at = [keys](int x) { return keys[x]; };
+        if (kk < nvalid)
+          th = radix_threshold<128, 4>(key_at, nvalid, kk, hw_base + r * 4 * kHistWords, hist, scr, etid,
+                                       kEpiBarrier);
+        const int kb = u.kb;
         if (u.slot < 0) {
-          const int64_t row = u.row + r;
-          for (int e = etid; e < p.topk; e += 128) {
-            const bool in = e < kk;
-            const uint2 c = in ? cb[r][e] : make_uint2(0u, 0u);
-            p.topk_idx[row * p.topk + e] = in ? static_cast<int32_t>(c.y) : -1;
-            if (p.topk_val != nullptr) p.topk_val[row * p.topk + e] = in ? key_to_float(c.x) : -__int_as_float(0x7f800000);
+          const int64_t rowoff = static_cast<int64_t>(u.row + r) * p.topk;
+          int32_t* oi = p.topk_idx + rowoff;
+          float* ov = p.topk_val != nullptr ? p.topk_val + rowoff : nullptr;
+          stable_emit<128>(key_at, nvalid, th.x, th.y, scr, etid, kEpiBarrier, [=](int pos, int x, uint32_t kv) {
+            oi[pos] = kb + x;
+            if (ov != nullptr) ov[pos] = key_to_float(kv);
+          });
+          for (int e = kk + etid; e < p.topk; e += 128) {
+            oi[e] = -1;
+            if (ov != nullptr) ov[e] = -__int_as_float(0x7f800000);
           }
-        } else {
-          for (int e = etid; e < kk; e += 128) p.cand[static_cast<int64_t>(u.slot) * p.topk + e] = cb[r][e];
-          if (etid == 0) p.cand_count[u.slot] = kk;
+        } else if (u.slot + r < p.cand_slots) {
+          uint2* slot = p.cand + static_cast<int64_t>(u.slot + r) * static_cast<int64_t>(cand_slot_entries(p.topk));
+          uint2* oc = slot + 2;
+          stable_emit<128>(key_at, nvalid, th.x, th.y, scr, etid, kEpiBarrier,
+                           [=](int pos, int x, uint32_t kv) { oc[pos] = make_uint2(kv, static_cast<uint32_t>(kb + x)); });
+          // odd counts get one pad entry so every list is a whole number of 16-byte pairs; key 0 is
+          // below every logit and never selected
+          if (etid == 0) {
+            if (kk & 1) oc[kk] = make_uint2(0u, 0xFFFFFFFFu);
+            slot[0] = make_uint2(static_cast<uint32_t>(kk), 0u);
+          }
+        } else if (etid == 0) {
+          set_status(p.status, IDX_FP4_DEV_CAPACITY);
         }
-        named_barrier_sync(kEpiBarrier, 128);
       }
+      named_barrier_sync(kEpiBarrier, 128);
     }
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == C::MMA_WARP) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
-// Merge the per-unit candidate lists of each split sequence into its final top-k; also
-// writes the all-padding output of sequences with no keys.
+// ---------------------------------------------------------------------------------------------
+// Merge of split rows (decode sequences spread over several units, prefill rows cut into key
+// chunks): the row's candidate lists (each exactly its unit's top-min(k, keys), in token order)
+// are bulk-copied into shared memory in key order and the exact selection runs over them. Also
+// writes the all-padding output of decode sequences with no keys.
 constexpr int kMergeThreads = 256;
+constexpr int kMergeCap = 20480;    // candidate entries held at once
+constexpr int kMergeKeep = kMaxTopk;
+constexpr size_t kMergeSmem = static_cast<size_t>(kMergeCap) * 8 + static_cast<size_t>(kMergeKeep) * 8 +
+                              8 * kHistWords * 4 + 2048 * 4 + 64 * 4 + 16 + 1024;
 
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const void* sched, size_t sched_bytes,
-                                                              const int32_t* ctx_lens, int batch, int topk,
-                                                              const uint2* __restrict__ cand,
-                                                              const int32_t* __restrict__ cand_count,
-                                                              int32_t* topk_idx, float* topk_val, int32_t* status) {
-  __shared__ uint2 cb[kCandCap];
-  __shared__ uint32_t hist[2048];
-  __shared__ uint32_t scr[select_scratch_words<kMergeThreads>() + 2 * 8];
-  const DecodeSchedHeader* h = static_cast<const DecodeSchedHeader*>(sched);
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  if (h->magic != kDecodeMagic || h->batch != batch || h->max_batch < batch ||
-      decode_sched_bytes(h->max_batch) > sched_bytes)
-    return;  // flagged by the scorer
-  const DecodeSchedView v = decode_sched_view(const_cast<void*>(sched), h->max_batch);
-  const int ctx = v.seq_ctx[b];
-  const int nu = v.seq_units[b];
-  if (tid == 0 && ctx_lens[b] >= 0 && ctx_lens[b] != ctx) set_status(status, IDX_FP4_DEV_BAD_SCHEDULE);
-  if (nu == 1) return;  // written by the scorer
-  const int kk = min(topk, ctx);
-  int cnt[1] = {0};
-  uint32_t tau = 0u;
-  int par = 0;
-  uint32_t* wc = scr + select_scratch_words<kMergeThreads>();
-  uint2* cbr[1] = {cb};
-  for (int ui = 0; ui < nu; ++ui) {
-    const int slot = v.seq_first[b] + ui;
-    const int n = min(cand_count[slot], topk);
-    for (int base = 0; base < n; base += kMergeThreads) {
-      const int e = base + tid;
-      const uint2 c = e < n ? cand[static_cast<int64_t>(slot) * topk + e] : make_uint2(0u, 0u);
-      bool keep[1] = {e < n && c.x > tau};
-      uint2 val[1] = {c};
-      block_append<1, kMergeThreads / 32>(cbr, cnt, keep, val, w, lane, wc, par, 1);
-      if (cnt[0] > kCandCap - kMergeThreads) {
-        tau = block_select<kMergeThreads>(cb, cnt[0], topk, hist, scr, tid, 1);
-        cnt[0] = topk;
+struct MergeParams {
+  const void* sched;                 // decode: the schedule, else nullptr
+  size_t sched_bytes;
+  const int32_t* ctx_lens;
+  int batch;
+  const PrefillSchedHeader* prefill; // prefill: the workspace header, else nullptr
+  int topk;
+  const uint2* cand;
+  int64_t cand_slots;
+  int32_t* topk_idx;
+  float* topk_val;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeParams mp) {
+  extern __shared__ uint8_t msm_raw[];
+  uint8_t* msm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(msm_raw) + 1023) & ~uintptr_t(1023));
+  uint2* buf = reinterpret_cast<uint2*>(msm);
+  uint2* keep = buf + kMergeCap;
+  uint32_t* hw = reinterpret_cast<uint32_t*>(keep + kMergeKeep);
+  uint32_t* hist = hw + 8 * kHistWords;
+  uint32_t* scr = hist + 2048;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(scr + 64);
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int topk = mp.topk;
+  int first, nu, stride, kk;
+  if (mp.sched != nullptr) {
+    const DecodeSchedHeader* h = static_cast<const DecodeSchedHeader*>(mp.sched);
+    if (h->magic != kDecodeMagic || h->batch != mp.batch || h->max_batch < mp.batch ||
+        decode_sched_bytes_for(h->max_batch, h->units_cap) > mp.sched_bytes)
+      return;  // flagged by the scorer
+    const DecodeSchedView v = decode_sched_view(const_cast<void*>(mp.sched), h->max_batch);
+    const int ctx = v.seq_ctx[row];
+    nu = v.seq_units[row];
+    first = v.seq_first[row];
+    stride = 1;
+    kk = min(topk, ctx);
+    if (tid == 0 && mp.ctx_lens[row] >= 0 && mp.ctx_lens[row] != ctx) set_status(mp.status, IDX_FP4_DEV_BAD_SCHEDULE);
+    if (nu == 0) {
+      for (int e = tid; e < topk; e += kMergeThreads) {
+        mp.topk_idx[static_cast<int64_t>(row) * topk + e] = -1;
+        if (mp.topk_val != nullptr) mp.topk_val[static_cast<int64_t>(row) * topk + e] = -__int_as_float(0x7f800000);
+      }
+      return;
+    }
+  } else {
+    if (mp.prefill->magic != kPrefillMagic) return;
+    const int4 rm = reinterpret_cast<const int4*>(mp.prefill + 1)[row];
+    first = rm.x;
+    nu = rm.y;
+    stride = mp.prefill->rows_per_unit;
+    kk = min(topk, rm.z);
+  }
+  if (nu <= 1) return;  // written by the scorer
+  const int64_t orow = static_cast<int64_t>(row) * topk;
+  const int64_t slot_entries = static_cast<int64_t>(cand_slot_entries(topk));
+  auto list_count = [&](int i) {
+    const int64_t s = first + static_cast<int64_t>(i) * stride;
+    return s < mp.cand_slots ? min(static_cast<int>(mp.cand[s * slot_entries].x), topk) : 0;
+  };
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  int kept = 0, next = 0, round = 0;
+  bool timed_out = false;
+  while (next < nu) {
+    // the lists that fit after the kept prefix
+    int total = kept, last = next;
+    uint32_t bytes = 0;
+    while (last < nu) {
+      const int ce = (list_count(last) + 1) & ~1;
+      if (total + ce > kMergeCap) break;
+      total += ce;
+      bytes += static_cast<uint32_t>(ce) * 8u;
+      ++last;
+    }
+    if (tid == 0 && bytes > 0) mbar_arrive_expect_tx(bar, bytes);
+    __syncthreads();
+    if (lane == 0 && bytes > 0) {
+      int off = kept;
+      for (int x = next; x < last; ++x) {
+        const int ce = (list_count(x) + 1) & ~1;
+        if ((x - next) % 8 == w && ce > 0)
+          bulk_load(buf + off, mp.cand + (first + static_cast<int64_t>(x) * stride) * slot_entries + 2,
+                    static_cast<uint32_t>(ce) * 8u, bar);
+        off += ce;
       }
     }
+    if (bytes > 0) {
+      if (!mbar_wait(bar, round & 1, kWaitLimitNs)) timed_out = true;
+      ++round;
+    }
+    __syncthreads();
+    next = last;
+    const int n = total;
+    const bool final = next >= nu;
+    const int kr = final ? kk : min(topk, n);
+    // level-1 histograms, one per warp
+    for (int wd = lane; wd < kHistWords; wd += 32) hw[w * kHistWords + wd] = 0u;
+    __syncwarp();
+    for (int x = tid; x < n; x += kMergeThreads) hist16_add(hw + w * kHistWords, buf[x].x);
+    __syncthreads();
+    auto key_at = [buf](int x) { return buf[x].x; };
+    uint2 th = make_uint2(0u, 0u);
+    if (kr < n) th = radix_threshold<kMergeThreads, 8>(key_at, n, kr, hw, hist, scr, tid, 1);
+    if (final) {
+      int32_t* oi = mp.topk_idx + orow;
+      float* ov = mp.topk_val != nullptr ? mp.topk_val + orow : nullptr;
+      stable_emit<kMergeThreads>(key_at, n, th.x, th.y, scr, tid, 1, [=](int pos, int x, uint32_t kv) {
+        oi[pos] = static_cast<int32_t>(buf[x].y);
+        if (ov != nullptr) ov[pos] = key_to_float(kv);
+      });
+      for (int e = kk + tid; e < topk; e += kMergeThreads) {
+        oi[e] = -1;
+        if (ov != nullptr) ov[e] = -__int_as_float(0x7f800000);
+      }
+    } else {
+      stable_emit<kMergeThreads>(key_at, n, th.x, th.y, scr, tid, 1,
+                                 [=](int pos, int x, uint32_t) { keep[pos] = buf[x]; });
+      kept = kr;
+      for (int x = tid; x < kept; x += kMergeThreads) buf[x] = keep[x];
+      if (kept & 1) {
+        if (tid == 0) buf[kept] = make_uint2(0u, 0xFFFFFFFFu);
+        kept += 1;
+      }
+      __syncthreads();
+    }
   }
-  if (cnt[0] > kk) {
-    block_select<kMergeThreads>(cb, cnt[0], kk, hist, scr, tid, 1);
-    cnt[0] = kk;
+  if (timed_out && tid == 0) set_status(mp.status, IDX_FP4_DEV_TIMEOUT);
+}
+
+cudaError_t launch_merge(const MergeParams& mp, int rows, cudaStream_t stream) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMergeSmem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  const int outn = min(cnt[0], kk);
-  for (int e = tid; e < topk; e += kMergeThreads) {
-    const bool in = e < outn;
-    const uint2 c = in ? cb[e] : make_uint2(0u, 0u);
-    topk_idx[static_cast<int64_t>(b) * topk + e] = in ? static_cast<int32_t>(c.y) : -1;
-    if (topk_val != nullptr)
-      topk_val[static_cast<int64_t>(b) * topk + e] = in ? key_to_float(c.x) : -__int_as_float(0x7f800000);
+  merge_kernel<<<rows, kMergeThreads, kMergeSmem, stream>>>(mp);
+  return cudaGetLastError();
+}
+
+// The shared-memory opt-in is set once per device (so that a launch inside stream capture is
+// only a launch).
+template <class Kernel>
+cudaError_t ensure_smem(Kernel k, size_t bytes, bool (&configured)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
   }
+  return cudaSuccess;
 }
 
 template <int H, int Q>
 cudaError_t launch_scorer_t(const ScorerParams& p, int grid, cudaStream_t stream) {
   using C = ScorerCfg<H, Q>;
-  cudaError_t e = cudaFuncSetAttribute(scorer_kernel<H, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::SMEM_BYTES));
+  static bool configured[64] = {};
+  cudaError_t e = ensure_smem(scorer_kernel<H, Q>, C::SMEM_BYTES, configured);
   if (e != cudaSuccess) return e;
   scorer_kernel<H, Q><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
@@ -564,10 +738,9 @@ cudaError_t launch_scorer_h(int H, const ScorerParams& p, int grid, cudaStream_t
 cudaError_t launch_decode(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
                           const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
                           const int32_t* block_tables, int bt_stride, const int32_t* ctx_lens, int batch, int H,
-                          int topk, const void* sched, size_t sched_bytes, void* workspace, int slots,
-                          int32_t* topk_idx,
-                          float* topk_val, float* logits_debug, int64_t logits_stride, int32_t* status, int grid,
-                          cudaStream_t stream) {
+                          int topk, const void* sched, size_t sched_bytes, void* workspace, int64_t cand_slots,
+                          int32_t* topk_idx, float* topk_val, float* logits_debug, int64_t logits_stride,
+                          int32_t* status, int grid, cudaStream_t stream) {
   ScorerParams p{};
   p.q_packed = q_packed;
   p.q_scale = q_scale;
@@ -585,24 +758,35 @@ cudaError_t launch_decode(const uint8_t* q_packed, const uint8_t* q_scale, const
   p.topk = topk;
   p.topk_idx = topk_idx;
   p.topk_val = topk_val;
-  p.cand_count = static_cast<int32_t*>(workspace);
-  p.cand = reinterpret_cast<uint2*>(static_cast<char*>(workspace) + round_up(sizeof(int32_t) * slots, 16));
+  p.cand = static_cast<uint2*>(workspace);
+  p.cand_slots = cand_slots;
   p.logits_debug = logits_debug;
   p.logits_stride = logits_stride;
   p.status = status;
   p.stream_once = 1;
   cudaError_t e = H == 128 ? launch_scorer_t<128, 1>(p, grid, stream) : launch_scorer_h<1>(H, p, grid, stream);
   if (e != cudaSuccess) return e;
-  merge_kernel<<<batch, kMergeThreads, 0, stream>>>(sched, sched_bytes, ctx_lens, batch, topk, p.cand, p.cand_count,
-                                                    topk_idx, topk_val, status);
-  return cudaGetLastError();
+  MergeParams mp{};
+  mp.sched = sched;
+  mp.sched_bytes = sched_bytes;
+  mp.ctx_lens = ctx_lens;
+  mp.batch = batch;
+  mp.prefill = nullptr;
+  mp.topk = topk;
+  mp.cand = p.cand;
+  mp.cand_slots = cand_slots;
+  mp.topk_idx = topk_idx;
+  mp.topk_val = topk_val;
+  mp.status = status;
+  return launch_merge(mp, batch, stream);
 }
 
 cudaError_t launch_prefill(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
                            const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
-                           const int32_t* block_tables, int bt_stride, const int32_t* row_ends, int H, int topk,
-                           void* workspace, int32_t* topk_idx, float* topk_val, float* logits_debug,
-                           int64_t logits_stride, int32_t* status, int grid, cudaStream_t stream) {
+                           const int32_t* block_tables, int bt_stride, const int32_t* row_ends, int num_rows, int H,
+                           int topk, void* workspace, int64_t units_cap, int64_t slots_cap, int32_t* topk_idx,
+                           float* topk_val, float* logits_debug, int64_t logits_stride, int32_t* status, int grid,
+                           cudaStream_t stream) {
   PrefillSchedHeader* hdr = static_cast<PrefillSchedHeader*>(workspace);
   ScorerParams p{};
   p.q_packed = q_packed;
@@ -619,12 +803,24 @@ cudaError_t launch_prefill(const uint8_t* q_packed, const uint8_t* q_scale, cons
   p.topk = topk;
   p.topk_idx = topk_idx;
   p.topk_val = topk_val;
+  p.cand = reinterpret_cast<uint2*>(static_cast<char*>(workspace) + prefill_slots_offset(num_rows, units_cap));
+  p.cand_slots = slots_cap;
   p.logits_debug = logits_debug;
   p.logits_stride = logits_stride;
   p.status = status;
   p.stream_once = 0;
-  if (H == 128) return launch_scorer_t<128, 1>(p, grid, stream);
-  return launch_scorer_h<2>(H, p, grid, stream);
+  cudaError_t e = H == 128 ? launch_scorer_t<128, 1>(p, grid, stream) : launch_scorer_h<2>(H, p, grid, stream);
+  if (e != cudaSuccess || slots_cap == 0) return e;
+  MergeParams mp{};
+  mp.sched = nullptr;
+  mp.prefill = hdr;
+  mp.topk = topk;
+  mp.cand = p.cand;
+  mp.cand_slots = slots_cap;
+  mp.topk_idx = topk_idx;
+  mp.topk_val = topk_val;
+  mp.status = status;
+  return launch_merge(mp, num_rows, stream);
 }
 
 }  // namespace idxfp4

@@ -82,8 +82,12 @@ extern "C" {
 #define IDX_FP4_DEV_BAD_SCHEDULE 0x10 /* decode: schedule built for another batch or grid, or ctx_lens
                                          changed since it was built (call skipped) */
 #define IDX_FP4_DEV_TIMEOUT 0x20      /* a bounded on-chip wait gave up (results undefined) */
+#define IDX_FP4_DEV_CAPACITY 0x40     /* the schedule or workspace was sized for smaller contexts than
+                                         the call met (affected rows come out as -1) */
 
 #define IDX_FP4_MAX_TOPK 2048
+#define IDX_FP4_MAX_BATCH 4096        /* sequences per decode call, requests per prefill call */
+#define IDX_FP4_MAX_PREFILL_ROWS 8192 /* query rows per prefill call */
 
 /* Writer: quantise bf16 keys to MXFP4 and store them in the paged cache; optionally quantise
  * query heads to the plain MXFP4 layout. ("Score a DSA sparse indexer in FP4", squashed commit
@@ -103,8 +107,9 @@ int idx_fp4_quant_and_cache(const uint16_t *k_bf16, int64_t num_tokens, const in
                             int64_t num_q_rows, int num_heads, uint8_t *q_packed, uint8_t *q_scale,
                             int32_t *status_dev, cudaStream_t stream);
 
-/* Bytes of the decode schedule buffer for up to `max_batch` sequences (host, no device work). */
-size_t idx_fp4_decode_schedule_bytes(int max_batch);
+/* Bytes of the decode schedule buffer for up to `max_batch` sequences of up to `max_ctx` keys
+ * (host; queries nothing on the device; 0 for invalid arguments). */
+size_t idx_fp4_decode_schedule_bytes(int max_batch, int64_t max_ctx);
 
 /* Build the decode CTA schedule once per step, before the layers; every decode call of the
  * step reads it. ("Score a DSA sparse indexer in FP4", squashed commit message and PR section
@@ -114,13 +119,16 @@ size_t idx_fp4_decode_schedule_bytes(int max_batch);
  *   ctx_lens_dev  device int32 [batch]: keys visible to each sequence (0 allowed)
  *   batch <= max_batch; max_ctx bounds every context (larger sets IDX_FP4_DEV_BAD_CTX and the
  *   sequence is treated as empty)
- *   sched_dev     device buffer of sched_bytes >= idx_fp4_decode_schedule_bytes(max_batch)
- * The schedule targets the current device's SM count; use it on that device. */
+ *   sched_dev     device buffer of sched_bytes >= idx_fp4_decode_schedule_bytes(max_batch, max_ctx)
+ * The schedule targets the current device's SM count; use it on that device. Each CTA gets an
+ * equal block of tile ranges of at most 16384 keys; a sequence spread over several ranges is
+ * merged inside idx_fp4_decode_logits_topk. */
 int idx_fp4_build_decode_schedule(const int32_t *ctx_lens_dev, int batch, int max_batch, int64_t max_ctx,
                                   void *sched_dev, size_t sched_bytes, int32_t *status_dev, cudaStream_t stream);
 
-/* Bytes of the decode workspace (candidate lists of sequences split across CTAs). */
-size_t idx_fp4_decode_workspace_bytes(int max_batch, int topk);
+/* Bytes of the decode workspace (candidate lists of sequences split across CTAs) for schedules
+ * built with (max_batch, max_ctx) and the given topk (host; 0 for invalid arguments). */
+size_t idx_fp4_decode_workspace_bytes(int max_batch, int64_t max_ctx, int topk);
 
 /* Decode: one query row per sequence b scores keys [0, ctx_lens[b]) through block_tables[b]
  * and selects its top-k. ("Score a DSA sparse indexer in FP4": the decode scorer reads q,
@@ -131,7 +139,8 @@ size_t idx_fp4_decode_workspace_bytes(int max_batch, int topk);
  *   block_tables, block_table_stride  device int32 [batch][stride]
  *   ctx_lens_dev   the vector the schedule was built from (checked against it)
  *   sched_dev/sched_bytes   from idx_fp4_build_decode_schedule for this batch
- *   workspace      device, >= idx_fp4_decode_workspace_bytes(max_batch, topk)
+ *   workspace      device, >= idx_fp4_decode_workspace_bytes(max_batch, max_ctx, topk) for the
+ *                  schedule's sizes (a smaller one sets IDX_FP4_DEV_CAPACITY)
  *   topk_idx [batch][topk] (device, required), topk_val [batch][topk] (nullable)
  *   logits_debug   nullable device float [batch][logits_stride]: every scored logit (testing) */
 int idx_fp4_decode_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
@@ -142,8 +151,10 @@ int idx_fp4_decode_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, 
                                float *logits_debug, int64_t logits_stride, int32_t *status_dev,
                                cudaStream_t stream);
 
-/* Bytes of the prefill workspace (its per-call unit table). */
-size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_heads);
+/* Bytes of the prefill workspace (the call's unit table, and candidate lists for rows longer
+ * than one unit's 8192-key (64-head) / 16384-key (128-head) share) for rows of up to max_ctx
+ * keys (host; 0 for invalid arguments). */
+size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_heads, int64_t max_ctx, int topk);
 
 /* Causal prefill: row r of request g (cu_seqlens[g] <= r < cu_seqlens[g+1]) scores keys
  * [0, row_ends[r]) through block_tables[g] and selects its top-min(topk, row_ends[r]).
@@ -155,15 +166,17 @@ size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_h
  *   ctx_lens_dev [num_requests]: keys cached per request; row_ends[r] <= ctx_lens[g] is checked
  *   cu_seqlens_dev [num_requests + 1], non-decreasing, cu_seqlens[0] = 0, cu_seqlens[G] = num_rows
  *   row_ends_dev [num_rows]: a real row at 0-based position p carries p + 1
- *   workspace  device, >= idx_fp4_prefill_workspace_bytes(num_requests, num_rows, num_heads)
+ *   max_ctx    bound on every row end, the value the workspace was sized with
+ *   workspace  device, >= idx_fp4_prefill_workspace_bytes(num_requests, num_rows, num_heads, max_ctx, topk)
+ * Rows longer than one unit's share are scored in key chunks and merged inside the call.
  *   topk_idx [num_rows][topk] (required), topk_val (nullable), logits_debug as for decode */
 int idx_fp4_prefill_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
                                 const uint8_t *kv_packed, const uint8_t *kv_scale, int64_t num_pages,
                                 const int32_t *block_tables, int block_table_stride, const int32_t *ctx_lens_dev,
                                 const int32_t *cu_seqlens_dev, const int32_t *row_ends_dev, int num_requests,
-                                int num_rows, int num_heads, int topk, void *workspace, size_t workspace_bytes,
-                                int32_t *topk_idx, float *topk_val, float *logits_debug, int64_t logits_stride,
-                                int32_t *status_dev, cudaStream_t stream);
+                                int num_rows, int num_heads, int topk, int64_t max_ctx, void *workspace,
+                                size_t workspace_bytes, int32_t *topk_idx, float *topk_val, float *logits_debug,
+                                int64_t logits_stride, int32_t *status_dev, cudaStream_t stream);
 
 /* Human-readable name of a return code. */
 const char *idx_fp4_error_string(int code);

@@ -26,6 +26,7 @@ import numpy as np
 PAGE = 64
 HEAD_DIM = 128
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_CHUNK = 1 << 20
 
 
 def _splitmix64(x: np.ndarray) -> np.ndarray:
@@ -52,22 +53,31 @@ class Rng:
 
     def u64(self, n: int) -> np.ndarray:
         base = np.uint64((self.seed * (1 << 32) + self.stream) & ((1 << 64) - 1))
-        with np.errstate(over="ignore"):
-            ctr = np.arange(self._ctr, self._ctr + n, dtype=np.uint64) * _GOLDEN + base
+        out = np.empty(n, np.uint64)
+        for a in range(0, n, _CHUNK):
+            b = min(n, a + _CHUNK)
+            with np.errstate(over="ignore"):
+                ctr = np.arange(self._ctr + a, self._ctr + b, dtype=np.uint64) * _GOLDEN + base
+            out[a:b] = _splitmix64(ctr)
         self._ctr += n
-        return _splitmix64(ctr)
+        return out
 
     def uniform(self, n: int) -> np.ndarray:
         """Uniform doubles in [0, 1) with 53 random bits."""
         return (self.u64(n) >> np.uint64(11)).astype(np.float64) * (1.0 / (1 << 53))
 
-    def normal(self, n: int) -> np.ndarray:
+    def normal(self, n: int, dtype=np.float64) -> np.ndarray:
+        """Box-Muller pairs: element 2i and 2i+1 come from uniforms 2i (radius) and 2i+1 (angle)."""
         m = (n + 1) // 2
-        u1 = 1.0 - self.uniform(m)  # (0, 1]
-        u2 = self.uniform(m)
-        r = np.sqrt(-2.0 * np.log(u1))
-        t = 2.0 * np.pi * u2
-        return np.concatenate([r * np.cos(t), r * np.sin(t)])[:n]
+        out = np.empty(2 * m, dtype)
+        for a in range(0, m, _CHUNK // 2):
+            b = min(m, a + _CHUNK // 2)
+            u = (self.u64(2 * (b - a)) >> np.uint64(11)).astype(np.float64) * (1.0 / (1 << 53))
+            r = np.sqrt(-2.0 * np.log(1.0 - u[0::2]))
+            t = (2.0 * np.pi) * u[1::2]
+            out[2 * a:2 * b:2] = r * np.cos(t)
+            out[2 * a + 1:2 * b:2] = r * np.sin(t)
+        return out[:n]
 
     def integers(self, lo: int, hi: int, n: int) -> np.ndarray:
         """Integers in [lo, hi] inclusive."""
@@ -95,7 +105,7 @@ def qk_bf16(rng: Rng, lead_shape, outliers: int = 4, factor: float = 5.0) -> np.
     """N(0,1) fp32 vectors of HEAD_DIM with `outliers` channels (drawn once per tensor) scaled, as bf16 bits."""
     lead_shape = tuple(int(s) for s in lead_shape)
     n = int(np.prod(lead_shape)) * HEAD_DIM if lead_shape else HEAD_DIM
-    x = rng.normal(n).astype(np.float32).reshape(lead_shape + (HEAD_DIM,))
+    x = rng.normal(n, np.float32).reshape(lead_shape + (HEAD_DIM,))
     ch = rng.fork(7).permutation(HEAD_DIM)[:outliers]
     x[..., ch] *= np.float32(factor)
     return bf16_bits(x)
@@ -186,13 +196,16 @@ def decode_config(n: int) -> DecodeCase:
     raise ValueError(n)
 
 
-def replay_ctx_sets(seed: int, batch: int, max_ctx: int):
-    """Context-length vectors for graph replay: {max}, {U[65536, max]}, {U[1, max]}, {max} again."""
+def replay_ctx_sets(seed: int, batch: int, max_ctx: int, short_below: int = 2048):
+    """Context-length vectors for graph replay: {max}, {U[65536, max]}, {U[1, max]} with its first
+    entry drawn below `short_below` (a context shorter than k), then {max} again."""
     r = Rng(seed).fork(11)
     lo = min(65536, max_ctx)
+    third = r.fork(1).integers(1, max_ctx, batch).astype(np.int32)
+    third[0] = int(r.fork(2).integers(1, max(1, min(short_below, max_ctx) - 1), 1)[0])
     return [np.full(batch, max_ctx, np.int32),
             r.integers(lo, max_ctx, batch).astype(np.int32),
-            r.fork(1).integers(1, max_ctx, batch).astype(np.int32),
+            third,
             np.full(batch, max_ctx, np.int32)]
 
 

@@ -61,9 +61,10 @@ class DecodeRun:
         self.ctx = dev(case.ctx_lens)
         self.max_batch = max_batch or B
         self.max_ctx = max_ctx or int(case.ctx_lens.max())
-        self.sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(self.max_batch), dtype=torch.uint8, device="cuda")
-        self.ws = torch.zeros(fx.idx_fp4_decode_workspace_bytes(self.max_batch, case.topk), dtype=torch.uint8,
-                              device="cuda")
+        self.sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(self.max_batch, self.max_ctx), dtype=torch.uint8,
+                                 device="cuda")
+        self.ws = torch.zeros(fx.idx_fp4_decode_workspace_bytes(self.max_batch, self.max_ctx, case.topk),
+                              dtype=torch.uint8, device="cuda")
         self.topk_idx = torch.full((B, case.topk), -7, dtype=torch.int32, device="cuda")
         self.topk_val = torch.full((B, case.topk), 7.0, dtype=torch.float32, device="cuda")
         self.logits = None

@@ -59,10 +59,14 @@ def test_writer_rejects_bad_arguments(L):
 
 
 def test_schedule_sizing_and_rejections(L):
-    assert L.idx_fp4_decode_schedule_bytes(0) == 0
-    assert L.idx_fp4_decode_schedule_bytes(100000) == 0
-    n16 = L.idx_fp4_decode_schedule_bytes(16)
-    assert n16 > 0 and L.idx_fp4_decode_schedule_bytes(32) > n16
+    assert L.idx_fp4_decode_schedule_bytes(0, 1 << 20) == 0
+    assert L.idx_fp4_decode_schedule_bytes(100000, 1 << 20) == 0
+    assert L.idx_fp4_decode_schedule_bytes(16, -1) == 0
+    n16 = L.idx_fp4_decode_schedule_bytes(16, 1 << 20)
+    assert n16 > 0 and L.idx_fp4_decode_schedule_bytes(32, 1 << 20) > n16
+    assert L.idx_fp4_decode_schedule_bytes(16, 1 << 22) > n16
+    assert L.idx_fp4_decode_workspace_bytes(16, 1 << 20, 2048) > L.idx_fp4_decode_workspace_bytes(16, 1 << 20, 64)
+    assert L.idx_fp4_decode_workspace_bytes(16, 1 << 20, 0) == 0
     f = L.idx_fp4_build_decode_schedule
     assert f(FAKE, 17, 16, 1 << 20, FAKE, n16, None, None) == ARG      # batch > max_batch
     assert f(FAKE, 4, 16, -1, FAKE, n16, None, None) == ARG             # negative max_ctx
@@ -97,8 +101,8 @@ def test_decode_rejects_bad_arguments(L):
 
 def _prefill(L, **kw):
     a = dict(q=FAKE, qs=FAKE, w=FAKE, kp=FAKE, ks=FAKE, pages=10, bt=FAKE, stride=4, ctx=FAKE, cu=FAKE, re=FAKE,
-             G=2, R=100, heads=64, topk=2048, ws=FAKE, ws_bytes=1 << 20, idx=FAKE, val=None, dbg=None, dbg_stride=0,
-             status=None, stream=None)
+             G=2, R=100, heads=64, topk=2048, max_ctx=4096, ws=FAKE, ws_bytes=1 << 20, idx=FAKE, val=None, dbg=None,
+             dbg_stride=0, status=None, stream=None)
     a.update(kw)
     return L.idx_fp4_prefill_logits_topk(*a.values())
 
@@ -111,7 +115,11 @@ def test_prefill_rejects_bad_arguments(L):
     assert _prefill(L, cu=None) == ARG
     assert _prefill(L, re=None) == ARG
     assert _prefill(L, ws_bytes=16) == CAP
-    need = L.idx_fp4_prefill_workspace_bytes(2, 100, 64)
+    need = L.idx_fp4_prefill_workspace_bytes(2, 100, 64, 4096, 2048)
     assert need > 0 and _prefill(L, ws_bytes=need - 1) == CAP
-    assert L.idx_fp4_prefill_workspace_bytes(0, 100, 64) == 0
-    assert L.idx_fp4_prefill_workspace_bytes(2, 100, 48) == 0
+    long_need = L.idx_fp4_prefill_workspace_bytes(2, 100, 64, 100000, 2048)
+    assert long_need > need  # rows longer than a unit's share need candidate slots
+    assert _prefill(L, max_ctx=100000, ws_bytes=need) == CAP
+    assert _prefill(L, R=9000) == ARG  # more rows than one call takes
+    assert L.idx_fp4_prefill_workspace_bytes(0, 100, 64, 4096, 2048) == 0
+    assert L.idx_fp4_prefill_workspace_bytes(2, 100, 48, 4096, 2048) == 0

@@ -197,11 +197,11 @@ def test_decode_schedule_invariants():
     from fp4_sparse_attention_mxfp4_gb300 import _lib  # noqa: F401
     ctx = np.array([131072, 5, 0, 70000, 128, 129, 1, 262144], np.int32)
     t = dev(ctx)
-    sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(16), dtype=torch.uint8, device="cuda")
+    sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(16, 262144), dtype=torch.uint8, device="cuda")
     fx.idx_fp4_build_decode_schedule(t, 16, 262144, sched)
     torch.cuda.synchronize()
     s = sched.cpu().numpy().view(np.int32)
-    magic, ctas, batch, max_batch, num_units, total_tiles, per = s[:7]
+    magic, ctas, batch, max_batch, num_units, total_tiles, per, units_cap = s[:8]
     assert batch == 8 and max_batch == 16
     assert ctas == torch.cuda.get_device_properties(0).multi_processor_count
     cta_first = s[8:8 + 1024]
@@ -219,9 +219,9 @@ def test_decode_schedule_invariants():
             row, table, kb, ke, nq, slot = units[ui][:6]
             covered[row].append((kb, ke, ui))
             tiles += -(-(ke - kb) // 128)
-            assert kb % 128 == 0 and nq == 1 and table == row
+            assert kb % 128 == 0 and nq == 1 and table == row and ke - kb <= 16384
             assert (slot == -1) == (seq_units[row] == 1)
-        assert tiles <= per
+        assert tiles <= per * (-(-total_tiles // (ctas * 128)))
     assert cta_first[ctas - 1] + cta_count[ctas - 1] == num_units
     for b in range(8):
         r = sorted(covered[b])

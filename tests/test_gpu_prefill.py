@@ -44,14 +44,15 @@ class PrefillRun:
         fx.idx_fp4_quant_and_cache(bf16_dev(case.k_bf16[:0]), dev(np.zeros(0, np.int32)), self.kv_p, self.kv_s,
                                    q_bf16=bf16_dev(q), q_packed=qp, q_scale=qs)
         bt = dev(self.bt_all[st.requests])
-        ws = torch.zeros(fx.idx_fp4_prefill_workspace_bytes(len(st.requests), R, H), dtype=torch.uint8,
-                         device="cuda")
+        max_ctx = max(int(st.ctx_lens.max()), 1)
+        ws = torch.zeros(fx.idx_fp4_prefill_workspace_bytes(len(st.requests), R, H, max_ctx, case.topk),
+                         dtype=torch.uint8, device="cuda")
         idx = torch.full((R, case.topk), -7, dtype=torch.int32, device="cuda")
         val = torch.full((R, case.topk), 7.0, dtype=torch.float32, device="cuda")
         width = max(int(st.row_ends.max()), 1)
         lg = torch.full((R, width), float("nan"), dtype=torch.float32, device="cuda") if self.debug else None
         fx.idx_fp4_prefill_logits_topk(qp, qs, dev(w), self.kv_p, self.kv_s, bt, dev(st.ctx_lens), dev(st.cu_seqlens),
-                                       dev(st.row_ends), case.topk, ws, idx, val, logits_debug=lg,
+                                       dev(st.row_ends), case.topk, max_ctx, ws, idx, val, logits_debug=lg,
                                        status=self.status)
         torch.cuda.synchronize()
         return q, w, qp, qs, idx.cpu().numpy(), val.cpu().numpy(), (lg.cpu().numpy() if lg is not None else None)
