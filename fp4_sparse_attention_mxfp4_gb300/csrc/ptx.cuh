@@ -18,6 +18,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Shared-memory reduction with an explicit shared address (never a generic atomic).
+__device__ __forceinline__ void smem_red_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
 // ---- mbarrier ---------------------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

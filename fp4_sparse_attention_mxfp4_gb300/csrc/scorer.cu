@@ -70,7 +70,7 @@ struct ScorerCfg {
   static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * ACC + 6;
   static constexpr uint32_t OFF_BAR = OFF_SCR + 64 * 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
   static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM");
   static_assert(UNIT_BYTES % 16 == 0, "bulk copies need 16-byte sizes");
 };
@@ -189,13 +189,14 @@ template <int H, int Q>
 __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(const __grid_constant__ ScorerParams p) {
   using C = ScorerCfg<H, Q>;
   constexpr int N = C::N, ACC = C::ACC, STAGES = C::STAGES;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // The dynamic shared memory is used through this base directly: pointers derived from it keep
+  // the shared state space, so accesses compile to shared-memory instructions.
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // Schedule checks (uniform across the grid; nothing is allocated yet).
   const UnitIter it = unit_range(p);
-  if (!it.ok) {
+  if (!it.ok || (smem_addr(smem) & 1023u) != 0u) {
     if (tid == 0 && blockIdx.x == 0) set_status(p.status, IDX_FP4_DEV_BAD_SCHEDULE);
     return;
   }
@@ -549,7 +550,7 @@ constexpr int kMergeThreads = 256;
 constexpr int kMergeCap = 20480;    // candidate entries held at once
 constexpr int kMergeKeep = kMaxTopk;
 constexpr size_t kMergeSmem = static_cast<size_t>(kMergeCap) * 8 + static_cast<size_t>(kMergeKeep) * 8 +
-                              8 * kHistWords * 4 + 2048 * 4 + 64 * 4 + 16 + 1024;
+                              8 * kHistWords * 4 + 2048 * 4 + 64 * 4 + 16;
 
 struct MergeParams {
   const void* sched;                 // decode: the schedule, else nullptr
@@ -566,8 +567,7 @@ struct MergeParams {
 };
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeParams mp) {
-  extern __shared__ uint8_t msm_raw[];
-  uint8_t* msm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(msm_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t msm[];
   uint2* buf = reinterpret_cast<uint2*>(msm);
   uint2* keep = buf + kMergeCap;
   uint32_t* hw = reinterpret_cast<uint32_t*>(keep + kMergeKeep);

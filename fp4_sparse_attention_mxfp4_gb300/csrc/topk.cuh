@@ -21,7 +21,7 @@ constexpr int kHistWords = 1024;
 
 __device__ __forceinline__ void hist16_add(uint32_t* h, uint32_t key) {
   const uint32_t bin = key >> 21;
-  atomicAdd(&h[bin >> 1], 1u << ((bin & 1u) * 16u));
+  smem_red_add(&h[bin >> 1], 1u << ((bin & 1u) * 16u));
 }
 
 // Group-wide search for the bin holding the need-th largest element (1-based) of a histogram of
@@ -63,7 +63,7 @@ __device__ __forceinline__ uint2 find_bin(const uint32_t* hist, int nb, uint32_t
 // per-warp packed level-1 histograms of exactly these keys; `hist` is 2048 words of scratch.
 // Returns (T, need): every key > T is selected, plus the first `need` keys equal to T.
 template <int NT, int NW_H, class KeyAt>
-__device__ uint2 radix_threshold(KeyAt key, int n, int kk, const uint32_t* hw, uint32_t* hist, uint32_t* sc,
+__device__ __forceinline__ uint2 radix_threshold(KeyAt key, int n, int kk, const uint32_t* hw, uint32_t* hist, uint32_t* sc,
                                  int tid, int bar) {
   for (int wd = tid; wd < kHistWords; wd += NT) {
     uint32_t lo = 0, hi = 0;
@@ -89,7 +89,7 @@ __device__ uint2 radix_threshold(KeyAt key, int n, int kk, const uint32_t* hw, u
     named_barrier_sync(bar, NT);
     for (int i = tid; i < n; i += NT) {
       const uint32_t u = key(i);
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+      if ((u & mask) == prefix) smem_red_add(&hist[(u >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
     }
     named_barrier_sync(bar, NT);
     r = find_bin<NT>(hist, nb, need, sc, tid, bar);
@@ -105,7 +105,7 @@ __device__ uint2 radix_threshold(KeyAt key, int n, int kk, const uint32_t* hw, u
 // dense from 0 in token order. Each warp scans one contiguous segment twice (count, emit).
 // Uses sc[0 .. 2*NW-1].
 template <int NT, class KeyAt, class Emit>
-__device__ void stable_emit(KeyAt key, int n, uint32_t thr, uint32_t need, uint32_t* sc, int tid, int bar,
+__device__ __forceinline__ void stable_emit(KeyAt key, int n, uint32_t thr, uint32_t need, uint32_t* sc, int tid, int bar,
                             Emit emit) {
   const int lane = tid & 31, w = tid >> 5;
   const int seg = ((n + NT - 1) / NT) * 32;
