@@ -62,6 +62,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   return true;
 }
 
+// Monotonic shared-memory counters (CTA scope): the producer side adds with release order, the
+// consumer side reads with acquire order.
+__device__ __forceinline__ void smem_add_release(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_load_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+
+// Wait until *p >= target; false after `limit_ns`.
+__device__ __forceinline__ bool smem_wait_geq(const uint32_t* p, uint32_t target, uint64_t limit_ns) {
+  if (smem_load_acquire(p) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (smem_load_acquire(p) < target) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
 // ---- bulk copies (1-D TMA) ----------------------------------------------------------------
 
 // Global -> shared, completion signalled on `bar` as transaction bytes. dst and src
@@ -162,6 +184,17 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 __device__ __forceinline__ void tmem_copy_sf_chunk(uint32_t taddr, uint32_t saddr) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(smem_desc(saddr, 0, 128))
                : "memory");
+}
+
+// Warp-collective TMEM store of four 32-bit cells per lane: lane i of the warp's 32-lane
+// quarter writes columns [taddr, taddr + 4) of its TMEM lane, then waits until the stores are
+// done (so that a following fence and barrier arrive publish them).
+__device__ __forceinline__ void tmem_store_x4_wait(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n"
+      "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+      "r"(a), "r"(b), "r"(c), "r"(d)
+      : "memory");
 }
 
 // Warp-collective TMEM load of 32-bit cells: lane i of the warp's 32-lane quarter reads N

@@ -44,35 +44,36 @@ constexpr uint32_t kEpiBarrier = 1;
 template <int H, int Q>
 struct ScorerCfg {
   static constexpr int N = H * Q;
-  static constexpr int ACC = N <= 64 ? 4 : 2;  // TMEM accumulator stages
-  static constexpr int STAGES = 8;             // tiles in flight; one producer warp per stage
-  static constexpr int MMA_WARP = STAGES;
-  static constexpr int THREADS = (STAGES + 1 + 4) * 32;
+  static constexpr int ACC = N <= 64 ? 6 : 2;  // TMEM accumulators (even: a tile's group is fixed by it)
+  static constexpr int STAGES = 12;            // tiles in flight; one stage warp per stage
+  static constexpr int EPI_WARP0 = STAGES;
+  static constexpr int EPI_WARPS = 8;          // two groups of four (one warp per lane quarter)
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int THREADS = (STAGES + EPI_WARPS) * 32;
   static constexpr int UCAP = unit_key_cap(Q);   // keys per unit and row (row buffer size)
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t SFA_COL = 256;            // ACC chunks of 4 columns
-  static constexpr uint32_t SFB_COL = 256 + 4 * 4;    // 2 chunks of 4 columns (unit parity)
-  static_assert(ACC * N <= 256, "accumulators fit below the scale columns");
+  static constexpr uint32_t SFA_COL = ACC * N;             // STAGES chunks of 4 columns
+  static constexpr uint32_t SFB_COL = SFA_COL + 4 * STAGES;  // 2 chunks of 4 columns (unit parity)
+  static_assert(ACC % 2 == 0, "tiles sharing an accumulator belong to one epilogue group");
+  static_assert(SFB_COL + 8 <= TMEM_COLS, "accumulators and scale chunks fit the allocation");
   static_assert(UCAP % kTileKeys == 0, "whole tiles per unit");
   // shared memory map (offsets from a 1024-byte aligned base)
   static constexpr uint32_t OFF_PACKED = 0;                              // [STAGES][4][128][16]
-  static constexpr uint32_t OFF_SCALE = OFF_PACKED + STAGES * 8192;      // [STAGES][2 pages][256]
-  static constexpr uint32_t OFF_SFA = OFF_SCALE + STAGES * 512;          // [STAGES][512] tensor-core layout
-  static constexpr uint32_t RAW_Q = Q * H * 64, RAW_QS = Q * H * 4, RAW_W = Q * H * 4;
-  static constexpr uint32_t UNIT_BYTES = RAW_Q + RAW_QS + RAW_W;
-  static constexpr uint32_t OFF_UNIT = OFF_SFA + STAGES * 512;           // [2][UNIT_BYTES]
-  static constexpr uint32_t OFF_QB = (OFF_UNIT + 2 * UNIT_BYTES + 1023) / 1024 * 1024;  // [2][4][N][16]
+  static constexpr uint32_t OFF_SFA = OFF_PACKED + STAGES * 8192;        // [STAGES][512] tensor-core layout
+  static constexpr uint32_t OFF_QB = OFF_SFA + STAGES * 512;             // [2][4][N][16]
   static constexpr uint32_t OFF_SFB = OFF_QB + 2 * N * 64;               // [2][512]
-  static constexpr uint32_t OFF_LG = OFF_SFB + 2 * 512;                  // [Q][UCAP] ordered keys
-  static constexpr uint32_t OFF_HW = OFF_LG + Q * UCAP * 4;              // [Q][4 warps][1024] packed counts
+  static constexpr uint32_t OFF_W = OFF_SFB + 2 * 512;                   // [2][N] head weights
+  static constexpr uint32_t OFF_LG = OFF_W + 2 * N * 4;                  // [Q][UCAP] ordered keys
+  static constexpr uint32_t OFF_HW = OFF_LG + Q * UCAP * 4;              // [Q][4 quarters][1024] packed counts
   static constexpr uint32_t OFF_HIST = OFF_HW + Q * 4 * kHistWords * 4;  // [2048]
   static constexpr uint32_t OFF_SCR = OFF_HIST + 2048 * 4;               // [64]
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + 2 * ACC + 6;
-  static constexpr uint32_t OFF_BAR = OFF_SCR + 64 * 4;
+  static constexpr uint32_t OFF_ACCREL = OFF_SCR + 64 * 4;               // [ACC] released-tile counters (x4)
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + ACC + 4;
+  static constexpr uint32_t OFF_BAR = (OFF_ACCREL + ACC * 4 + 7) / 8 * 8;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
   static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM");
-  static_assert(UNIT_BYTES % 16 == 0, "bulk copies need 16-byte sizes");
+  static_assert(OFF_LG % 16 == 0 && OFF_SFA % 16 == 0 && OFF_QB % 128 == 0, "operand and row-buffer alignment");
 };
 
 struct ScorerParams {
@@ -166,13 +167,19 @@ __device__ __forceinline__ bool cursor_advance(Cursor& c, int steps, const UnitI
   return c.i < it.count;
 }
 
-__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                             int32_t* status) {
+// Slow path of a wait: bounded spin; a timeout raises the CTA's abort flag and the status bit,
+// after which every later wait of the CTA returns at once.
+__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
   if (*abort_flag) return false;
   if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
   *abort_flag = 1;
   set_status(status, IDX_FP4_DEV_TIMEOUT);
   return false;
+}
+
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             int32_t* status) {
+  return mbar_try_wait(bar, parity) || wait_slow(bar, parity, abort_flag, status);
 }
 
 // Page id of the tile at cursor c: lane 0 reads the tile's first page, lane 1 its second (or -1
@@ -202,13 +209,11 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
   }
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* full_bar = bars;
-  uint64_t* empty_bar = bars + STAGES;
-  uint64_t* acc_full = bars + 2 * STAGES;
-  uint64_t* acc_empty = acc_full + ACC;
-  uint64_t* unit_full = acc_empty + ACC;
-  uint64_t* unit_empty = unit_full + 2;
-  uint64_t* q_free = unit_empty + 2;
+  uint64_t* full_bar = bars;                  // stage data landed (TMA transaction count)
+  uint64_t* empty_bar = bars + STAGES;        // stage consumed by its MMAs (tcgen05.commit)
+  uint64_t* acc_full = bars + 2 * STAGES;     // accumulator written (tcgen05.commit)
+  uint64_t* q_ready = acc_full + ACC;         // unit query operand in place (tcgen05.commit)
+  uint32_t* acc_rel = reinterpret_cast<uint32_t*>(smem + C::OFF_ACCREL);  // epilogue warps done, per accumulator
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -219,26 +224,40 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 128);
+      acc_rel[a] = 0u;
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&unit_full[i], 1);
-      mbar_init(&unit_empty[i], 1 + 128);
-      mbar_init(&q_free[i], 1);
-    }
+    mbar_init(&q_ready[0], 1);
+    mbar_init(&q_ready[1], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == C::MMA_WARP) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  {
+    uint32_t* hw = reinterpret_cast<uint32_t*>(smem + C::OFF_HW);
+    for (int x = tid; x < Q * 4 * kHistWords; x += C::THREADS) hw[x] = 0u;
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
   if (warp < STAGES) {
-    // ---------------- producers: warp p fills stage p with tiles p, p+8, p+16, ... -----------
+    // ---------------- stage warps: warp w streams tiles w, w+12, ... through stage w and issues
+    // their MMAs. Issue work is spread over twelve warps because a bulk copy or a tcgen05
+    // instruction occupies its issuing warp or thread for a long time; one stage per warp also
+    // keeps every wait on a barrier this warp alone advances.
     const int ps = warp;
     const uint64_t pol = policy_evict_first();
+    uint8_t* stage = smem + C::OFF_PACKED + ps * 8192;
+    uint8_t* sfa_s = smem + C::OFF_SFA + ps * 512;
+    const uint64_t a_desc = smem_desc(smem_addr(stage), 2048, 128);
+    const uint32_t sfa_t = tmem + C::SFA_COL + 4u * static_cast<uint32_t>(ps);
+    const uint32_t idesc0 = mxf4_idesc(128, N, 0), idesc2 = mxf4_idesc(128, N, 2);
+    // Scale plane words of this lane: the 16x4 row transpose puts rows l%16 + 16*b at byte b of
+    // word l%16, so lane l takes byte l/16 (rows l, l+64 of the tile) and byte 2 + l/16 (rows
+    // l+32, l+96) of each group's word; a tile row m goes to TMEM lane m%32, column m/32.
+    const uint32_t sel_lo = static_cast<uint32_t>(lane >> 4), sel_hi = sel_lo + 2u;
+    const uint32_t perm_lo = sel_lo | ((sel_lo + 4u) << 4), perm_hi = sel_hi | ((sel_hi + 4u) << 4);
     Cursor c{0, 0, 0, Unit{}};
     bool have = it.count > 0;
     if (have) {
@@ -246,23 +265,10 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
       c.nt = unit_tiles(c.u);
       have = cursor_advance(c, ps, it);
     }
-    int st = 0;  // warp 0 stages the unit inputs of every unit, in order
-    auto stage_unit = [&](int i) {
-      const Unit u = it.at(i);
-      const int par = i & 1;
-      uint8_t* dst = smem + C::OFF_UNIT + par * C::UNIT_BYTES;
-      if (i >= 2) bounded_wait(&unit_empty[par], ((i >> 1) - 1) & 1, abort_flag, p.status);
-      const uint32_t rq = u.nq * H * 64, rqs = u.nq * H * 4;
-      mbar_arrive_expect_tx(&unit_full[par], rq + 2 * rqs);
-      bulk_load(dst, p.q_packed + static_cast<int64_t>(u.row) * H * 64, rq, &unit_full[par]);
-      bulk_load(dst + C::RAW_Q, p.q_scale + static_cast<int64_t>(u.row) * H * 4, rqs, &unit_full[par]);
-      bulk_load(dst + C::RAW_Q + C::RAW_QS, p.weights + static_cast<int64_t>(u.row) * H, rqs, &unit_full[par]);
-    };
     int entry = have ? load_tile_page(p, c, lane) : -1;
     int f = ps;
+    int qnext = 0;  // next unit whose query operand this warp has waited for
     while (have) {
-      if (ps == 0 && lane == 0)
-        while (st <= c.i) stage_unit(st++);
       int pid0 = __shfl_sync(0xFFFFFFFFu, entry, 0);
       int pid1 = __shfl_sync(0xFFFFFFFFu, entry, 1);
       const bool has1 = pid1 != -1;
@@ -275,35 +281,69 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         if (lane == 0 && pid1 != -2) set_status(p.status, IDX_FP4_DEV_BAD_PAGE);
         pid1 = 0;
       }
+      // the previous tile's MMAs (and its scale copy) are done with the stage
+      if (lane == 0) {
+        bounded_wait(&empty_bar[ps], ((f / STAGES) & 1) ^ 1, abort_flag, p.status);
+        mbar_arrive_expect_tx(&full_bar[ps], (has1 ? 2u : 1u) * kPageBytes);
+      }
+      __syncwarp();
+      // lanes 0..3: group chunks of page 0; lanes 4..7: page 1. A page's chunk g lands at
+      // g * 2048 + page * 1024, which makes the stage a canonical no-swizzle K-major operand.
+      if (lane < 8 && (lane < 4 || has1)) {
+        const int pg = lane >> 2, k = lane & 3;
+        const int64_t pid = pg == 0 ? pid0 : pid1;
+        uint8_t* dst = stage + k * 2048 + pg * 1024;
+        const uint8_t* src = p.kv_packed + pid * kPageBytes + k * 1024;
+        if (p.stream_once)
+          bulk_load_evict_first(dst, src, 1024, &full_bar[ps], pol);
+        else
+          bulk_load(dst, src, 1024, &full_bar[ps]);
+      }
+      // scale bytes: plain loads, in flight together with the bulk copies
+      uint32_t w0[4], w1[4];
+      {
+        const uint32_t* s0 = reinterpret_cast<const uint32_t*>(p.kv_scale + static_cast<int64_t>(pid0) * kPageScaleBytes) + (lane & 15);
+        const uint32_t* s1 = reinterpret_cast<const uint32_t*>(p.kv_scale + static_cast<int64_t>(pid1 < 0 ? 0 : pid1) * kPageScaleBytes) + (lane & 15);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          w0[g] = __ldg(s0 + 16 * g);
+          w1[g] = has1 ? __ldg(s1 + 16 * g) : 0x7F7F7F7Fu;
+        }
+      }
       // the next tile of this stage: its page ids load while this one streams
       Cursor nc = c;
       const bool next = cursor_advance(nc, STAGES, it);
       const int next_entry = next ? load_tile_page(p, nc, lane) : -1;
-      if (lane == 0) {
-        bounded_wait(&empty_bar[ps], ((f / STAGES) & 1) ^ 1, abort_flag, p.status);
-        mbar_arrive_expect_tx(&full_bar[ps], (has1 ? 2u : 1u) * (kPageBytes + kPageScaleBytes));
+      {
+        const uint32_t c0 = __byte_perm(__byte_perm(w0[0], w0[1], perm_lo), __byte_perm(w0[2], w0[3], perm_lo), 0x5410);
+        const uint32_t c1 = __byte_perm(__byte_perm(w0[0], w0[1], perm_hi), __byte_perm(w0[2], w0[3], perm_hi), 0x5410);
+        const uint32_t c2 = __byte_perm(__byte_perm(w1[0], w1[1], perm_lo), __byte_perm(w1[2], w1[3], perm_lo), 0x5410);
+        const uint32_t c3 = __byte_perm(__byte_perm(w1[0], w1[1], perm_hi), __byte_perm(w1[2], w1[3], perm_hi), 0x5410);
+        *reinterpret_cast<uint4*>(sfa_s + lane * 16) = make_uint4(c0, c1, c2, c3);
       }
+      fence_proxy_async_smem();
       __syncwarp();
-      // lanes 0..3: group chunks of page 0; lane 4: page 0 scales; lanes 5..9: the same for page 1
-      if (lane < 10 && (lane < 5 || has1)) {
-        const int pg = lane < 5 ? 0 : 1, k = lane < 5 ? lane : lane - 5;
-        const int64_t pid = pg == 0 ? pid0 : pid1;
-        uint8_t* dst;
-        const uint8_t* src;
-        uint32_t bytes;
-        if (k < 4) {
-          dst = smem + C::OFF_PACKED + ps * 8192 + k * 2048 + pg * 1024;
-          src = p.kv_packed + pid * kPageBytes + k * 1024;
-          bytes = 1024;
-        } else {
-          dst = smem + C::OFF_SCALE + ps * 512 + pg * 256;
-          src = p.kv_scale + pid * kPageScaleBytes;
-          bytes = 256;
+      if (lane == 0) {
+        bounded_wait(&full_bar[ps], (f / STAGES) & 1, abort_flag, p.status);
+        while (qnext <= c.i) {
+          bounded_wait(&q_ready[qnext & 1], (qnext >> 1) & 1, abort_flag, p.status);
+          ++qnext;
         }
-        if (p.stream_once)
-          bulk_load_evict_first(dst, src, bytes, &full_bar[ps], pol);
-        else
-          bulk_load(dst, src, bytes, &full_bar[ps]);
+        const int a = f % ACC;
+        if (!*abort_flag && !smem_wait_geq(&acc_rel[a], 4u * static_cast<uint32_t>(f / ACC), kWaitLimitNs)) {
+          *abort_flag = 1;
+          set_status(p.status, IDX_FP4_DEV_TIMEOUT);
+        }
+        tc_fence_after_sync();
+        const int par = c.i & 1;
+        const uint32_t qb = smem_addr(smem + C::OFF_QB + par * (N * 64));
+        const uint32_t sfb = tmem + C::SFB_COL + 4u * static_cast<uint32_t>(par);
+        const uint32_t d = tmem + static_cast<uint32_t>(a * N);
+        tmem_copy_sf_chunk(sfa_t, smem_addr(sfa_s));
+        mma_mxf4(d, a_desc, smem_desc(qb, N * 16, 128), idesc0, sfa_t, sfb, 0u);
+        mma_mxf4(d, a_desc + (4096 >> 4), smem_desc(qb + 2 * N * 16, N * 16, 128), idesc2, sfa_t, sfb, 1u);
+        tc_commit(&empty_bar[ps]);
+        tc_commit(&acc_full[a]);
       }
       __syncwarp();
       c = nc;
@@ -311,126 +351,78 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
       entry = next_entry;
       f += STAGES;
     }
-    if (ps == 0 && lane == 0)
-      while (st < it.count) stage_unit(st++);
-    // After an abort the consumers stop waiting; drain this warp's copies before teardown.
-    if (lane == 0 && *abort_flag) {
-      if (f - STAGES >= 0) mbar_wait(&full_bar[ps], ((f - STAGES) / STAGES) & 1, kWaitLimitNs);
-      if (ps == 0)
-        for (int i = it.count - 2 < 0 ? 0 : it.count - 2; i < it.count; ++i)
-          mbar_wait(&unit_full[i & 1], (i >> 1) & 1, kWaitLimitNs);
-    }
-  } else if (warp == C::MMA_WARP) {
-    // ---------------- MMA issuer ----------------
-    int f = 0, t = 0;
-    for (int i = 0; i < it.count; ++i) {
-      const Unit u = it.at(i);
-      const int par = i & 1;
-      const uint8_t* raw = smem + C::OFF_UNIT + par * C::UNIT_BYTES;
-      uint8_t* qb = smem + C::OFF_QB + par * (N * 64);
-      uint8_t* sfb = smem + C::OFF_SFB + par * 512;
-      bounded_wait(&unit_full[par], (i >> 1) & 1, abort_flag, p.status);
-      if (lane == 0 && i >= 2) bounded_wait(&q_free[par], ((i >> 1) - 1) & 1, abort_flag, p.status);
-      __syncwarp();
-      // Plain [rows*H][64 B] query -> canonical K-major [4 chunks][N][16 B]; missing rows zeroed.
-      const int live = u.nq * H;
-      for (int cc = lane; cc < 4 * N; cc += 32) {
-        const int g = cc / N, n = cc % N;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (n < live) v = *reinterpret_cast<const uint4*>(raw + n * 64 + g * 16);
-        *reinterpret_cast<uint4*>(qb + g * N * 16 + n * 16) = v;
-      }
-      // Query scales -> tensor-core scale layout: row n at line n%32, word n/32.
-      for (int n = lane; n < 128; n += 32) {
-        uint32_t wv = 0x7F7F7F7Fu;
-        if (n < live) wv = *reinterpret_cast<const uint32_t*>(raw + C::RAW_Q + n * 4);
-        *reinterpret_cast<uint32_t*>(sfb + (n & 31) * 16 + (n >> 5) * 4) = wv;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&unit_empty[par]);
-        tc_fence_after_sync();
-        tmem_copy_sf_chunk(tmem + C::SFB_COL + 4 * par, smem_addr(sfb));
-      }
-      __syncwarp();
-      const int ntiles = unit_tiles(u);
-      for (int j = 0; j < ntiles; ++j, ++f, ++t) {
-        const int s = f % STAGES;
-        bounded_wait(&full_bar[s], (f / STAGES) & 1, abort_flag, p.status);
-        // Scale bytes of the two pages -> tensor-core layout; key m = 64*page + row lives in
-        // the cache at [page][group][(row % 16) * 4 + row / 16].
-        const uint8_t* sc = smem + C::OFF_SCALE + s * 512;
-        uint32_t w4[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int m = lane + 32 * jj;
-          const int pg = m >> 6, row = m & 63;
-          const uint8_t* b = sc + pg * 256 + scale_slot(row);
-          w4[jj] = static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[64]) << 8) |
-                   (static_cast<uint32_t>(b[128]) << 16) | (static_cast<uint32_t>(b[192]) << 24);
-        }
-        uint8_t* sfa = smem + C::OFF_SFA + s * 512;
-        *reinterpret_cast<uint4*>(sfa + lane * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int a = t % ACC;
-          bounded_wait(&acc_empty[a], ((t / ACC) & 1) ^ 1, abort_flag, p.status);
-          tc_fence_after_sync();
-          tmem_copy_sf_chunk(tmem + C::SFA_COL + 4 * a, smem_addr(sfa));
-          const uint32_t a_base = smem_addr(smem + C::OFF_PACKED + s * 8192);
-          const uint32_t b_base = smem_addr(qb);
-          const uint32_t d = tmem + a * N;
-          mma_mxf4(d, smem_desc(a_base, 2048, 128), smem_desc(b_base, N * 16, 128), mxf4_idesc(128, N, 0),
-                   tmem + C::SFA_COL + 4 * a, tmem + C::SFB_COL + 4 * par, 0u);
-          mma_mxf4(d, smem_desc(a_base + 4096, 2048, 128), smem_desc(b_base + 2 * N * 16, N * 16, 128),
-                   mxf4_idesc(128, N, 2), tmem + C::SFA_COL + 4 * a, tmem + C::SFB_COL + 4 * par, 1u);
-          tc_commit(&empty_bar[s]);
-          tc_commit(&acc_full[a]);
-        }
-        __syncwarp();
-      }
-      if (lane == 0) tc_commit(&q_free[par]);
-      __syncwarp();
-    }
-    if (lane == 0 && it.count > 0) {
-      const int i = it.count - 1;
-      mbar_wait(&q_free[i & 1], (i >> 1) & 1, kWaitLimitNs);
+    // Teardown waits for this warp's last copies and MMAs (they normally finished long ago).
+    if (lane == 0 && f - STAGES >= 0) {
+      mbar_wait(&full_bar[ps], ((f - STAGES) / STAGES) & 1, kWaitLimitNs);
+      mbar_wait(&empty_bar[ps], ((f - STAGES) / STAGES) & 1, kWaitLimitNs);
     }
     __syncwarp();
   } else {
     // ---------------- epilogue: head-weighted ReLU sum, row buffer, exact top-k ----------------
+    // Two groups of four warps (one per TMEM lane quarter) take alternate tiles; the epilogue also
+    // lays out each unit's query operand and weights, two units ahead.
+    const int e = warp - C::EPI_WARP0;
+    const int grp = e >> 2;                 // tile parity handled by this warp's group
     const int qtr = warp & 3;               // TMEM lane quarter of this warp
-    const int etid = qtr * 32 + lane;       // key row within the tile, and rank in the group
+    const int etid = e * 32 + lane;         // rank in the 256-thread epilogue group
+    const int krow = qtr * 32 + lane;       // key row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(qtr * 32) << 16;
     uint32_t* lg_base = reinterpret_cast<uint32_t*>(smem + C::OFF_LG);
     uint32_t* hw_base = reinterpret_cast<uint32_t*>(smem + C::OFF_HW);
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + C::OFF_HIST);
     uint32_t* scr = reinterpret_cast<uint32_t*>(smem + C::OFF_SCR);
-    int t = 0;
+    // Query heads of unit i -> canonical K-major [4 chunks][N][16 B] operand (rows past the unit's
+    // live rows zeroed), query scales -> the tensor core's scale layout (row n at line n%32, word
+    // n/32), weights -> plain floats; then one thread copies the scales to TMEM and commits.
+    // The buffers of parity i&1 are free: the unit that used them last has been fully consumed.
+    auto prep = [&](int i) {
+      const Unit u = it.at(i);
+      const int par = i & 1;
+      const int live = u.nq * H;
+      uint8_t* qb = smem + C::OFF_QB + par * (N * 64);
+      uint8_t* sfb = smem + C::OFF_SFB + par * 512;
+      float* wq = reinterpret_cast<float*>(smem + C::OFF_W) + par * N;
+      const uint8_t* qsrc = p.q_packed + static_cast<int64_t>(u.row) * H * 64;
+      for (int cc = etid; cc < 4 * N; cc += C::EPI_THREADS) {
+        const int g = cc / N, n = cc % N;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (n < live) v = __ldg(reinterpret_cast<const uint4*>(qsrc + n * 64 + g * 16));
+        *reinterpret_cast<uint4*>(qb + g * N * 16 + n * 16) = v;
+      }
+      for (int n = etid; n < 128; n += C::EPI_THREADS) {
+        uint32_t wv = 0x7F7F7F7Fu;
+        if (n < live) wv = __ldg(reinterpret_cast<const uint32_t*>(p.q_scale + (static_cast<int64_t>(u.row) * H + n) * 4));
+        *reinterpret_cast<uint32_t*>(sfb + (n & 31) * 16 + (n >> 5) * 4) = wv;
+      }
+      for (int x = etid; x < N; x += C::EPI_THREADS)
+        wq[x] = x < live ? __ldg(p.weights + static_cast<int64_t>(u.row) * H + x) : 0.f;
+      fence_proxy_async_smem();
+      named_barrier_sync(kEpiBarrier, C::EPI_THREADS);
+      if (etid == 0) {
+        tc_fence_after_sync();
+        tmem_copy_sf_chunk(tmem + C::SFB_COL + 4u * static_cast<uint32_t>(par), smem_addr(sfb));
+        tc_commit(&q_ready[par]);
+      }
+    };
+    if (it.count > 0) prep(0);
+    if (it.count > 1) prep(1);
+    int t0 = 0;
     for (int i = 0; i < it.count; ++i) {
       const Unit u = it.at(i);
       const int upar = i & 1;
-      const float* wsm = reinterpret_cast<const float*>(smem + C::OFF_UNIT + upar * C::UNIT_BYTES + C::RAW_Q +
-                                                        C::RAW_QS);
-      // this warp's histograms start empty (the previous unit's selection ended with a barrier)
-#pragma unroll
-      for (int r = 0; r < Q; ++r)
-        for (int wd = lane; wd < kHistWords; wd += 32) hw_base[(r * 4 + qtr) * kHistWords + wd] = 0u;
-      __syncwarp();
-      bounded_wait(&unit_full[upar], (i >> 1) & 1, abort_flag, p.status);
+      const float* wsm = reinterpret_cast<const float*>(smem + C::OFF_W) + upar * N;
       int end[Q];
 #pragma unroll
       for (int r = 0; r < Q; ++r) {
-        int e = 0;
-        if (r < u.nq) e = p.row_ends != nullptr ? min(max(p.row_ends[u.row + r], 0), u.ke) : u.ke;
-        end[r] = e;
+        int ee = 0;
+        if (r < u.nq) ee = p.row_ends != nullptr ? min(max(p.row_ends[u.row + r], 0), u.ke) : u.ke;
+        end[r] = ee;
       }
       const int ntiles = unit_tiles(u);
-      for (int j = 0; j < ntiles; ++j, ++t) {
-        const int a = t % ACC;
-        bounded_wait(&acc_full[a], (t / ACC) & 1, abort_flag, p.status);
+      for (int j = (grp - t0) & 1; j < ntiles; j += 2) {
+        const int tt = t0 + j;
+        const int a = tt % ACC;
+        bounded_wait(&acc_full[a], static_cast<uint32_t>(tt / ACC) & 1u, abort_flag, p.status);
         tc_fence_after_sync();
         float logit[Q];
 #pragma unroll
@@ -476,8 +468,9 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
           logit[r] = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
         }
         tc_fence_before_sync();
-        mbar_arrive(&acc_empty[a]);
-        const int rel = j * kTileKeys + etid;  // < UCAP: a unit holds at most UCAP keys
+        __syncwarp();
+        if (lane == 0) smem_add_release(&acc_rel[a], 1u);
+        const int rel = j * kTileKeys + krow;  // < UCAP: a unit holds at most UCAP keys
         const int key = u.kb + rel;
 #pragma unroll
         for (int r = 0; r < Q; ++r) {
@@ -489,36 +482,39 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
             p.logits_debug[static_cast<int64_t>(u.row + r) * p.logits_stride + key] = logit[r];
         }
       }
-      mbar_arrive(&unit_empty[upar]);  // the unit's weights are no longer read
-      named_barrier_sync(kEpiBarrier, 128);
+      t0 += ntiles;
+      named_barrier_sync(kEpiBarrier, C::EPI_THREADS);
       // select each row: exactly min(k, valid keys) keys, in token order
       for (int r = 0; r < u.nq && r < Q; ++r) {
         const uint32_t* keys = lg_base + r * C::UCAP;
         const int nvalid = max(0, end[r] - u.kb);
         const int kk = min(p.topk, nvalid);
         uint2 th = make_uint2(0u, 0u);  // (T, need): T = 0 keeps every valid key
-        auto key_at = [keys](int x) { return keys[x]; };
+        auto load4 = [keys](int x) { return *reinterpret_cast<const uint4*>(keys + x); };
         if (kk < nvalid)
-          th = radix_threshold<128, 4>(key_at, nvalid, kk, hw_base + r * 4 * kHistWords, hist, scr, etid,
-                                       kEpiBarrier);
+          th = radix_threshold<C::EPI_THREADS, 4>(load4, nvalid, kk, hw_base + r * 4 * kHistWords, hist, scr, etid,
+                                                  kEpiBarrier);
         const int kb = u.kb;
         if (u.slot < 0) {
           const int64_t rowoff = static_cast<int64_t>(u.row + r) * p.topk;
           int32_t* oi = p.topk_idx + rowoff;
           float* ov = p.topk_val != nullptr ? p.topk_val + rowoff : nullptr;
-          stable_emit<128>(key_at, nvalid, th.x, th.y, scr, etid, kEpiBarrier, [=](int pos, int x, uint32_t kv) {
-            oi[pos] = kb + x;
-            if (ov != nullptr) ov[pos] = key_to_float(kv);
-          });
-          for (int e = kk + etid; e < p.topk; e += 128) {
-            oi[e] = -1;
-            if (ov != nullptr) ov[e] = -__int_as_float(0x7f800000);
+          stable_emit<C::EPI_THREADS>(load4, nvalid, th.x, th.y, scr, etid, kEpiBarrier,
+                                      [=](int pos, int x, uint32_t kv) {
+                                        oi[pos] = kb + x;
+                                        if (ov != nullptr) ov[pos] = key_to_float(kv);
+                                      });
+          for (int x = kk + etid; x < p.topk; x += C::EPI_THREADS) {
+            oi[x] = -1;
+            if (ov != nullptr) ov[x] = -__int_as_float(0x7f800000);
           }
         } else if (u.slot + r < p.cand_slots) {
           uint2* slot = p.cand + static_cast<int64_t>(u.slot + r) * static_cast<int64_t>(cand_slot_entries(p.topk));
           uint2* oc = slot + 2;
-          stable_emit<128>(key_at, nvalid, th.x, th.y, scr, etid, kEpiBarrier,
-                           [=](int pos, int x, uint32_t kv) { oc[pos] = make_uint2(kv, static_cast<uint32_t>(kb + x)); });
+          stable_emit<C::EPI_THREADS>(load4, nvalid, th.x, th.y, scr, etid, kEpiBarrier,
+                                      [=](int pos, int x, uint32_t kv) {
+                                        oc[pos] = make_uint2(kv, static_cast<uint32_t>(kb + x));
+                                      });
           // odd counts get one pad entry so every list is a whole number of 16-byte pairs; key 0 is
           // below every logit and never selected
           if (etid == 0) {
@@ -529,13 +525,20 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
           set_status(p.status, IDX_FP4_DEV_CAPACITY);
         }
       }
-      named_barrier_sync(kEpiBarrier, 128);
+      // the next unit counts into cleared histograms
+      for (int x = etid; x < Q * 4 * kHistWords; x += C::EPI_THREADS) hw_base[x] = 0u;
+      named_barrier_sync(kEpiBarrier, C::EPI_THREADS);
+      if (i + 2 < it.count) prep(i + 2);
     }
+    // Teardown waits for the last scale copies into TMEM (they normally finished long ago).
+    if (etid == 0)
+      for (int k = it.count - 2 < 0 ? 0 : it.count - 2; k < it.count; ++k)
+        mbar_wait(&q_ready[k & 1], (k >> 1) & 1, kWaitLimitNs);
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == C::MMA_WARP) {
+  if (warp == 0) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -546,11 +549,12 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
 // chunks): the row's candidate lists (each exactly its unit's top-min(k, keys), in token order)
 // are bulk-copied into shared memory in key order and the exact selection runs over them. Also
 // writes the all-padding output of decode sequences with no keys.
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 512;
 constexpr int kMergeCap = 20480;    // candidate entries held at once
 constexpr int kMergeKeep = kMaxTopk;
+constexpr int kMergeHists = 4;      // level-1 histograms (warp w counts into w % 4)
 constexpr size_t kMergeSmem = static_cast<size_t>(kMergeCap) * 8 + static_cast<size_t>(kMergeKeep) * 8 +
-                              8 * kHistWords * 4 + 2048 * 4 + 64 * 4 + 16;
+                              kMergeHists * kHistWords * 4 + 2048 * 4 + 64 * 4 + 64 * 4 + 16;
 
 struct MergeParams {
   const void* sched;                 // decode: the schedule, else nullptr
@@ -571,9 +575,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   uint2* buf = reinterpret_cast<uint2*>(msm);
   uint2* keep = buf + kMergeCap;
   uint32_t* hw = reinterpret_cast<uint32_t*>(keep + kMergeKeep);
-  uint32_t* hist = hw + 8 * kHistWords;
+  uint32_t* hist = hw + kMergeHists * kHistWords;
   uint32_t* scr = hist + 2048;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(scr + 64);
+  uint32_t* wsum = scr + 64;  // [0, 32): warp sums of the list scan, [32]: bytes of the round
+  uint64_t* bar = reinterpret_cast<uint64_t*>(wsum + 64);
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int topk = mp.topk;
   int first, nu, stride, kk;
@@ -619,28 +624,37 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   int kept = 0, next = 0, round = 0;
   bool timed_out = false;
   while (next < nu) {
-    // the lists that fit after the kept prefix
-    int total = kept, last = next;
-    uint32_t bytes = 0;
-    while (last < nu) {
-      const int ce = (list_count(last) + 1) & ~1;
-      if (total + ce > kMergeCap) break;
-      total += ce;
-      bytes += static_cast<uint32_t>(ce) * 8u;
-      ++last;
+    // The next kMergeThreads lists' sizes load in parallel; a block scan gives each list its
+    // offset after the kept prefix, the lists that fit form a prefix, and every thread bulk-copies
+    // its own list, so a round costs one dependent global read instead of one per list.
+    const int lx = next + tid;
+    const int ce = lx < nu ? (list_count(lx) + 1) & ~1 : 0;
+    int incl = ce;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += v;
     }
-    if (tid == 0 && bytes > 0) mbar_arrive_expect_tx(bar, bytes);
+    if (lane == 31) wsum[w] = incl;
     __syncthreads();
-    if (lane == 0 && bytes > 0) {
-      int off = kept;
-      for (int x = next; x < last; ++x) {
-        const int ce = (list_count(x) + 1) & ~1;
-        if ((x - next) % 8 == w && ce > 0)
-          bulk_load(buf + off, mp.cand + (first + static_cast<int64_t>(x) * stride) * slot_entries + 2,
-                    static_cast<uint32_t>(ce) * 8u, bar);
-        off += ce;
-      }
+    for (int w2 = 0; w2 < w; ++w2) incl += static_cast<int>(wsum[w2]);
+    const bool fits = lx < nu && kept + incl <= kMergeCap;
+    const int nfit = __syncthreads_count(fits);
+    if (nfit == 0) {  // cannot happen while kMergeCap >= 2 * (kMaxTopk + 1); never spin on it
+      if (tid == 0) set_status(mp.status, IDX_FP4_DEV_CAPACITY);
+      break;
     }
+    if (tid == nfit - 1) wsum[32] = static_cast<uint32_t>(incl);
+    __syncthreads();
+    const int last = next + nfit;
+    const int total = kept + static_cast<int>(wsum[32]);
+    const uint32_t bytes = static_cast<uint32_t>(total - kept) * 8u;
+    if (tid == 0 && bytes > 0) mbar_arrive_expect_tx(bar, bytes);
+    fence_proxy_async_smem();  // the buffer was last written and read by threads
+    __syncthreads();
+    if (fits && ce > 0)
+      bulk_load(buf + kept + incl - ce, mp.cand + (first + static_cast<int64_t>(lx) * stride) * slot_entries + 2,
+                static_cast<uint32_t>(ce) * 8u, bar);
     if (bytes > 0) {
       if (!mbar_wait(bar, round & 1, kWaitLimitNs)) timed_out = true;
       ++round;
@@ -651,17 +665,26 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     const bool final = next >= nu;
     const int kr = final ? kk : min(topk, n);
     // level-1 histograms, one per warp
-    for (int wd = lane; wd < kHistWords; wd += 32) hw[w * kHistWords + wd] = 0u;
-    __syncwarp();
-    for (int x = tid; x < n; x += kMergeThreads) hist16_add(hw + w * kHistWords, buf[x].x);
+    for (int wd = tid; wd < kMergeHists * kHistWords; wd += kMergeThreads) hw[wd] = 0u;
     __syncthreads();
-    auto key_at = [buf](int x) { return buf[x].x; };
+    // n is even and the buffer holds whole 16-byte pairs: read two entries per load
+    for (int x = 2 * tid; x < n; x += 2 * kMergeThreads) {
+      const uint4 v = *reinterpret_cast<const uint4*>(buf + x);
+      hist16_add(hw + (w % kMergeHists) * kHistWords, v.x);
+      hist16_add(hw + (w % kMergeHists) * kHistWords, v.z);
+    }
+    __syncthreads();
+    auto load4 = [buf](int x) {
+      const uint4 a = *reinterpret_cast<const uint4*>(buf + x);
+      const uint4 b = *reinterpret_cast<const uint4*>(buf + x + 2);
+      return make_uint4(a.x, a.z, b.x, b.z);
+    };
     uint2 th = make_uint2(0u, 0u);
-    if (kr < n) th = radix_threshold<kMergeThreads, 8>(key_at, n, kr, hw, hist, scr, tid, 1);
+    if (kr < n) th = radix_threshold<kMergeThreads, kMergeHists>(load4, n, kr, hw, hist, scr, tid, 1);
     if (final) {
       int32_t* oi = mp.topk_idx + orow;
       float* ov = mp.topk_val != nullptr ? mp.topk_val + orow : nullptr;
-      stable_emit<kMergeThreads>(key_at, n, th.x, th.y, scr, tid, 1, [=](int pos, int x, uint32_t kv) {
+      stable_emit<kMergeThreads>(load4, n, th.x, th.y, scr, tid, 1, [=](int pos, int x, uint32_t kv) {
         oi[pos] = static_cast<int32_t>(buf[x].y);
         if (ov != nullptr) ov[pos] = key_to_float(kv);
       });
@@ -670,7 +693,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         if (ov != nullptr) ov[e] = -__int_as_float(0x7f800000);
       }
     } else {
-      stable_emit<kMergeThreads>(key_at, n, th.x, th.y, scr, tid, 1,
+      stable_emit<kMergeThreads>(load4, n, th.x, th.y, scr, tid, 1,
                                  [=](int pos, int x, uint32_t) { keep[pos] = buf[x]; });
       kept = kr;
       for (int x = tid; x < kept; x += kMergeThreads) buf[x] = keep[x];
