@@ -67,9 +67,13 @@ struct ScorerCfg {
   static constexpr uint32_t OFF_HW = OFF_LG + Q * UCAP * 4;              // [Q][4 quarters][1024] packed counts
   static constexpr uint32_t OFF_HIST = OFF_HW + Q * 4 * kHistWords * 4;  // [2048]
   static constexpr uint32_t OFF_SCR = OFF_HIST + 2048 * 4;               // [64]
-  static constexpr uint32_t OFF_ACCREL = OFF_SCR + 64 * 4;               // [ACC] released-tile counters (x4)
-  static constexpr uint32_t NUM_BARS = 2 * STAGES + ACC + 4;
-  static constexpr uint32_t OFF_BAR = (OFF_ACCREL + ACC * 4 + 7) / 8 * 8;
+  // Release barriers per accumulator, used in turn. A stage warp's tiles all use one accumulator,
+  // STAGES / ACC of its tiles apart; with this many barriers the one it waits on has always seen
+  // the completion before the awaited one.
+  static constexpr int REL_RING = STAGES / ACC + 2;
+  static_assert(STAGES % ACC == 0, "a stage warp keeps to one accumulator");
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + ACC + ACC * REL_RING + 2;
+  static constexpr uint32_t OFF_BAR = OFF_SCR + 64 * 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
   static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM");
@@ -212,8 +216,12 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
   uint64_t* full_bar = bars;                  // stage data landed (TMA transaction count)
   uint64_t* empty_bar = bars + STAGES;        // stage consumed by its MMAs (tcgen05.commit)
   uint64_t* acc_full = bars + 2 * STAGES;     // accumulator written (tcgen05.commit)
-  uint64_t* q_ready = acc_full + ACC;         // unit query operand in place (tcgen05.commit)
-  uint32_t* acc_rel = reinterpret_cast<uint32_t*>(smem + C::OFF_ACCREL);  // epilogue warps done, per accumulator
+  // Release of an accumulator after its j-th tile: acc_rel[a * REL_RING + j % REL_RING]. Tiles of
+  // one accumulator are issued by different stage warps, so an issuer skips phases of the
+  // accumulator's sequence; spread over REL_RING barriers, the one it waits on is never two
+  // phases behind, which keeps parity waits exact.
+  uint64_t* acc_rel = acc_full + ACC;
+  uint64_t* q_ready = acc_rel + ACC * C::REL_RING;  // unit query operand in place (tcgen05.commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -222,10 +230,8 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int a = 0; a < ACC; ++a) {
-      mbar_init(&acc_full[a], 1);
-      acc_rel[a] = 0u;
-    }
+    for (int a = 0; a < ACC; ++a) mbar_init(&acc_full[a], 1);
+    for (int x = 0; x < ACC * C::REL_RING; ++x) mbar_init(&acc_rel[x], 4);
     mbar_init(&q_ready[0], 1);
     mbar_init(&q_ready[1], 1);
     *abort_flag = 0;
@@ -329,11 +335,10 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
           bounded_wait(&q_ready[qnext & 1], (qnext >> 1) & 1, abort_flag, p.status);
           ++qnext;
         }
-        const int a = f % ACC;
-        if (!*abort_flag && !smem_wait_geq(&acc_rel[a], 4u * static_cast<uint32_t>(f / ACC), kWaitLimitNs)) {
-          *abort_flag = 1;
-          set_status(p.status, IDX_FP4_DEV_TIMEOUT);
-        }
+        const int a = f % ACC, jf = f / ACC;
+        if (jf >= 1)  // the accumulator's previous tile has been read out
+          bounded_wait(&acc_rel[a * C::REL_RING + (jf - 1) % C::REL_RING],
+                       static_cast<uint32_t>((jf - 1) / C::REL_RING) & 1u, abort_flag, p.status);
         tc_fence_after_sync();
         const int par = c.i & 1;
         const uint32_t qb = smem_addr(smem + C::OFF_QB + par * (N * 64));
@@ -445,6 +450,25 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
               s6 = fmaf(wb.z, fmaxf(v[h + 6], 0.f), s6);
               s7 = fmaf(wb.w, fmaxf(v[h + 7], 0.f), s7);
             }
+          } else if constexpr (H % 64 == 0) {
+#pragma unroll
+            for (int cc = 0; cc < H; cc += 64) {
+              float v[64];
+              tmem_load_2x32(col + cc, col + cc + 32, v);
+#pragma unroll
+              for (int h = 0; h < 64; h += 8) {
+                const float4 wa = *reinterpret_cast<const float4*>(wsm + r * H + cc + h);
+                const float4 wb = *reinterpret_cast<const float4*>(wsm + r * H + cc + h + 4);
+                s0 = fmaf(wa.x, fmaxf(v[h], 0.f), s0);
+                s1 = fmaf(wa.y, fmaxf(v[h + 1], 0.f), s1);
+                s2 = fmaf(wa.z, fmaxf(v[h + 2], 0.f), s2);
+                s3 = fmaf(wa.w, fmaxf(v[h + 3], 0.f), s3);
+                s4 = fmaf(wb.x, fmaxf(v[h + 4], 0.f), s4);
+                s5 = fmaf(wb.y, fmaxf(v[h + 5], 0.f), s5);
+                s6 = fmaf(wb.z, fmaxf(v[h + 6], 0.f), s6);
+                s7 = fmaf(wb.w, fmaxf(v[h + 7], 0.f), s7);
+              }
+            }
           } else {
 #pragma unroll
             for (int cc = 0; cc < H; cc += 32) {
@@ -469,7 +493,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) smem_add_release(&acc_rel[a], 1u);
+        if (lane == 0) mbar_arrive(&acc_rel[a * C::REL_RING + (tt / ACC) % C::REL_RING]);
         const int rel = j * kTileKeys + krow;  // < UCAP: a unit holds at most UCAP keys
         const int key = u.kb + rel;
 #pragma unroll
@@ -489,21 +513,18 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         const uint32_t* keys = lg_base + r * C::UCAP;
         const int nvalid = max(0, end[r] - u.kb);
         const int kk = min(p.topk, nvalid);
-        uint2 th = make_uint2(0u, 0u);  // (T, need): T = 0 keeps every valid key
         auto load4 = [keys](int x) { return *reinterpret_cast<const uint4*>(keys + x); };
-        if (kk < nvalid)
-          th = radix_threshold<C::EPI_THREADS, 4>(load4, nvalid, kk, hw_base + r * 4 * kHistWords, hist, scr, etid,
-                                                  kEpiBarrier);
+        uint32_t* hw_r = hw_base + r * 4 * kHistWords;
         const int kb = u.kb;
         if (u.slot < 0) {
           const int64_t rowoff = static_cast<int64_t>(u.row + r) * p.topk;
           int32_t* oi = p.topk_idx + rowoff;
           float* ov = p.topk_val != nullptr ? p.topk_val + rowoff : nullptr;
-          stable_emit<C::EPI_THREADS>(load4, nvalid, th.x, th.y, scr, etid, kEpiBarrier,
-                                      [=](int pos, int x, uint32_t kv) {
-                                        oi[pos] = kb + x;
-                                        if (ov != nullptr) ov[pos] = key_to_float(kv);
-                                      });
+          select_topk<C::EPI_THREADS, 4>(load4, nvalid, kk, hw_r, hist, scr, etid, kEpiBarrier,
+                                         [=](int pos, int x, uint32_t kv) {
+                                           oi[pos] = kb + x;
+                                           if (ov != nullptr) ov[pos] = key_to_float(kv);
+                                         });
           for (int x = kk + etid; x < p.topk; x += C::EPI_THREADS) {
             oi[x] = -1;
             if (ov != nullptr) ov[x] = -__int_as_float(0x7f800000);
@@ -511,10 +532,10 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         } else if (u.slot + r < p.cand_slots) {
           uint2* slot = p.cand + static_cast<int64_t>(u.slot + r) * static_cast<int64_t>(cand_slot_entries(p.topk));
           uint2* oc = slot + 2;
-          stable_emit<C::EPI_THREADS>(load4, nvalid, th.x, th.y, scr, etid, kEpiBarrier,
-                                      [=](int pos, int x, uint32_t kv) {
-                                        oc[pos] = make_uint2(kv, static_cast<uint32_t>(kb + x));
-                                      });
+          select_topk<C::EPI_THREADS, 4>(load4, nvalid, kk, hw_r, hist, scr, etid, kEpiBarrier,
+                                         [=](int pos, int x, uint32_t kv) {
+                                           oc[pos] = make_uint2(kv, static_cast<uint32_t>(kb + x));
+                                         });
           // odd counts get one pad entry so every list is a whole number of 16-byte pairs; key 0 is
           // below every logit and never selected
           if (etid == 0) {
@@ -547,14 +568,14 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
 // ---------------------------------------------------------------------------------------------
 // Merge of split rows (decode sequences spread over several units, prefill rows cut into key
 // chunks): the row's candidate lists (each exactly its unit's top-min(k, keys), in token order)
-// are bulk-copied into shared memory in key order and the exact selection runs over them. Also
+// are copied into shared memory in key order and the exact selection runs over them. Also
 // writes the all-padding output of decode sequences with no keys.
 constexpr int kMergeThreads = 512;
 constexpr int kMergeCap = 20480;    // candidate entries held at once
 constexpr int kMergeKeep = kMaxTopk;
 constexpr int kMergeHists = 4;      // level-1 histograms (warp w counts into w % 4)
 constexpr size_t kMergeSmem = static_cast<size_t>(kMergeCap) * 8 + static_cast<size_t>(kMergeKeep) * 8 +
-                              kMergeHists * kHistWords * 4 + 2048 * 4 + 64 * 4 + 64 * 4 + 16;
+                              kMergeHists * kHistWords * 4 + 2048 * 4 + 64 * 4 + 64 * 4 + 2 * kMergeThreads * 4;
 
 struct MergeParams {
   const void* sched;                 // decode: the schedule, else nullptr
@@ -577,8 +598,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   uint32_t* hw = reinterpret_cast<uint32_t*>(keep + kMergeKeep);
   uint32_t* hist = hw + kMergeHists * kHistWords;
   uint32_t* scr = hist + 2048;
-  uint32_t* wsum = scr + 64;  // [0, 32): warp sums of the list scan, [32]: bytes of the round
-  uint64_t* bar = reinterpret_cast<uint64_t*>(wsum + 64);
+  uint32_t* wsum = scr + 64;  // [0, 32): warp sums of the list scan, [32]: entries of the round
+  uint32_t* loff = wsum + 64;  // per list of the round: first entry in the buffer
+  uint32_t* lcnt = loff + kMergeThreads;  // per list of the round: entries (even)
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int topk = mp.topk;
   int first, nu, stride, kk;
@@ -616,17 +638,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     const int64_t s = first + static_cast<int64_t>(i) * stride;
     return s < mp.cand_slots ? min(static_cast<int>(mp.cand[s * slot_entries].x), topk) : 0;
   };
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  int kept = 0, next = 0, round = 0;
-  bool timed_out = false;
+  int kept = 0, next = 0;
   while (next < nu) {
-    // The next kMergeThreads lists' sizes load in parallel; a block scan gives each list its
-    // offset after the kept prefix, the lists that fit form a prefix, and every thread bulk-copies
-    // its own list, so a round costs one dependent global read instead of one per list.
+    // The next kMergeThreads lists' sizes load in parallel and a block scan gives each list its
+    // offset after the kept prefix; the lists that fit form a prefix of them. A round thus costs
+    // one dependent global read instead of one per list.
     const int lx = next + tid;
     const int ce = lx < nu ? (list_count(lx) + 1) & ~1 : 0;
     int incl = ce;
@@ -645,19 +661,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       break;
     }
     if (tid == nfit - 1) wsum[32] = static_cast<uint32_t>(incl);
+    if (fits) {
+      loff[tid] = static_cast<uint32_t>(kept + incl - ce);
+      lcnt[tid] = static_cast<uint32_t>(ce);
+    }
     __syncthreads();
     const int last = next + nfit;
     const int total = kept + static_cast<int>(wsum[32]);
-    const uint32_t bytes = static_cast<uint32_t>(total - kept) * 8u;
-    if (tid == 0 && bytes > 0) mbar_arrive_expect_tx(bar, bytes);
-    fence_proxy_async_smem();  // the buffer was last written and read by threads
-    __syncthreads();
-    if (fits && ce > 0)
-      bulk_load(buf + kept + incl - ce, mp.cand + (first + static_cast<int64_t>(lx) * stride) * slot_entries + 2,
-                static_cast<uint32_t>(ce) * 8u, bar);
-    if (bytes > 0) {
-      if (!mbar_wait(bar, round & 1, kWaitLimitNs)) timed_out = true;
-      ++round;
+    // Every thread copies 16-byte pairs of every list: plain vector loads keep hundreds of
+    // requests in flight, where bulk copies issued by one warp would move one after another.
+    for (int li = 0; li < nfit; ++li) {
+      const uint4* src = reinterpret_cast<const uint4*>(mp.cand + (first + static_cast<int64_t>(next + li) * stride) *
+                                                                      slot_entries + 2);
+      uint4* dst = reinterpret_cast<uint4*>(buf + loff[li]);
+      const int pairs = static_cast<int>(lcnt[li]) >> 1;
+      for (int x = tid; x < pairs; x += kMergeThreads) dst[x] = src[x];
     }
     __syncthreads();
     next = last;
@@ -679,12 +697,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       const uint4 b = *reinterpret_cast<const uint4*>(buf + x + 2);
       return make_uint4(a.x, a.z, b.x, b.z);
     };
-    uint2 th = make_uint2(0u, 0u);
-    if (kr < n) th = radix_threshold<kMergeThreads, kMergeHists>(load4, n, kr, hw, hist, scr, tid, 1);
     if (final) {
       int32_t* oi = mp.topk_idx + orow;
       float* ov = mp.topk_val != nullptr ? mp.topk_val + orow : nullptr;
-      stable_emit<kMergeThreads>(load4, n, th.x, th.y, scr, tid, 1, [=](int pos, int x, uint32_t kv) {
+      select_topk<kMergeThreads, kMergeHists>(load4, n, kr, hw, hist, scr, tid, 1, [=](int pos, int x, uint32_t kv) {
         oi[pos] = static_cast<int32_t>(buf[x].y);
         if (ov != nullptr) ov[pos] = key_to_float(kv);
       });
@@ -693,8 +709,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         if (ov != nullptr) ov[e] = -__int_as_float(0x7f800000);
       }
     } else {
-      stable_emit<kMergeThreads>(load4, n, th.x, th.y, scr, tid, 1,
-                                 [=](int pos, int x, uint32_t) { keep[pos] = buf[x]; });
+      select_topk<kMergeThreads, kMergeHists>(load4, n, kr, hw, hist, scr, tid, 1,
+                                              [=](int pos, int x, uint32_t) { keep[pos] = buf[x]; });
       kept = kr;
       for (int x = tid; x < kept; x += kMergeThreads) buf[x] = keep[x];
       if (kept & 1) {
@@ -704,7 +720,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       __syncthreads();
     }
   }
-  if (timed_out && tid == 0) set_status(mp.status, IDX_FP4_DEV_TIMEOUT);
 }
 
 cudaError_t launch_merge(const MergeParams& mp, int rows, cudaStream_t stream) {
