@@ -19,8 +19,11 @@ from ._lib import (  # noqa: F401
     DEV_TIMEOUT,
     IDX_FP4_MAX_TOPK,
     IdxFp4Error,
+    STATIC_SCRATCH_BYTES,
     idx_fp4_build_decode_schedule,
     idx_fp4_decode_logits_topk,
+    idx_fp4_decode_logits_topk_static,
+    idx_fp4_decode_static_bytes,
     idx_fp4_decode_schedule_bytes,
     idx_fp4_decode_workspace_bytes,
     idx_fp4_prefill_logits_topk,

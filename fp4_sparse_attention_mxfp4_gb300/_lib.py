@@ -46,6 +46,9 @@ SIGNATURES = {
     "idx_fp4_decode_logits_topk": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _P, _SZ, _P,
                                           _SZ, _P, _P, _P, _I64, _P, _P]),
     "idx_fp4_prefill_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I64, _I32]),
+    "idx_fp4_decode_static_bytes": (_SZ, [_I32, _I64, _I32]),
+    "idx_fp4_decode_logits_topk_static": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I64, _P,
+                                                 _SZ, _P, _P, _P, _I64, _P, _P]),
     "idx_fp4_prefill_logits_topk": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _P, _P, _I32, _I32, _I32, _I32,
                                            _I64, _P, _SZ, _P, _P, _P, _I64, _P, _P]),
     "idx_fp4_error_string": (ctypes.c_char_p, [_I32]),
@@ -196,6 +199,57 @@ def idx_fp4_decode_logits_topk(q_packed, q_scale, weights, kv_packed, kv_scale, 
         _ptr(status), _stream(stream))
     _check("idx_fp4_decode_logits_topk", code)
 
+
+# Bytes of the library's fixed decode scratch array (per GPU).
+STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def idx_fp4_decode_static_bytes(batch: int, max_ctx: int, topk: int) -> int:
+    """Scratch bytes idx_fp4_decode_logits_topk_static needs for this batch on the current device."""
+    return int(lib().idx_fp4_decode_static_bytes(int(batch), int(max_ctx), int(topk)))
+
+
+def idx_fp4_decode_logits_topk_static(q_packed, q_scale, weights, kv_packed, kv_scale, block_tables, ctx_lens,
+                                      topk: int, max_ctx: int, sched, topk_idx, topk_val=None, logits_debug=None,
+                                      status=None, stream=None):
+    """Decode scoring + top-k without a workspace argument, for callers that cannot allocate device
+    memory: the candidate lists go to a fixed 16 MiB array the library keeps on each GPU. Same
+    outputs as idx_fp4_decode_logits_topk. `max_ctx` is the bound the schedule was built with.
+    Calls that overlap on the GPU share that array and race; the first call on a device should
+    come before any stream capture."""
+    _need(q_packed, "q_packed", torch.uint8, 3)
+    B, H = q_packed.shape[0], q_packed.shape[1]
+    _need(q_scale, "q_scale", torch.uint8, 3)
+    _need(weights, "weights", torch.float32, 2)
+    _need(kv_packed, "kv_packed", torch.uint8, 4)
+    _need(kv_scale, "kv_scale", torch.uint8, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    _need(sched, "sched", torch.uint8, 1)
+    _need(topk_idx, "topk_idx", torch.int32, 2)
+    if tuple(q_scale.shape) != (B, H, 4) or tuple(weights.shape) != (B, H) or q_packed.shape[2] != 64:
+        raise ValueError("q_packed [B,H,64], q_scale [B,H,4], weights [B,H] expected")
+    if block_tables.shape[0] < B or ctx_lens.shape[0] != B or tuple(topk_idx.shape) != (B, topk):
+        raise ValueError("block_tables [>=B, W], ctx_lens [B], topk_idx [B, topk] expected")
+    if topk_val is not None:
+        _need(topk_val, "topk_val", torch.float32, 2)
+        if tuple(topk_val.shape) != (B, topk):
+            raise ValueError("topk_val must be [B, topk]")
+    stride = 0
+    if logits_debug is not None:
+        _need(logits_debug, "logits_debug", torch.float32, 2)
+        stride = logits_debug.shape[1]
+    if status is not None:
+        _need(status, "status", torch.int32)
+    need = idx_fp4_decode_static_bytes(B, max_ctx, topk) if B > 0 else 0
+    if need > STATIC_SCRATCH_BYTES:
+        raise ValueError(f"batch {B} x max_ctx {max_ctx} at top-{topk} needs {need} scratch bytes, more than the "
+                         f"fixed {STATIC_SCRATCH_BYTES}; split the batch or use idx_fp4_decode_logits_topk")
+    code = lib().idx_fp4_decode_logits_topk_static(
+        _ptr(q_packed), _ptr(q_scale), _ptr(weights), _ptr(kv_packed), _ptr(kv_scale), kv_packed.shape[0],
+        _ptr(block_tables), block_tables.shape[1], _ptr(ctx_lens), B, H, int(topk), int(max_ctx), _ptr(sched),
+        sched.numel(), _ptr(topk_idx), _ptr(topk_val), _ptr(logits_debug), stride, _ptr(status), _stream(stream))
+    _check("idx_fp4_decode_logits_topk_static", code)
 
 def idx_fp4_prefill_workspace_bytes(num_requests: int, num_rows: int, num_heads: int, max_ctx: int,
                                     topk: int) -> int:

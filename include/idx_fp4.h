@@ -178,6 +178,36 @@ int idx_fp4_prefill_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale,
                                 size_t workspace_bytes, int32_t *topk_idx, float *topk_val, float *logits_debug,
                                 int64_t logits_stride, int32_t *status_dev, cudaStream_t stream);
 
+/* ---- Decode without a caller workspace -------------------------------------------------
+ * The pages have no counterpart of this call; it is here for callers that cannot allocate
+ * device memory (code running inside an allocator or memory-pool hook, an embedding runtime
+ * that owns every device allocation, or a path that must never wait on the allocator). It does
+ * what idx_fp4_decode_logits_topk does, with the candidate workspace taken from a fixed array
+ * of IDX_FP4_STATIC_SCRATCH_BYTES (16 MiB) that the library holds on every GPU it is loaded
+ * on until the process exits. It allocates nothing.
+ *   Arguments as for idx_fp4_decode_logits_topk, minus workspace/workspace_bytes, plus
+ *   max_ctx: the bound the schedule was built with (every ctx_lens[b] <= max_ctx).
+ *   Returns IDX_FP4_ERR_CAPACITY, launching nothing, when the candidate lists such a schedule
+ *   may need (idx_fp4_decode_static_bytes) exceed the array: split the batch or use the
+ *   workspace call.
+ * The first call on a device looks up the array's device address (and may load the library's
+ * device code); make that first call before any stream capture. All calls on a device share
+ * the one array, so calls that overlap on the GPU (other streams, other host threads) race and
+ * must be serialised by the caller. Nothing in the array needs to start at zero. */
+#define IDX_FP4_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* Scratch bytes idx_fp4_decode_logits_topk_static needs for this batch on the current device
+ * (host + a device attribute query; 0 for invalid arguments or a failed query). */
+size_t idx_fp4_decode_static_bytes(int batch, int64_t max_ctx, int topk);
+
+int idx_fp4_decode_logits_topk_static(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
+                                      const uint8_t *kv_packed, const uint8_t *kv_scale, int64_t num_pages,
+                                      const int32_t *block_tables, int block_table_stride,
+                                      const int32_t *ctx_lens_dev, int batch, int num_heads, int topk,
+                                      int64_t max_ctx, const void *sched_dev, size_t sched_bytes,
+                                      int32_t *topk_idx, float *topk_val, float *logits_debug,
+                                      int64_t logits_stride, int32_t *status_dev, cudaStream_t stream);
+
 /* Human-readable name of a return code. */
 const char *idx_fp4_error_string(int code);
 
