@@ -28,6 +28,7 @@
 //     row never reaches global memory (unless a debug buffer is passed).
 //   * Persistent grid, one CTA per SM; every on-chip wait is bounded and reports a timeout in the
 //     status word instead of hanging.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -567,15 +568,28 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
 
 // ---------------------------------------------------------------------------------------------
 // Merge of split rows (decode sequences spread over several units, prefill rows cut into key
-// chunks): the row's candidate lists (each exactly its unit's top-min(k, keys), in token order)
-// are copied into shared memory in key order and the exact selection runs over them. Also
-// writes the all-padding output of decode sequences with no keys.
-constexpr int kMergeThreads = 512;
-constexpr int kMergeCap = 20480;    // candidate entries held at once
-constexpr int kMergeKeep = kMaxTopk;
-constexpr int kMergeHists = 4;      // level-1 histograms (warp w counts into w % 4)
-constexpr size_t kMergeSmem = static_cast<size_t>(kMergeCap) * 8 + static_cast<size_t>(kMergeKeep) * 8 +
-                              kMergeHists * kHistWords * 4 + 2048 * 4 + 64 * 4 + 64 * 4 + 2 * kMergeThreads * 4;
+// chunks). A row's candidate lists (each exactly its unit's top-min(k, keys), in token order)
+// are merged by one cluster of kMergeG CTAs: CTA r takes the r-th share of the lists'
+// concatenation and streams it from L2 in every pass. Each CTA counts its share into local
+// radix histograms; the cluster sums them through distributed shared memory, so every CTA
+// arrives at the same threshold; each then writes its selected keys at an offset given by the
+// counts of the CTAs before it, which keeps the output in token order. Keys are first shifted
+// past the bits that all the row's candidates share, so that the first radix level spreads
+// them over its bins (the candidates are the top of the row and would otherwise fill a few
+// bins). Also writes the all-padding output of decode sequences with no keys.
+constexpr int kMergeG = 8;               // CTAs per row (one cluster)
+constexpr int kMergeThreads = 256;
+constexpr int kMergeNW = kMergeThreads / 32;
+constexpr int kMergeMaxLists = 2048;     // lists of one row (rows with more set CAPACITY)
+constexpr int kMergeCbuf = 4096;         // keys of the threshold bin a CTA lists
+constexpr int kMergeUnion = 4096;        // keys of the threshold bin gathered from the cluster
+constexpr int kMergeStage = 6144;        // candidates of a CTA's share staged in shared memory
+// shared memory (32-bit words): staged share [2 * kMergeStage] | local histogram [2048] | summed
+// histogram [2048] | bin list [kMergeCbuf] | gathered bin [kMergeUnion] | list starts
+// [kMergeMaxLists + 1] | scratch [64] | values pulled from the cluster [64] | published values
+// [8]. About 104 KB: two CTAs fit an SM, so every row's cluster is resident at once.
+constexpr size_t kMergeSmem =
+    (2 * kMergeStage + 2048 + 2048 + kMergeCbuf + kMergeUnion + kMergeMaxLists + 1 + 64 + 64 + 8) * 4;
 
 struct MergeParams {
   const void* sched;                 // decode: the schedule, else nullptr
@@ -591,18 +605,32 @@ struct MergeParams {
   int32_t* status;
 };
 
+// Order-preserving shift of the row's candidate keys past their p common leading bits (p = 32:
+// all keys equal). Real keys are nonzero, and so are their images.
+__device__ __forceinline__ uint32_t merge_xform(uint32_t k, uint32_t p) {
+  return p >= 32u ? 1u : ((k << p) | (p != 0u ? 1u : 0u));
+}
+
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeParams mp) {
-  extern __shared__ __align__(1024) uint8_t msm[];
-  uint2* buf = reinterpret_cast<uint2*>(msm);
-  uint2* keep = buf + kMergeCap;
-  uint32_t* hw = reinterpret_cast<uint32_t*>(keep + kMergeKeep);
-  uint32_t* hist = hw + kMergeHists * kHistWords;
-  uint32_t* scr = hist + 2048;
-  uint32_t* wsum = scr + 64;  // [0, 32): warp sums of the list scan, [32]: entries of the round
-  uint32_t* loff = wsum + 64;  // per list of the round: first entry in the buffer
-  uint32_t* lcnt = loff + kMergeThreads;  // per list of the round: entries (even)
-  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ __align__(16) uint32_t msm[];
+  uint2* stage = reinterpret_cast<uint2*>(msm);
+  uint32_t* hl = msm + 2 * kMergeStage;     // this CTA's histogram (read by the cluster)
+  uint32_t* hs = hl + 2048;                 // cluster sums
+  uint32_t* cbuf = hs + 2048;               // this CTA's keys of the threshold bin (read by the cluster)
+  uint32_t* ubuf = cbuf + kMergeCbuf;       // the cluster's keys of the threshold bin
+  uint32_t* lstart = ubuf + kMergeUnion;
+  uint32_t* sc = lstart + kMergeMaxLists + 1;
+  uint32_t* rv = sc + 64;                   // values pulled from every CTA of the cluster
+  uint32_t* pub = rv + 64;  // [0] AND, [1] OR, [2] keys > T, [3] keys == T, [4] listed keys,
+                            // [5] list complete, [6] slice total
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int row = static_cast<int>(blockIdx.x) / kMergeG;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int topk = mp.topk;
+  // Row setup: every CTA of the cluster reads the same row, so every early return below is
+  // taken by the whole cluster.
   int first, nu, stride, kk;
   if (mp.sched != nullptr) {
     const DecodeSchedHeader* h = static_cast<const DecodeSchedHeader*>(mp.sched);
@@ -615,12 +643,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     first = v.seq_first[row];
     stride = 1;
     kk = min(topk, ctx);
-    if (tid == 0 && mp.ctx_lens[row] >= 0 && mp.ctx_lens[row] != ctx) set_status(mp.status, IDX_FP4_DEV_BAD_SCHEDULE);
+    if (rank == 0 && tid == 0 && mp.ctx_lens[row] >= 0 && mp.ctx_lens[row] != ctx)
+      set_status(mp.status, IDX_FP4_DEV_BAD_SCHEDULE);
     if (nu == 0) {
-      for (int e = tid; e < topk; e += kMergeThreads) {
-        mp.topk_idx[static_cast<int64_t>(row) * topk + e] = -1;
-        if (mp.topk_val != nullptr) mp.topk_val[static_cast<int64_t>(row) * topk + e] = -__int_as_float(0x7f800000);
-      }
+      if (rank == 0)
+        for (int e = tid; e < topk; e += kMergeThreads) {
+          mp.topk_idx[static_cast<int64_t>(row) * topk + e] = -1;
+          if (mp.topk_val != nullptr) mp.topk_val[static_cast<int64_t>(row) * topk + e] = -__int_as_float(0x7f800000);
+        }
       return;
     }
   } else {
@@ -632,94 +662,427 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     kk = min(topk, rm.z);
   }
   if (nu <= 1) return;  // written by the scorer
-  const int64_t orow = static_cast<int64_t>(row) * topk;
+  if (nu > kMergeMaxLists) {
+    if (rank == 0 && tid == 0) set_status(mp.status, IDX_FP4_DEV_CAPACITY);
+    return;
+  }
   const int64_t slot_entries = static_cast<int64_t>(cand_slot_entries(topk));
-  auto list_count = [&](int i) {
-    const int64_t s = first + static_cast<int64_t>(i) * stride;
-    return s < mp.cand_slots ? min(static_cast<int>(mp.cand[s * slot_entries].x), topk) : 0;
+  auto list_base = [&](int li) { return mp.cand + (first + static_cast<int64_t>(li) * stride) * slot_entries + 2; };
+  // After a cluster barrier: rv[r * nv + j] = CTA r's pub[j0 + j], read by kMergeG * nv threads at once.
+  auto pull = [&](int j0, int nv) {
+    if (tid < kMergeG * nv) rv[tid] = cluster.map_shared_rank(pub, tid / nv)[j0 + tid % nv];
+    __syncthreads();
   };
-  int kept = 0, next = 0;
-  while (next < nu) {
-    // The next kMergeThreads lists' sizes load in parallel and a block scan gives each list its
-    // offset after the kept prefix; the lists that fit form a prefix of them. A round thus costs
-    // one dependent global read instead of one per list.
-    const int lx = next + tid;
-    const int ce = lx < nu ? (list_count(lx) + 1) & ~1 : 0;
-    int incl = ce;
+
+  // 1. List starts: block scan of the lists' sizes (every CTA).
+  {
+    constexpr int kPerMax = kMergeMaxLists / kMergeThreads;
+    const int per = (nu + kMergeThreads - 1) / kMergeThreads;
+    const int l0 = min(nu, tid * per);
+    uint32_t cnt[kPerMax];
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < kPerMax; ++j) {
+      const int li = l0 + j;
+      const int64_t sl = first + static_cast<int64_t>(li) * stride;
+      cnt[j] = (j < per && li < nu && sl < mp.cand_slots)
+                   ? static_cast<uint32_t>(min(static_cast<int>(mp.cand[sl * slot_entries].x), topk))
+                   : 0u;
+      s += cnt[j];
+    }
+    uint32_t incl = s;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
       if (lane >= off) incl += v;
     }
-    if (lane == 31) wsum[w] = incl;
+    if (lane == 31) sc[w] = incl;
+    for (int b = tid; b < 2048; b += kMergeThreads) hl[b] = 0u;
     __syncthreads();
-    for (int w2 = 0; w2 < w; ++w2) incl += static_cast<int>(wsum[w2]);
-    const bool fits = lx < nu && kept + incl <= kMergeCap;
-    const int nfit = __syncthreads_count(fits);
-    if (nfit == 0) {  // cannot happen while kMergeCap >= 2 * (kMaxTopk + 1); never spin on it
-      if (tid == 0) set_status(mp.status, IDX_FP4_DEV_CAPACITY);
-      break;
-    }
-    if (tid == nfit - 1) wsum[32] = static_cast<uint32_t>(incl);
-    if (fits) {
-      loff[tid] = static_cast<uint32_t>(kept + incl - ce);
-      lcnt[tid] = static_cast<uint32_t>(ce);
+    uint32_t run = incl - s;
+    for (int w2 = 0; w2 < w; ++w2) run += sc[w2];
+    if (tid == 0) lstart[0] = 0u;
+#pragma unroll
+    for (int j = 0; j < kPerMax; ++j) {
+      run += cnt[j];
+      if (j < per && l0 + j < nu) lstart[l0 + j + 1] = run;
     }
     __syncthreads();
-    const int last = next + nfit;
-    const int total = kept + static_cast<int>(wsum[32]);
-    // Every thread copies 16-byte pairs of every list: plain vector loads keep hundreds of
-    // requests in flight, where bulk copies issued by one warp would move one after another.
-    for (int li = 0; li < nfit; ++li) {
-      const uint4* src = reinterpret_cast<const uint4*>(mp.cand + (first + static_cast<int64_t>(next + li) * stride) *
-                                                                      slot_entries + 2);
-      uint4* dst = reinterpret_cast<uint4*>(buf + loff[li]);
-      const int pairs = static_cast<int>(lcnt[li]) >> 1;
-      for (int x = tid; x < pairs; x += kMergeThreads) dst[x] = src[x];
+  }
+  const int total = static_cast<int>(lstart[nu]);
+  const int share = (total + kMergeG - 1) / kMergeG;
+  const int p0 = min(total, rank * share), p1 = min(total, p0 + share);
+  // entry p of the row: list by binary search over the starts
+  auto entry = [&](int p) {
+    int lo = 0, hi = nu;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<int>(lstart[mid]) <= p) lo = mid; else hi = mid;
     }
-    __syncthreads();
-    next = last;
-    const int n = total;
-    const bool final = next >= nu;
-    const int kr = final ? kk : min(topk, n);
-    // level-1 histograms, one per warp
-    for (int wd = tid; wd < kMergeHists * kHistWords; wd += kMergeThreads) hw[wd] = 0u;
-    __syncthreads();
-    // n is even and the buffer holds whole 16-byte pairs: read two entries per load
-    for (int x = 2 * tid; x < n; x += 2 * kMergeThreads) {
-      const uint4 v = *reinterpret_cast<const uint4*>(buf + x);
-      hist16_add(hw + (w % kMergeHists) * kHistWords, v.x);
-      hist16_add(hw + (w % kMergeHists) * kHistWords, v.z);
-    }
-    __syncthreads();
-    auto load4 = [buf](int x) {
-      const uint4 a = *reinterpret_cast<const uint4*>(buf + x);
-      const uint4 b = *reinterpret_cast<const uint4*>(buf + x + 2);
-      return make_uint4(a.x, a.z, b.x, b.z);
-    };
-    if (final) {
-      int32_t* oi = mp.topk_idx + orow;
-      float* ov = mp.topk_val != nullptr ? mp.topk_val + orow : nullptr;
-      select_topk<kMergeThreads, kMergeHists>(load4, n, kr, hw, hist, scr, tid, 1, [=](int pos, int x, uint32_t kv) {
-        oi[pos] = static_cast<int32_t>(buf[x].y);
-        if (ov != nullptr) ov[pos] = key_to_float(kv);
-      });
-      for (int e = kk + tid; e < topk; e += kMergeThreads) {
-        oi[e] = -1;
-        if (ov != nullptr) ov[e] = -__int_as_float(0x7f800000);
+    return list_base(lo)[p - static_cast<int>(lstart[lo])];
+  };
+  // The share is staged in shared memory with independent loads, twelve in flight per thread;
+  // a share too large for the stage (rows of more than kMergeG * kMergeStage candidates) is
+  // read from global memory in every pass instead.
+  const bool staged = p1 - p0 <= kMergeStage;
+  if (staged) {
+    for (int b = p0; b < p1; b += 12 * kMergeThreads) {
+      uint2 v[12];
+#pragma unroll
+      for (int j = 0; j < 12; ++j) {
+        const int p = b + j * kMergeThreads + tid;
+        if (p < p1) v[j] = entry(p);
       }
+#pragma unroll
+      for (int j = 0; j < 12; ++j) {
+        const int p = b + j * kMergeThreads + tid;
+        if (p < p1) stage[p - p0] = v[j];
+      }
+    }
+    __syncthreads();
+  }
+  auto get = [&](int p) { return staged ? stage[p - p0] : entry(p); };
+  // Entries p .. p+3 (p - p0 a multiple of 4); entries at or past `end` come back as zero keys.
+  auto get4 = [&](int p, int end, uint2 (&e)[4]) {
+    if (staged) {
+      const uint4* q = reinterpret_cast<const uint4*>(stage + (p - p0));
+      const uint4 a = q[0], b = q[1];
+      e[0] = make_uint2(a.x, a.y);
+      e[1] = make_uint2(a.z, a.w);
+      e[2] = make_uint2(b.x, b.y);
+      e[3] = make_uint2(b.z, b.w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (p + j >= end) e[j] = make_uint2(0u, 0u);
     } else {
-      select_topk<kMergeThreads, kMergeHists>(load4, n, kr, hw, hist, scr, tid, 1,
-                                              [=](int pos, int x, uint32_t) { keep[pos] = buf[x]; });
-      kept = kr;
-      for (int x = tid; x < kept; x += kMergeThreads) buf[x] = keep[x];
-      if (kept & 1) {
-        if (tid == 0) buf[kept] = make_uint2(0u, 0xFFFFFFFFu);
-        kept += 1;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) e[j] = p + j < end ? entry(p + j) : make_uint2(0u, 0u);
+    }
+  };
+  // warp segments of this CTA's share (multiples of 4 entries), in token order
+  const int seg = ((p1 - p0 + kMergeNW - 1) / kMergeNW + 3) & ~3;
+  const int s0 = min(p1, p0 + w * seg), s1 = min(p1, s0 + seg);
+  const uint32_t lt = (1u << lane) - 1u;
+
+  // 2. Common leading bits of the row's keys.
+  {
+    uint32_t a = 0xFFFFFFFFu, o = 0u;
+    for (int p = p0 + tid; p < p1; p += kMergeThreads) {
+      const uint32_t k = get(p).x;
+      a &= k;
+      o |= k;
+    }
+    a = __reduce_and_sync(0xFFFFFFFFu, a);
+    o = __reduce_or_sync(0xFFFFFFFFu, o);
+    if (lane == 0) {
+      sc[2 * w] = a;
+      sc[2 * w + 1] = o;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t aa = 0xFFFFFFFFu, oo = 0u;
+      for (int w2 = 0; w2 < kMergeNW; ++w2) {
+        aa &= sc[2 * w2];
+        oo |= sc[2 * w2 + 1];
       }
-      __syncthreads();
+      pub[0] = aa;
+      pub[1] = oo;
     }
   }
+  cluster.sync();
+  pull(0, 2);
+  uint32_t pbits;
+  {
+    uint32_t aa = 0xFFFFFFFFu, oo = 0u;
+#pragma unroll
+    for (int r = 0; r < kMergeG; ++r) {
+      aa &= rv[2 * r];
+      oo |= rv[2 * r + 1];
+    }
+    pbits = (aa ^ oo) == 0u ? 32u : static_cast<uint32_t>(__clz(aa ^ oo));
+  }
+  // 3. Level 1: top 11 bits of the shifted keys.
+  for (int p = p0 + tid; p < p1; p += kMergeThreads) smem_red_add(&hl[merge_xform(get(p).x, pbits) >> 21], 1u);
+  __syncthreads();
+  cluster.sync();
+  // The level-1 bin of the threshold without moving whole histograms: CTA r sums bins
+  // [256 r, 256 r + 256) over the cluster (one remote word per thread and CTA) and publishes the
+  // slice's total; every CTA then finds the slice holding the kk-th largest key from the eight
+  // totals and reads only that slice's sums.
+  constexpr int kSlice = 2048 / kMergeG;
+  static_assert(kSlice == kMergeThreads, "one bin of the slice per thread");
+  {
+    uint32_t v[kMergeG];
+#pragma unroll
+    for (int r = 0; r < kMergeG; ++r) v[r] = cluster.map_shared_rank(hl, r)[rank * kSlice + tid];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int r = 0; r < kMergeG; ++r) sum += v[r];
+    hs[rank * kSlice + tid] = sum;
+    const uint32_t ws = __reduce_add_sync(0xFFFFFFFFu, sum);
+    if (lane == 0) sc[w] = ws;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t t = 0;
+      for (int w2 = 0; w2 < kMergeNW; ++w2) t += sc[w2];
+      pub[6] = t;
+    }
+  }
+  cluster.sync();
+  pull(6, 1);
+  // Fallback sum for the levels below, when the threshold bin is too large to gather.
+  auto cluster_sum = [&](int nb) {
+    for (int b0 = tid; b0 < nb; b0 += kMergeThreads) {
+      uint32_t v[kMergeG];
+#pragma unroll
+      for (int r = 0; r < kMergeG; ++r) v[r] = cluster.map_shared_rank(hl, r)[b0];
+      uint32_t sum = 0;
+#pragma unroll
+      for (int r = 0; r < kMergeG; ++r) sum += v[r];
+      hs[b0] = sum;
+    }
+    __syncthreads();
+  };
+  uint32_t thr = 0u, need = 0u;  // keep shifted key > thr, and the first `need` equal to it
+  uint32_t* gtw = sc + 16;      // per warp: keys > thr
+  uint32_t* eqw = sc + 32;      // per warp: keys == thr
+  if (kk < total) {
+    // slice holding the kk-th largest, scanning slices from the top
+    uint32_t above_slice = 0;
+    int sl = kMergeG - 1;
+    for (; sl > 0; --sl) {
+      if (above_slice + rv[sl] >= static_cast<uint32_t>(kk)) break;
+      above_slice += rv[sl];
+    }
+    // the slice's sums land in the gather buffer, which is unused until the gather below
+    ubuf[tid] = cluster.map_shared_rank(hs, sl)[sl * kSlice + tid];
+    __syncthreads();
+    const uint2 r1 = find_bin<kMergeThreads>(ubuf, kSlice, static_cast<uint32_t>(kk) - above_slice, sc, tid, 1);
+    const uint32_t bin = static_cast<uint32_t>(sl * kSlice) + r1.x;
+    need = static_cast<uint32_t>(kk) - above_slice - r1.y;
+    const uint32_t in_bin = ubuf[r1.x];  // the cluster's keys in the threshold bin
+    const bool listed = hl[bin] <= static_cast<uint32_t>(kMergeCbuf);
+    // one pass: keys above the bin per warp, keys in the bin listed as (low 21 bits | warp << 21)
+    if (tid == 0) sc[48] = 0u;
+    __syncthreads();
+    uint32_t above = 0;
+    for (int base = s0; base < s1; base += 128) {
+      const int p = base + 4 * lane;
+      uint2 e[4];
+      get4(p, s1, e);
+      uint32_t eqm = 0, t[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool in = p + j < s1;
+        t[j] = merge_xform(e[j].x, pbits);
+        above += (in && (t[j] >> 21) > bin) ? 1u : 0u;
+        eqm |= (in && (t[j] >> 21) == bin) ? (1u << j) : 0u;
+      }
+      uint32_t pre = 0, tot = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t bb = __ballot_sync(0xFFFFFFFFu, (eqm >> j) & 1u);
+        pre += __popc(bb & lt);
+        tot += __popc(bb);
+      }
+      if (listed && tot != 0u) {
+        uint32_t slot = 0;
+        if (lane == 0) slot = atomicAdd(&sc[48], tot);
+        slot = __shfl_sync(0xFFFFFFFFu, slot, 0) + pre;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if ((eqm >> j) & 1u) cbuf[slot++] = (t[j] & 0x1FFFFFu) | (static_cast<uint32_t>(w) << 21);
+      }
+    }
+    above = __reduce_add_sync(0xFFFFFFFFu, above);
+    if (lane == 0) gtw[w] = above;
+    __syncthreads();
+    const int m = static_cast<int>(sc[48]);
+    if (tid == 0) {
+      pub[4] = static_cast<uint32_t>(m);
+      pub[5] = listed ? 1u : 0u;
+    }
+    cluster.sync();  // every CTA's list is complete, and no CTA reads level-1 sums any more
+    pull(4, 2);
+    bool gather = in_bin <= static_cast<uint32_t>(kMergeUnion);
+    uint32_t base_of[kMergeG + 1];
+    base_of[0] = 0u;
+#pragma unroll
+    for (int r = 0; r < kMergeG; ++r) {
+      base_of[r + 1] = base_of[r] + rv[2 * r];
+      gather = gather && rv[2 * r + 1] != 0u;
+    }
+    uint32_t low = 0u;
+    if (gather) {
+      // The bin's keys of the whole cluster, gathered here with independent remote loads:
+      // levels 2 and 3 run inside this CTA.
+      for (int u = tid; u < static_cast<int>(in_bin); u += kMergeThreads) {
+        int r = 0;
+#pragma unroll
+        for (int q = 1; q < kMergeG; ++q) r += static_cast<uint32_t>(u) >= base_of[q] ? 1 : 0;
+        ubuf[u] = cluster.map_shared_rank(cbuf, r)[u - static_cast<int>(base_of[r])] & 0x1FFFFFu;
+      }
+#pragma unroll 1
+      for (int level = 0; level < 2; ++level) {
+        const int nb = level == 0 ? 2048 : 1024;
+        for (int x = tid; x < 2048; x += kMergeThreads) hl[x] = 0u;
+        __syncthreads();
+        for (int x = tid; x < static_cast<int>(in_bin); x += kMergeThreads) {
+          const uint32_t c = ubuf[x];
+          if (level == 0) smem_red_add(&hl[c >> 10], 1u);
+          else if ((c >> 10) == (low >> 10)) smem_red_add(&hl[c & 1023u], 1u);
+        }
+        __syncthreads();
+        const uint2 r = find_bin<kMergeThreads>(hl, nb, need, sc, tid, 1);
+        need -= r.y;
+        low |= level == 0 ? (r.x << 10) : r.x;
+      }
+    } else {
+      // Levels 2 and 3 through cluster sums (from the list, or from the share when it did not fit).
+#pragma unroll 1
+      for (int level = 0; level < 2; ++level) {
+        const int nb = level == 0 ? 2048 : 1024;
+        if (level == 1) cluster.sync();  // every CTA has finished reading the level-2 histograms
+        for (int b0 = tid; b0 < 2048; b0 += kMergeThreads) hl[b0] = 0u;
+        __syncthreads();
+        auto count = [&](uint32_t c) {
+          if (level == 0) smem_red_add(&hl[c >> 10], 1u);
+          else if ((c >> 10) == (low >> 10)) smem_red_add(&hl[c & 1023u], 1u);
+        };
+        if (listed) {
+          for (int x = tid; x < m; x += kMergeThreads) count(cbuf[x] & 0x1FFFFFu);
+        } else {
+          for (int p = p0 + tid; p < p1; p += kMergeThreads) {
+            const uint32_t t = merge_xform(get(p).x, pbits);
+            if ((t >> 21) == bin) count(t & 0x1FFFFFu);
+          }
+        }
+        __syncthreads();
+        cluster.sync();
+        cluster_sum(nb);
+        const uint2 r = find_bin<kMergeThreads>(hs, nb, need, sc, tid, 1);
+        need -= r.y;
+        low |= level == 0 ? (r.x << 10) : r.x;
+      }
+    }
+    thr = (bin << 21) | low;
+    // per-warp counts of keys > thr and == thr
+    if (tid < kMergeNW) eqw[tid] = 0u;
+    __syncthreads();
+    if (listed) {
+      for (int x = tid; x < m; x += kMergeThreads) {
+        const uint32_t c = cbuf[x];
+        const uint32_t ww = c >> 21, lo = c & 0x1FFFFFu;
+        if (lo > low)
+          smem_red_add(&gtw[ww], 1u);
+        else if (lo == low)
+          smem_red_add(&eqw[ww], 1u);
+      }
+    } else {
+      uint32_t g = 0, e = 0;
+      for (int base = s0; base < s1; base += 32) {
+        const int p = base + lane;
+        if (p < s1) {
+          const uint32_t t = merge_xform(get(p).x, pbits);
+          if ((t >> 21) == bin) {
+            g += (t & 0x1FFFFFu) > low ? 1u : 0u;
+            e += (t & 0x1FFFFFu) == low ? 1u : 0u;
+          }
+        }
+      }
+      g = __reduce_add_sync(0xFFFFFFFFu, g);
+      e = __reduce_add_sync(0xFFFFFFFFu, e);
+      if (lane == 0) {
+        gtw[w] += g;
+        eqw[w] = e;
+      }
+    }
+    __syncthreads();
+  } else {
+    // every candidate is kept
+    const uint32_t g = s1 > s0 ? static_cast<uint32_t>(s1 - s0) : 0u;
+    if (lane == 0) {
+      gtw[w] = g;
+      eqw[w] = 0u;
+    }
+    __syncthreads();
+  }
+  // 4. Offsets: this CTA's place among the cluster's, then each warp's place in the CTA.
+  if (tid == 0) {
+    uint32_t g = 0, e = 0;
+    for (int w2 = 0; w2 < kMergeNW; ++w2) {
+      g += gtw[w2];
+      e += eqw[w2];
+    }
+    pub[2] = g;
+    pub[3] = e;
+  }
+  cluster.sync();
+  pull(2, 2);
+  uint32_t out = 0, eq_before = 0;
+  for (int r = 0; r < rank; ++r) {
+    out += rv[2 * r];
+    eq_before += rv[2 * r + 1];
+  }
+  out += min(eq_before, need);
+  for (int w2 = 0; w2 < w; ++w2) {
+    out += gtw[w2] + (eq_before >= need ? 0u : min(eqw[w2], need - eq_before));
+    eq_before += eqw[w2];
+  }
+  // 5. Output pass in token order, four entries per lane.
+  int32_t* oi = mp.topk_idx + static_cast<int64_t>(row) * topk;
+  float* ov = mp.topk_val != nullptr ? mp.topk_val + static_cast<int64_t>(row) * topk : nullptr;
+  for (int base = s0; base < s1; base += 128) {
+    const int p = base + 4 * lane;
+    uint2 e[4];
+    get4(p, s1, e);
+    uint32_t gtm = 0, eqm = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool in = p + j < s1;
+      const uint32_t t = merge_xform(e[j].x, pbits);
+      gtm |= (in && t > thr) ? (1u << j) : 0u;
+      eqm |= (in && t == thr) ? (1u << j) : 0u;
+    }
+    uint32_t eq_lanes = 0, eq_chunk = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t bb = __ballot_sync(0xFFFFFFFFu, (eqm >> j) & 1u);
+      eq_lanes += __popc(bb & lt);
+      eq_chunk += __popc(bb);
+    }
+    uint32_t keepm = 0, rk = eq_before + eq_lanes;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool eq = (eqm >> j) & 1u;
+      keepm |= (((gtm >> j) & 1u) || (eq && rk < need)) ? (1u << j) : 0u;
+      rk += eq ? 1u : 0u;
+    }
+    uint32_t k_lanes = 0, k_chunk = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t bb = __ballot_sync(0xFFFFFFFFu, (keepm >> j) & 1u);
+      k_lanes += __popc(bb & lt);
+      k_chunk += __popc(bb);
+    }
+    uint32_t pos = out + k_lanes;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if ((keepm >> j) & 1u) {
+        oi[pos] = static_cast<int32_t>(e[j].y);
+        if (ov != nullptr) ov[pos] = key_to_float(e[j].x);
+        ++pos;
+      }
+    }
+    out += k_chunk;
+    eq_before += eq_chunk;
+  }
+  if (rank == 0)
+    for (int e = kk + tid; e < topk; e += kMergeThreads) {
+      oi[e] = -1;
+      if (ov != nullptr) ov[e] = -__int_as_float(0x7f800000);
+    }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 cudaError_t launch_merge(const MergeParams& mp, int rows, cudaStream_t stream) {
@@ -732,7 +1095,20 @@ cudaError_t launch_merge(const MergeParams& mp, int rows, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  merge_kernel<<<rows, kMergeThreads, kMergeSmem, stream>>>(mp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(rows) * kMergeG, 1, 1);
+  cfg.blockDim = dim3(kMergeThreads, 1, 1);
+  cfg.dynamicSmemBytes = kMergeSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kMergeG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, merge_kernel, mp);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
