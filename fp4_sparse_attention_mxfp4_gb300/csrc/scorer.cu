@@ -514,38 +514,45 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         const uint32_t* keys = lg_base + r * C::UCAP;
         const int nvalid = max(0, end[r] - u.kb);
         const int kk = min(p.topk, nvalid);
-        auto load4 = [keys](int x) { return *reinterpret_cast<const uint4*>(keys + x); };
         uint32_t* hw_r = hw_base + r * 4 * kHistWords;
         const int kb = u.kb;
-        if (u.slot < 0) {
+        const bool to_slot = u.slot >= 0;
+        if (to_slot && u.slot + r >= p.cand_slots) {
+          if (etid == 0) set_status(p.status, IDX_FP4_DEV_CAPACITY);
+          continue;
+        }
+        // The selection is emitted into this row's level-1 histogram area (free by then: 2048
+        // (key, index) pairs fit its 16 KB) and then copied out with coalesced stores.
+        uint2* sel = reinterpret_cast<uint2*>(hw_r);
+        uint2* spare = reinterpret_cast<uint2*>(hist) + lane;  // where keys not kept are written
+        select_topk<C::EPI_THREADS, 4>(keys, nvalid, kk, hw_r, hist, scr, etid, kEpiBarrier,
+                                       [=](bool keep, int pos, int x, uint32_t kv) {
+                                         *(keep ? sel + pos : spare) = make_uint2(kv, static_cast<uint32_t>(x));
+                                       });
+        if (!to_slot) {
           const int64_t rowoff = static_cast<int64_t>(u.row + r) * p.topk;
           int32_t* oi = p.topk_idx + rowoff;
           float* ov = p.topk_val != nullptr ? p.topk_val + rowoff : nullptr;
-          select_topk<C::EPI_THREADS, 4>(load4, nvalid, kk, hw_r, hist, scr, etid, kEpiBarrier,
-                                         [=](int pos, int x, uint32_t kv) {
-                                           oi[pos] = kb + x;
-                                           if (ov != nullptr) ov[pos] = key_to_float(kv);
-                                         });
-          for (int x = kk + etid; x < p.topk; x += C::EPI_THREADS) {
-            oi[x] = -1;
-            if (ov != nullptr) ov[x] = -__int_as_float(0x7f800000);
+          for (int x = etid; x < p.topk; x += C::EPI_THREADS) {
+            const uint2 e = x < kk ? sel[x] : make_uint2(0u, 0u);
+            oi[x] = x < kk ? kb + static_cast<int>(e.y) : -1;
+            if (ov != nullptr) ov[x] = x < kk ? key_to_float(e.x) : -__int_as_float(0x7f800000);
           }
-        } else if (u.slot + r < p.cand_slots) {
+        } else {
           uint2* slot = p.cand + static_cast<int64_t>(u.slot + r) * static_cast<int64_t>(cand_slot_entries(p.topk));
           uint2* oc = slot + 2;
-          select_topk<C::EPI_THREADS, 4>(load4, nvalid, kk, hw_r, hist, scr, etid, kEpiBarrier,
-                                         [=](int pos, int x, uint32_t kv) {
-                                           oc[pos] = make_uint2(kv, static_cast<uint32_t>(kb + x));
-                                         });
+          for (int x = etid; x < kk; x += C::EPI_THREADS) {
+            const uint2 e = sel[x];
+            oc[x] = make_uint2(e.x, static_cast<uint32_t>(kb) + e.y);
+          }
           // odd counts get one pad entry so every list is a whole number of 16-byte pairs; key 0 is
           // below every logit and never selected
           if (etid == 0) {
             if (kk & 1) oc[kk] = make_uint2(0u, 0xFFFFFFFFu);
             slot[0] = make_uint2(static_cast<uint32_t>(kk), 0u);
           }
-        } else if (etid == 0) {
-          set_status(p.status, IDX_FP4_DEV_CAPACITY);
         }
+        named_barrier_sync(kEpiBarrier, C::EPI_THREADS);  // the area is cleared or reused next
       }
       // the next unit counts into cleared histograms
       for (int x = etid; x < Q * 4 * kHistWords; x += C::EPI_THREADS) hw_base[x] = 0u;
