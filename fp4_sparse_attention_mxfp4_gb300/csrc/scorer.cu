@@ -40,22 +40,28 @@
 namespace idxfp4 {
 namespace {
 
-constexpr uint32_t kEpiBarrier = 1;
+constexpr uint32_t kEpiBarrier = 1;  // all epilogue warps
+constexpr uint32_t kSelBarrier = 2;  // the warps that run the unit-end selection
 
 template <int H, int Q>
 struct ScorerCfg {
   static constexpr int N = H * Q;
-  static constexpr int ACC = N <= 64 ? 6 : 2;  // TMEM accumulators (even: a tile's group is fixed by it)
+  // Epilogue groups of four warps (one per TMEM lane quarter) take tiles in turn; tiles that
+  // share an accumulator belong to one group (ACC a multiple of GROUPS). Three groups keep up
+  // with the stream at up to 64 columns per tile; wider tiles use two, with paired TMEM loads.
+  static constexpr int GROUPS = N <= 64 ? 3 : 2;
+  static constexpr int ACC = N <= 64 ? 6 : 2;  // TMEM accumulators
   static constexpr int STAGES = 12;            // tiles in flight; one stage warp per stage
   static constexpr int EPI_WARP0 = STAGES;
-  static constexpr int EPI_WARPS = 8;          // two groups of four (one warp per lane quarter)
+  static constexpr int EPI_WARPS = 4 * GROUPS;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int SEL_THREADS = 256;      // the unit-end selection runs on the first two groups
   static constexpr int THREADS = (STAGES + EPI_WARPS) * 32;
   static constexpr int UCAP = unit_key_cap(Q);   // keys per unit and row (row buffer size)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SFA_COL = ACC * N;             // STAGES chunks of 4 columns
   static constexpr uint32_t SFB_COL = SFA_COL + 4 * STAGES;  // 2 chunks of 4 columns (unit parity)
-  static_assert(ACC % 2 == 0, "tiles sharing an accumulator belong to one epilogue group");
+  static_assert(ACC % GROUPS == 0, "tiles sharing an accumulator belong to one epilogue group");
   static_assert(SFB_COL + 8 <= TMEM_COLS, "accumulators and scale chunks fit the allocation");
   static_assert(UCAP % kTileKeys == 0, "whole tiles per unit");
   // shared memory map (offsets from a 1024-byte aligned base)
@@ -368,7 +374,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
     // Two groups of four warps (one per TMEM lane quarter) take alternate tiles; the epilogue also
     // lays out each unit's query operand and weights, two units ahead.
     const int e = warp - C::EPI_WARP0;
-    const int grp = e >> 2;                 // tile parity handled by this warp's group
+    const int grp = e >> 2;                 // tiles t with t % GROUPS == grp are this group's
     const int qtr = warp & 3;               // TMEM lane quarter of this warp
     const int etid = e * 32 + lane;         // rank in the 256-thread epilogue group
     const int krow = qtr * 32 + lane;       // key row within the tile
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         end[r] = ee;
       }
       const int ntiles = unit_tiles(u);
-      for (int j = (grp - t0) & 1; j < ntiles; j += 2) {
+      for (int j = ((grp - t0) % C::GROUPS + C::GROUPS) % C::GROUPS; j < ntiles; j += C::GROUPS) {
         const int tt = t0 + j;
         const int a = tt % ACC;
         bounded_wait(&acc_full[a], static_cast<uint32_t>(tt / ACC) & 1u, abort_flag, p.status);
@@ -451,7 +457,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
               s6 = fmaf(wb.z, fmaxf(v[h + 6], 0.f), s6);
               s7 = fmaf(wb.w, fmaxf(v[h + 7], 0.f), s7);
             }
-          } else if constexpr (H % 64 == 0) {
+          } else if constexpr (H % 64 == 0 && C::GROUPS == 2) {
 #pragma unroll
             for (int cc = 0; cc < H; cc += 64) {
               float v[64];
@@ -509,8 +515,8 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
       }
       t0 += ntiles;
       named_barrier_sync(kEpiBarrier, C::EPI_THREADS);
-      // select each row: exactly min(k, valid keys) keys, in token order
-      for (int r = 0; r < u.nq && r < Q; ++r) {
+      // select each row: exactly min(k, valid keys) keys, in token order (first SEL_THREADS)
+      for (int r = 0; etid < C::SEL_THREADS && r < u.nq && r < Q; ++r) {
         const uint32_t* keys = lg_base + r * C::UCAP;
         const int nvalid = max(0, end[r] - u.kb);
         const int kk = min(p.topk, nvalid);
@@ -525,7 +531,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         // (key, index) pairs fit its 16 KB) and then copied out with coalesced stores.
         uint2* sel = reinterpret_cast<uint2*>(hw_r);
         uint2* spare = reinterpret_cast<uint2*>(hist) + lane;  // where keys not kept are written
-        select_topk<C::EPI_THREADS, 4>(keys, nvalid, kk, hw_r, hist, scr, etid, kEpiBarrier,
+        select_topk<C::SEL_THREADS, 4>(keys, nvalid, kk, hw_r, hist, scr, etid, kSelBarrier,
                                        [=](bool keep, int pos, int x, uint32_t kv) {
                                          *(keep ? sel + pos : spare) = make_uint2(kv, static_cast<uint32_t>(x));
                                        });
@@ -533,7 +539,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
           const int64_t rowoff = static_cast<int64_t>(u.row + r) * p.topk;
           int32_t* oi = p.topk_idx + rowoff;
           float* ov = p.topk_val != nullptr ? p.topk_val + rowoff : nullptr;
-          for (int x = etid; x < p.topk; x += C::EPI_THREADS) {
+          for (int x = etid; x < p.topk; x += C::SEL_THREADS) {
             const uint2 e = x < kk ? sel[x] : make_uint2(0u, 0u);
             oi[x] = x < kk ? kb + static_cast<int>(e.y) : -1;
             if (ov != nullptr) ov[x] = x < kk ? key_to_float(e.x) : -__int_as_float(0x7f800000);
@@ -541,7 +547,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         } else {
           uint2* slot = p.cand + static_cast<int64_t>(u.slot + r) * static_cast<int64_t>(cand_slot_entries(p.topk));
           uint2* oc = slot + 2;
-          for (int x = etid; x < kk; x += C::EPI_THREADS) {
+          for (int x = etid; x < kk; x += C::SEL_THREADS) {
             const uint2 e = sel[x];
             oc[x] = make_uint2(e.x, static_cast<uint32_t>(kb) + e.y);
           }
@@ -552,8 +558,9 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
             slot[0] = make_uint2(static_cast<uint32_t>(kk), 0u);
           }
         }
-        named_barrier_sync(kEpiBarrier, C::EPI_THREADS);  // the area is cleared or reused next
+        named_barrier_sync(kSelBarrier, C::SEL_THREADS);  // the area is reused by the next row
       }
+      named_barrier_sync(kEpiBarrier, C::EPI_THREADS);  // selection done before the areas are cleared
       // the next unit counts into cleared histograms
       for (int x = etid; x < Q * 4 * kHistWords; x += C::EPI_THREADS) hw_base[x] = 0u;
       named_barrier_sync(kEpiBarrier, C::EPI_THREADS);
