@@ -84,6 +84,17 @@ __device__ __forceinline__ bool smem_wait_geq(const uint32_t* p, uint32_t target
   return true;
 }
 
+// Warpgroup register re-split (all four warps of the warpgroup execute it). The decrease
+// returns registers to the block's pool; the increase waits until the pool holds them.
+template <uint32_t R>
+__device__ __forceinline__ void warpgroup_regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R) : "memory");
+}
+template <uint32_t R>
+__device__ __forceinline__ void warpgroup_regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R) : "memory");
+}
+
 // ---- bulk copies (1-D TMA) ----------------------------------------------------------------
 
 // Global -> shared, completion signalled on `bar` as transaction bytes. dst and src
@@ -257,6 +268,19 @@ __device__ __forceinline__ void tmem_load_2x32(uint32_t taddr0, uint32_t taddr1,
       : "memory");
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// acc (two fp32 lanes) += (w0, w1) * (x0, x1), one packed fma per lane (round to nearest).
+__device__ __forceinline__ void fma2(unsigned long long& acc, float w0, float w1, float x0, float x1) {
+  asm("{\n .reg .b64 w, x;\n mov.b64 w, {%1, %2};\n mov.b64 x, {%3, %4};\n fma.rn.f32x2 %0, w, x, %0;\n}\n"
+      : "+l"(acc)
+      : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
+
+__device__ __forceinline__ float2 unpack2(unsigned long long v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return make_float2(a, b);
 }
 
 }  // namespace idxfp4

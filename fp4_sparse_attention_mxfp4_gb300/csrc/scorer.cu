@@ -57,6 +57,17 @@ struct ScorerCfg {
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int SEL_THREADS = 256;      // the unit-end selection runs on the first two groups
   static constexpr int THREADS = (STAGES + EPI_WARPS) * 32;
+  // Registers per thread: the launch gets 65536 / THREADS (rounded down to 8); the stage
+  // warpgroups give registers back and the epilogue warpgroups take them, enough to hold a
+  // tile's 64 accumulator columns in flight at once. The split sums to the launch's share.
+  static constexpr uint32_t LAUNCH_REGS = (65536u / static_cast<uint32_t>(THREADS)) / 8u * 8u;
+  static constexpr bool RESPLIT = GROUPS == 3;  // two-group tiles already fit at the launch share
+  static constexpr uint32_t STAGE_REGS = RESPLIT ? 56u : LAUNCH_REGS;
+  static constexpr uint32_t EPI_REGS =
+      (LAUNCH_REGS * (STAGES + EPI_WARPS) - STAGE_REGS * STAGES) / EPI_WARPS / 8u * 8u;
+  static_assert(STAGES % 4 == 0 && EPI_WARPS % 4 == 0, "roles are whole warpgroups");
+  static_assert(STAGE_REGS * STAGES + EPI_REGS * EPI_WARPS <= LAUNCH_REGS * (STAGES + EPI_WARPS),
+                "the re-split fits the registers the block is launched with");
   static constexpr int UCAP = unit_key_cap(Q);   // keys per unit and row (row buffer size)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SFA_COL = ACC * N;             // STAGES chunks of 4 columns
@@ -180,7 +191,7 @@ __device__ __forceinline__ bool cursor_advance(Cursor& c, int steps, const UnitI
 
 // Slow path of a wait: bounded spin; a timeout raises the CTA's abort flag and the status bit,
 // after which every later wait of the CTA returns at once.
-__device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
+__device__ __forceinline__ bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
   if (*abort_flag) return false;
   if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
   *abort_flag = 1;
@@ -255,6 +266,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
   const uint32_t tmem = *tmem_slot;
 
   if (warp < STAGES) {
+    if constexpr (C::RESPLIT) warpgroup_regs_dec<C::STAGE_REGS>();
     // ---------------- stage warps: warp w streams tiles w, w+12, ... through stage w and issues
     // their MMAs. Issue work is spread over twelve warps because a bulk copy or a tcgen05
     // instruction occupies its issuing warp or thread for a long time; one stage per warp also
@@ -370,6 +382,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
     }
     __syncwarp();
   } else {
+    if constexpr (C::RESPLIT) warpgroup_regs_inc<C::EPI_REGS>();
     // ---------------- epilogue: head-weighted ReLU sum, row buffer, exact top-k ----------------
     // Two groups of four warps (one per TMEM lane quarter) take alternate tiles; the epilogue also
     // lays out each unit's query operand and weights, two units ahead.
@@ -457,7 +470,9 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
               s6 = fmaf(wb.z, fmaxf(v[h + 6], 0.f), s6);
               s7 = fmaf(wb.w, fmaxf(v[h + 7], 0.f), s7);
             }
-          } else if constexpr (H % 64 == 0 && C::GROUPS == 2) {
+          } else if constexpr (H % 64 == 0) {
+            // accumulator j holds heads j, j+8, ... in order; pairs of them share a packed fma
+            unsigned long long p01 = 0ull, p23 = 0ull, p45 = 0ull, p67 = 0ull;
 #pragma unroll
             for (int cc = 0; cc < H; cc += 64) {
               float v[64];
@@ -466,16 +481,15 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
               for (int h = 0; h < 64; h += 8) {
                 const float4 wa = *reinterpret_cast<const float4*>(wsm + r * H + cc + h);
                 const float4 wb = *reinterpret_cast<const float4*>(wsm + r * H + cc + h + 4);
-                s0 = fmaf(wa.x, fmaxf(v[h], 0.f), s0);
-                s1 = fmaf(wa.y, fmaxf(v[h + 1], 0.f), s1);
-                s2 = fmaf(wa.z, fmaxf(v[h + 2], 0.f), s2);
-                s3 = fmaf(wa.w, fmaxf(v[h + 3], 0.f), s3);
-                s4 = fmaf(wb.x, fmaxf(v[h + 4], 0.f), s4);
-                s5 = fmaf(wb.y, fmaxf(v[h + 5], 0.f), s5);
-                s6 = fmaf(wb.z, fmaxf(v[h + 6], 0.f), s6);
-                s7 = fmaf(wb.w, fmaxf(v[h + 7], 0.f), s7);
+                fma2(p01, wa.x, wa.y, fmaxf(v[h], 0.f), fmaxf(v[h + 1], 0.f));
+                fma2(p23, wa.z, wa.w, fmaxf(v[h + 2], 0.f), fmaxf(v[h + 3], 0.f));
+                fma2(p45, wb.x, wb.y, fmaxf(v[h + 4], 0.f), fmaxf(v[h + 5], 0.f));
+                fma2(p67, wb.z, wb.w, fmaxf(v[h + 6], 0.f), fmaxf(v[h + 7], 0.f));
               }
             }
+            const float2 a01 = unpack2(p01), a23 = unpack2(p23), a45 = unpack2(p45), a67 = unpack2(p67);
+            s0 = a01.x; s1 = a01.y; s2 = a23.x; s3 = a23.y;
+            s4 = a45.x; s5 = a45.y; s6 = a67.x; s7 = a67.y;
           } else {
 #pragma unroll
             for (int cc = 0; cc < H; cc += 32) {
