@@ -129,6 +129,18 @@ def test_decode_split_sequences_merge():
         _check_decode(run, ref)
 
 
+def test_decode_many_rows_merge():
+    # 16 split sequences, the merge's clusters all resident at once. Equal lengths keep every
+    # CTA's share of a row in shared memory; one long sequence among short ones has ~130 lists,
+    # more than the cluster stages, and is merged from global memory.
+    cases = [synth.decode_case("rows16_even", 31, [20000] * 16, 64, 2048),
+             synth.decode_case("rows16_long", 32, [200000] + [1500 + 97 * i for i in range(15)], 64, 2048)]
+    for case in cases:
+        run = DecodeRun(case).run()
+        ref = _oracle_side(case)
+        _check_decode(run, ref)
+
+
 def test_decode_config3_full():
     case = synth.decode_config(3)
     run = DecodeRun(case).run()
