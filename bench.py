@@ -294,34 +294,46 @@ def run_decode_timed(bench: DecodeBench, steps: int, warmup: int, dist, clock: C
 
 
 def run_decode_e2e(bench: DecodeBench, steps: int, warmup: int):
-    """Same step through the public API with host buffers: pinned host -> device copies of the
-    step's inputs, the three calls, and a device -> host read of the step's top-k."""
+    """Same step through the public API with host buffers: the step's inputs copied from pinned
+    host memory, the three calls, and a device -> host read of the step's top-k. The caller
+    keeps its inputs side by side in one pinned buffer (and the outputs in one device buffer),
+    so each direction is one copy."""
     import numpy as np
     torch, fx, case = bench.torch, bench.fx, bench.case
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     last = np.cumsum(case.ctx_lens) - 1
-    h_in = {
-        "k_new": pin(case.k_bf16[last].view(np.int16)), "slots": pin(case.all_slots()[last]),
-        "q": pin(case.q_bf16.view(np.int16)), "w": pin(case.w), "ctx": pin(case.ctx_lens),
-        "bt": pin(case.layout.block_tables),
+    arrays = {
+        "k_new": case.k_bf16[last].view(np.int16), "slots": case.all_slots()[last],
+        "q": case.q_bf16.view(np.int16), "w": case.w, "ctx": case.ctx_lens, "bt": case.layout.block_tables,
     }
-    d_in = {k: torch.empty_like(v, device="cuda") for k, v in h_in.items()}
-    h_idx = torch.empty(bench.topk_idx.shape, dtype=torch.int32).pin_memory()
-    h_val = torch.empty(bench.topk_val.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
-    d2h = h_idx.numel() * 4 + h_val.numel() * 4
+    offs, size = {}, 0
+    for name, a in arrays.items():
+        offs[name] = size
+        size += (a.nbytes + 255) // 256 * 256
+    h_in = torch.zeros(size, dtype=torch.uint8).pin_memory()
+    d_buf = torch.empty(size, dtype=torch.uint8, device="cuda")
+    d_in = {}
+    for name, a in arrays.items():
+        a = np.ascontiguousarray(a)
+        h_in.numpy()[offs[name]:offs[name] + a.nbytes] = a.reshape(-1).view(np.uint8)
+        dt = torch.from_numpy(a[:0]).dtype
+        d_in[name] = d_buf[offs[name]:offs[name] + a.nbytes].view(dt).view(a.shape)
+    B, k = bench.topk_idx.shape
+    d_out = torch.empty(B * k * 8, dtype=torch.uint8, device="cuda")
+    h_out = torch.empty(B * k * 8, dtype=torch.uint8).pin_memory()
+    out_idx = d_out[:B * k * 4].view(torch.int32).view(B, k)
+    out_val = d_out[B * k * 4:].view(torch.float32).view(B, k)
+    h2d = size
+    d2h = d_out.numel()
 
     def step():
-        for k, v in h_in.items():
-            d_in[k].copy_(v, non_blocking=True)
+        d_buf.copy_(h_in, non_blocking=True)
         fx.idx_fp4_quant_and_cache(d_in["k_new"], d_in["slots"], bench.kv_p, bench.kv_s, q_bf16=d_in["q"],
                                    q_packed=bench.q_packed, q_scale=bench.q_scale, status=bench.status)
         fx.idx_fp4_build_decode_schedule(d_in["ctx"], case.batch, bench.max_ctx, bench.sched, status=bench.status)
         fx.idx_fp4_decode_logits_topk(bench.q_packed, bench.q_scale, d_in["w"], bench.kv_p, bench.kv_s, d_in["bt"],
-                                      d_in["ctx"], case.topk, bench.sched, bench.ws, bench.topk_idx, bench.topk_val,
+                                      d_in["ctx"], case.topk, bench.sched, bench.ws, out_idx, out_val,
                                       status=bench.status)
-        h_idx.copy_(bench.topk_idx, non_blocking=True)
-        h_val.copy_(bench.topk_val, non_blocking=True)
+        h_out.copy_(d_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for _ in range(warmup):
@@ -331,6 +343,10 @@ def run_decode_e2e(bench: DecodeBench, steps: int, warmup: int):
         t0 = time.perf_counter()
         step()
         times.append(time.perf_counter() - t0)
+    # the read-back is the step's result: the same top-k as the device-resident run
+    got = h_out[:B * k * 4].view(torch.int32).view(B, k)
+    if not torch.equal(got, bench.topk_idx.cpu()):
+        raise RuntimeError("end-to-end top-k differs from the device-resident step")
     return statistics.mean(times), h2d, d2h
 
 

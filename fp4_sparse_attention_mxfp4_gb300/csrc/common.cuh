@@ -1,6 +1,9 @@
 // Layout constants, device status bits and the work-unit tables shared by the kernels.
 #pragma once
+#include <cuda_runtime.h>
+
 #include <cstdint>
+#include <utility>
 
 #include "idx_fp4.h"
 
@@ -174,6 +177,40 @@ __device__ __forceinline__ float key_to_float(uint32_t u) {
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
   if (status != nullptr) atomicOr(status, bits);
+}
+
+// Programmatic dependent launch. Every kernel of this library is launched with programmatic
+// stream serialization, so it may begin while the kernel before it in the stream is still
+// running, and starts with pdl_wait(): that returns once the preceding grid has completed and
+// its memory operations are visible (at once after anything that is not such a kernel). Only
+// then does it touch global memory, and only then pdl_trigger() lets the next kernel begin
+// launching. Since every kernel waits before it can complete, each completion implies its
+// predecessor's, and stream order holds as without the attribute; what is saved is the next
+// kernel's launch latency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with programmatic stream serialization (plus a cluster shape when cluster_x > 1).
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cluster_x > 1 ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace idxfp4

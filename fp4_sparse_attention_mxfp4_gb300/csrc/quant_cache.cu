@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(256) quant_and_cache_kernel(const uint16_t* __
                                                               uint8_t* kv_scale, int64_t num_pages,
                                                               const uint16_t* __restrict__ q, int64_t num_q_vec,
                                                               uint8_t* q_packed, uint8_t* q_scale, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -106,9 +108,8 @@ cudaError_t launch_quant_and_cache(const uint16_t* k, int64_t num_tokens, const 
   const int64_t blocks_needed = (vecs + 7) / 8;  // 8 warps per block
   const int blocks = static_cast<int>(blocks_needed < static_cast<int64_t>(num_sms) * 16 ? blocks_needed
                                                                                           : static_cast<int64_t>(num_sms) * 16);
-  quant_and_cache_kernel<<<blocks, 256, 0, stream>>>(k, num_tokens, slots, kv_packed, kv_scale, num_pages, q,
-                                                     num_q_vec, q_packed, q_scale, status);
-  return cudaGetLastError();
+  return launch_pdl(quant_and_cache_kernel, dim3(blocks), dim3(256), 0, stream, 1, k, num_tokens, slots, kv_packed,
+                    kv_scale, num_pages, q, num_q_vec, q_packed, q_scale, status);
 }
 
 }  // namespace idxfp4

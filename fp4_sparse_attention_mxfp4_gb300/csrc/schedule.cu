@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(kSchedThreads) build_decode_schedule_kernel(co
   __shared__ int s_ne[kMaxBatch + 1];     // exclusive prefix of non-empty sequences
   __shared__ int warp_sums[32];
   __shared__ int s_total, s_total_ne, s_scan;
+  pdl_wait();
+  pdl_trigger();
   DecodeSchedView v = decode_sched_view(sched, max_batch);
   const int tid = threadIdx.x;
 
@@ -201,6 +203,8 @@ __global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ row_ends,
     const int32_t* __restrict__ ctx_lens, int num_requests, int num_rows, int rows_per_unit, int table_width,
     int64_t units_cap, int64_t slots_cap, void* workspace, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int s_dyn[];
   int* s_off = s_dyn;                   // [kMaxBatch + 1] groups before each request
   int* s_n = s_dyn + kMaxBatch + 1;     // [kMaxPrefillGroups] chunks per group, then unit offsets
@@ -353,9 +357,8 @@ __global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
 cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, int batch, int max_batch, int64_t max_ctx, int ctas,
                                          int min_tiles, int64_t units_cap, void* sched, int32_t* status,
                                          cudaStream_t stream) {
-  build_decode_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(ctx_lens, batch, max_batch, max_ctx, ctas, min_tiles,
-                                                                 units_cap, sched, status);
-  return cudaGetLastError();
+  return launch_pdl(build_decode_schedule_kernel, dim3(1), dim3(kSchedThreads), 0, stream, 1, ctx_lens, batch,
+                    max_batch, max_ctx, ctas, min_tiles, units_cap, sched, status);
 }
 
 cudaError_t launch_build_prefill_schedule(const int32_t* cu_seqlens, const int32_t* row_ends, const int32_t* ctx_lens,
@@ -373,10 +376,9 @@ cudaError_t launch_build_prefill_schedule(const int32_t* cu_seqlens, const int32
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  build_prefill_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(cu_seqlens, row_ends, ctx_lens, num_requests,
-                                                                     num_rows, rows_per_unit, table_width, units_cap,
-                                                                     slots_cap, workspace, status);
-  return cudaGetLastError();
+  return launch_pdl(build_prefill_schedule_kernel, dim3(1), dim3(kSchedThreads), smem, stream, 1, cu_seqlens,
+                    row_ends, ctx_lens, num_requests, num_rows, rows_per_unit, table_width, units_cap, slots_cap,
+                    workspace, status);
 }
 
 }  // namespace idxfp4

@@ -222,6 +222,8 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
   // the shared state space, so accesses compile to shared-memory instructions.
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();
 
   // Schedule checks (uniform across the grid; nothing is allocated yet).
   const UnitIter it = unit_range(p);
@@ -655,6 +657,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
                             // [5] list complete, [6] slice total
   const int rank = static_cast<int>(cluster.block_rank());
   const int row = static_cast<int>(blockIdx.x) / kMergeG;
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int topk = mp.topk;
   // Row setup: every CTA of the cluster reads the same row, so every early return below is
@@ -1123,21 +1127,8 @@ cudaError_t launch_merge(const MergeParams& mp, int rows, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(rows) * kMergeG, 1, 1);
-  cfg.blockDim = dim3(kMergeThreads, 1, 1);
-  cfg.dynamicSmemBytes = kMergeSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kMergeG;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, merge_kernel, mp);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3(static_cast<unsigned>(rows) * kMergeG), dim3(kMergeThreads), kMergeSmem, stream,
+                    kMergeG, mp);
 }
 
 // The shared-memory opt-in is set once per device (so that a launch inside stream capture is
@@ -1161,8 +1152,7 @@ cudaError_t launch_scorer_t(const ScorerParams& p, int grid, cudaStream_t stream
   static bool configured[64] = {};
   cudaError_t e = ensure_smem(scorer_kernel<H, Q>, C::SMEM_BYTES, configured);
   if (e != cudaSuccess) return e;
-  scorer_kernel<H, Q><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(scorer_kernel<H, Q>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, 1, p);
 }
 
 template <int Q>
