@@ -563,15 +563,32 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         } else {
           uint2* slot = p.cand + static_cast<int64_t>(u.slot + r) * static_cast<int64_t>(cand_slot_entries(p.topk));
           uint2* oc = slot + 2;
+          uint32_t kand = 0xFFFFFFFFu, kor = 0u;
           for (int x = etid; x < kk; x += C::SEL_THREADS) {
             const uint2 e = sel[x];
             oc[x] = make_uint2(e.x, static_cast<uint32_t>(kb) + e.y);
+            kand &= e.x;
+            kor |= e.x;
           }
+          // The header also carries the AND and the OR of the list's keys, from which the merge
+          // finds the leading bits all of a row's candidates share without a pass of its own.
+          kand = __reduce_and_sync(0xFFFFFFFFu, kand);
+          kor = __reduce_or_sync(0xFFFFFFFFu, kor);
+          if (lane == 0) {
+            scr[32 + 2 * (etid >> 5)] = kand;
+            scr[33 + 2 * (etid >> 5)] = kor;
+          }
+          named_barrier_sync(kSelBarrier, C::SEL_THREADS);
           // odd counts get one pad entry so every list is a whole number of 16-byte pairs; key 0 is
           // below every logit and never selected
           if (etid == 0) {
+#pragma unroll
+            for (int w2 = 0; w2 < C::SEL_THREADS / 32; ++w2) {
+              kand &= scr[32 + 2 * w2];
+              kor |= scr[33 + 2 * w2];
+            }
             if (kk & 1) oc[kk] = make_uint2(0u, 0xFFFFFFFFu);
-            slot[0] = make_uint2(static_cast<uint32_t>(kk), 0u);
+            *reinterpret_cast<uint4*>(slot) = make_uint4(static_cast<uint32_t>(kk), 0u, kand, kor);
           }
         }
         named_barrier_sync(kSelBarrier, C::SEL_THREADS);  // the area is reused by the next row
@@ -653,7 +670,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   uint32_t* lstart = ubuf + kMergeUnion;
   uint32_t* sc = lstart + kMergeMaxLists + 1;
   uint32_t* rv = sc + 64;                   // values pulled from every CTA of the cluster
-  uint32_t* pub = rv + 64;  // [0] AND, [1] OR, [2] keys > T, [3] keys == T, [4] listed keys,
+  uint32_t* pub = rv + 64;  // [2] keys > T, [3] keys == T, [4] listed keys,
                             // [5] list complete, [6] slice total
   const int rank = static_cast<int>(cluster.block_rank());
   const int row = static_cast<int>(blockIdx.x) / kMergeG;
@@ -661,6 +678,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int topk = mp.topk;
+  uint32_t* gtw = sc + 16;  // per warp: keys > thr (first the lists' AND)
+  uint32_t* eqw = sc + 32;  // per warp: keys == thr (first the lists' OR)
   // Row setup: every CTA of the cluster reads the same row, so every early return below is
   // taken by the whole cluster.
   int first, nu, stride, kk;
@@ -706,20 +725,28 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     __syncthreads();
   };
 
-  // 1. List starts: block scan of the lists' sizes (every CTA).
+  // 1. List starts: block scan of the lists' sizes, and the AND and OR of all the row's keys,
+  // from the lists' headers (every CTA reads all of them).
+  uint32_t pbits;  // leading bits shared by all the row's candidate keys
   {
     constexpr int kPerMax = kMergeMaxLists / kMergeThreads;
     const int per = (nu + kMergeThreads - 1) / kMergeThreads;
     const int l0 = min(nu, tid * per);
     uint32_t cnt[kPerMax];
-    uint32_t s = 0;
+    uint32_t s = 0, ka = 0xFFFFFFFFu, ko = 0u;
 #pragma unroll
     for (int j = 0; j < kPerMax; ++j) {
       const int li = l0 + j;
       const int64_t sl = first + static_cast<int64_t>(li) * stride;
-      cnt[j] = (j < per && li < nu && sl < mp.cand_slots)
-                   ? static_cast<uint32_t>(min(static_cast<int>(mp.cand[sl * slot_entries].x), topk))
-                   : 0u;
+      cnt[j] = 0u;
+      if (j < per && li < nu && sl < mp.cand_slots) {
+        const uint4 h = *reinterpret_cast<const uint4*>(mp.cand + sl * slot_entries);
+        cnt[j] = static_cast<uint32_t>(min(static_cast<int>(h.x), topk));
+        if (cnt[j] != 0u) {
+          ka &= h.z;
+          ko |= h.w;
+        }
+      }
       s += cnt[j];
     }
     uint32_t incl = s;
@@ -728,7 +755,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
       if (lane >= off) incl += v;
     }
+    ka = __reduce_and_sync(0xFFFFFFFFu, ka);
+    ko = __reduce_or_sync(0xFFFFFFFFu, ko);
     if (lane == 31) sc[w] = incl;
+    if (lane == 0) {
+      gtw[w] = ka;
+      eqw[w] = ko;
+    }
     for (int b = tid; b < 2048; b += kMergeThreads) hl[b] = 0u;
     __syncthreads();
     uint32_t run = incl - s;
@@ -739,6 +772,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       run += cnt[j];
       if (j < per && l0 + j < nu) lstart[l0 + j + 1] = run;
     }
+    uint32_t aa = 0xFFFFFFFFu, oo = 0u;
+#pragma unroll
+    for (int w2 = 0; w2 < kMergeNW; ++w2) {
+      aa &= gtw[w2];
+      oo |= eqw[w2];
+    }
+    pbits = (aa ^ oo) == 0u ? 32u : static_cast<uint32_t>(__clz(aa ^ oo));
     __syncthreads();
   }
   const int total = static_cast<int>(lstart[nu]);
@@ -768,10 +808,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 #pragma unroll
       for (int j = 0; j < 12; ++j) {
         const int p = b + j * kMergeThreads + tid;
-        if (p < p1) stage[p - p0] = v[j];
+        if (p < p1) {
+          stage[p - p0] = v[j];
+          smem_red_add(&hl[merge_xform(v[j].x, pbits) >> 21], 1u);  // 2. level 1, below
+        }
       }
     }
-    __syncthreads();
   }
   auto get = [&](int p) { return staged ? stage[p - p0] : entry(p); };
   // Entries p .. p+3 (p - p0 a multiple of 4); entries at or past `end` come back as zero keys.
@@ -796,46 +838,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   const int s0 = min(p1, p0 + w * seg), s1 = min(p1, s0 + seg);
   const uint32_t lt = (1u << lane) - 1u;
 
-  // 2. Common leading bits of the row's keys.
-  {
-    uint32_t a = 0xFFFFFFFFu, o = 0u;
-    for (int p = p0 + tid; p < p1; p += kMergeThreads) {
-      const uint32_t k = get(p).x;
-      a &= k;
-      o |= k;
-    }
-    a = __reduce_and_sync(0xFFFFFFFFu, a);
-    o = __reduce_or_sync(0xFFFFFFFFu, o);
-    if (lane == 0) {
-      sc[2 * w] = a;
-      sc[2 * w + 1] = o;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      uint32_t aa = 0xFFFFFFFFu, oo = 0u;
-      for (int w2 = 0; w2 < kMergeNW; ++w2) {
-        aa &= sc[2 * w2];
-        oo |= sc[2 * w2 + 1];
-      }
-      pub[0] = aa;
-      pub[1] = oo;
-    }
-  }
-  cluster.sync();
-  pull(0, 2);
-  uint32_t pbits;
-  {
-    uint32_t aa = 0xFFFFFFFFu, oo = 0u;
-#pragma unroll
-    for (int r = 0; r < kMergeG; ++r) {
-      aa &= rv[2 * r];
-      oo |= rv[2 * r + 1];
-    }
-    pbits = (aa ^ oo) == 0u ? 32u : static_cast<uint32_t>(__clz(aa ^ oo));
-  }
-  // 3. Level 1: top 11 bits of the shifted keys.
-  for (int p = p0 + tid; p < p1; p += kMergeThreads) smem_red_add(&hl[merge_xform(get(p).x, pbits) >> 21], 1u);
-  __syncthreads();
+  // 2. Level 1: top 11 bits of the shifted keys (counted while staging, when staged).
+  if (!staged)
+    for (int p = p0 + tid; p < p1; p += kMergeThreads) smem_red_add(&hl[merge_xform(get(p).x, pbits) >> 21], 1u);
   cluster.sync();
   // The level-1 bin of the threshold without moving whole histograms: CTA r sums bins
   // [256 r, 256 r + 256) over the cluster (one remote word per thread and CTA) and publishes the
@@ -876,8 +881,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     __syncthreads();
   };
   uint32_t thr = 0u, need = 0u;  // keep shifted key > thr, and the first `need` equal to it
-  uint32_t* gtw = sc + 16;      // per warp: keys > thr
-  uint32_t* eqw = sc + 32;      // per warp: keys == thr
   if (kk < total) {
     // slice holding the kk-th largest, scanning slices from the top
     uint32_t above_slice = 0;
@@ -1039,7 +1042,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     }
     __syncthreads();
   }
-  // 4. Offsets: this CTA's place among the cluster's, then each warp's place in the CTA.
+  // 3. Offsets: this CTA's place among the cluster's, then each warp's place in the CTA.
   if (tid == 0) {
     uint32_t g = 0, e = 0;
     for (int w2 = 0; w2 < kMergeNW; ++w2) {
@@ -1051,6 +1054,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   }
   cluster.sync();
   pull(2, 2);
+  // That was the last read of another CTA's shared memory: arrive now, and wait for the others
+  // only before leaving (no CTA exits while another may still read its published counts).
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
   uint32_t out = 0, eq_before = 0;
   for (int r = 0; r < rank; ++r) {
     out += rv[2 * r];
@@ -1061,7 +1067,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     out += gtw[w2] + (eq_before >= need ? 0u : min(eqw[w2], need - eq_before));
     eq_before += eqw[w2];
   }
-  // 5. Output pass in token order, four entries per lane.
+  // 4. Output pass in token order, four entries per lane.
   int32_t* oi = mp.topk_idx + static_cast<int64_t>(row) * topk;
   float* ov = mp.topk_val != nullptr ? mp.topk_val + static_cast<int64_t>(row) * topk : nullptr;
   for (int base = s0; base < s1; base += 128) {
@@ -1114,7 +1120,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       oi[e] = -1;
       if (ov != nullptr) ov[e] = -__int_as_float(0x7f800000);
     }
-  cluster.sync();  // no CTA leaves while another may still read its shared memory
+  asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
 }
 
 cudaError_t launch_merge(const MergeParams& mp, int rows, cudaStream_t stream) {
