@@ -110,7 +110,7 @@ __host__ __device__ inline DecodeSchedView decode_sched_view(void* base, int max
 }
 
 // Candidate slots (decode units of split sequences, prefill rows split into key chunks): slot s
-// is a 16-byte header (entry count, 0, AND of the entries' keys, OR of their keys), then up to k
+// is a 16-byte header (entry count, smallest key, largest key, 0), then up to k
 // (ordered key, token index) entries in token order; an odd count is followed by one (0, -1) pad entry so each list
 // is a whole number of 16-byte pairs. Key 0 is below every logit's key and never selected.
 __host__ __device__ inline size_t cand_slot_entries(int topk) { return round_up(static_cast<size_t>(topk) + 2, 2); }

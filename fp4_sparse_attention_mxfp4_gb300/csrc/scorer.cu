@@ -563,20 +563,21 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         } else {
           uint2* slot = p.cand + static_cast<int64_t>(u.slot + r) * static_cast<int64_t>(cand_slot_entries(p.topk));
           uint2* oc = slot + 2;
-          uint32_t kand = 0xFFFFFFFFu, kor = 0u;
+          uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
           for (int x = etid; x < kk; x += C::SEL_THREADS) {
             const uint2 e = sel[x];
             oc[x] = make_uint2(e.x, static_cast<uint32_t>(kb) + e.y);
-            kand &= e.x;
-            kor |= e.x;
+            kmin = min(kmin, e.x);
+            kmax = max(kmax, e.x);
           }
-          // The header also carries the AND and the OR of the list's keys, from which the merge
-          // finds the leading bits all of a row's candidates share without a pass of its own.
-          kand = __reduce_and_sync(0xFFFFFFFFu, kand);
-          kor = __reduce_or_sync(0xFFFFFFFFu, kor);
+          // The header also carries the list's smallest and largest key: the merge bounds the
+          // row's threshold from below by the smallest key of a full list, and bins only the
+          // keys above that bound.
+          kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+          kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
           if (lane == 0) {
-            scr[32 + 2 * (etid >> 5)] = kand;
-            scr[33 + 2 * (etid >> 5)] = kor;
+            scr[32 + 2 * (etid >> 5)] = kmin;
+            scr[33 + 2 * (etid >> 5)] = kmax;
           }
           named_barrier_sync(kSelBarrier, C::SEL_THREADS);
           // odd counts get one pad entry so every list is a whole number of 16-byte pairs; key 0 is
@@ -584,11 +585,11 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
           if (etid == 0) {
 #pragma unroll
             for (int w2 = 0; w2 < C::SEL_THREADS / 32; ++w2) {
-              kand &= scr[32 + 2 * w2];
-              kor |= scr[33 + 2 * w2];
+              kmin = min(kmin, scr[32 + 2 * w2]);
+              kmax = max(kmax, scr[33 + 2 * w2]);
             }
             if (kk & 1) oc[kk] = make_uint2(0u, 0xFFFFFFFFu);
-            *reinterpret_cast<uint4*>(slot) = make_uint4(static_cast<uint32_t>(kk), 0u, kand, kor);
+            *reinterpret_cast<uint4*>(slot) = make_uint4(static_cast<uint32_t>(kk), kmin, kmax, 0u);
           }
         }
         named_barrier_sync(kSelBarrier, C::SEL_THREADS);  // the area is reused by the next row
@@ -652,10 +653,11 @@ struct MergeParams {
   int32_t* status;
 };
 
-// Order-preserving shift of the row's candidate keys past their p common leading bits (p = 32:
-// all keys equal). Real keys are nonzero, and so are their images.
-__device__ __forceinline__ uint32_t merge_xform(uint32_t k, uint32_t p) {
-  return p >= 32u ? 1u : ((k << p) | (p != 0u ? 1u : 0u));
+// Keys below `lo` (a lower bound on the row's threshold) map to 0, never counted or selected;
+// keys from lo up, which share their p leading bits, are shifted past them, order-preserving
+// (p = 32: all equal). Real keys are nonzero, and so are the images of those kept.
+__device__ __forceinline__ uint32_t merge_xform(uint32_t k, uint32_t p, uint32_t lo) {
+  return k < lo ? 0u : (p >= 32u ? 1u : ((k << p) | (p != 0u ? 1u : 0u)));
 }
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_constant__ MergeParams mp) {
@@ -678,8 +680,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int topk = mp.topk;
-  uint32_t* gtw = sc + 16;  // per warp: keys > thr (first the lists' AND)
-  uint32_t* eqw = sc + 32;  // per warp: keys == thr (first the lists' OR)
+  uint32_t* gtw = sc + 16;  // per warp: keys > thr (first a bound on the threshold)
+  uint32_t* eqw = sc + 32;  // per warp: keys == thr (first the lists' smallest key)
   // Row setup: every CTA of the cluster reads the same row, so every early return below is
   // taken by the whole cluster.
   int first, nu, stride, kk;
@@ -725,15 +727,18 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     __syncthreads();
   };
 
-  // 1. List starts: block scan of the lists' sizes, and the AND and OR of all the row's keys,
-  // from the lists' headers (every CTA reads all of them).
-  uint32_t pbits;  // leading bits shared by all the row's candidate keys
+  // 1. List starts: block scan of the lists' sizes, and the range of keys that matter, from the
+  // lists' headers (every CTA reads all of them). A full list (k keys) is the top-k of its unit,
+  // so the row's k-th largest key is at least that list's smallest: `lo` is the largest such
+  // bound (with no full list, the smallest key of all). Only keys from lo to the largest key
+  // `hi` are binned, shifted past the leading bits lo and hi share.
+  uint32_t pbits, lo;
   {
     constexpr int kPerMax = kMergeMaxLists / kMergeThreads;
     const int per = (nu + kMergeThreads - 1) / kMergeThreads;
     const int l0 = min(nu, tid * per);
     uint32_t cnt[kPerMax];
-    uint32_t s = 0, ka = 0xFFFFFFFFu, ko = 0u;
+    uint32_t s = 0, lo_full = 0u, lo_all = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
     for (int j = 0; j < kPerMax; ++j) {
       const int li = l0 + j;
@@ -743,8 +748,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         const uint4 h = *reinterpret_cast<const uint4*>(mp.cand + sl * slot_entries);
         cnt[j] = static_cast<uint32_t>(min(static_cast<int>(h.x), topk));
         if (cnt[j] != 0u) {
-          ka &= h.z;
-          ko |= h.w;
+          lo_all = min(lo_all, h.y);
+          hi = max(hi, h.z);
+          if (h.x >= static_cast<uint32_t>(topk)) lo_full = max(lo_full, h.y);
         }
       }
       s += cnt[j];
@@ -755,12 +761,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
       if (lane >= off) incl += v;
     }
-    ka = __reduce_and_sync(0xFFFFFFFFu, ka);
-    ko = __reduce_or_sync(0xFFFFFFFFu, ko);
+    lo_full = __reduce_max_sync(0xFFFFFFFFu, lo_full);
+    lo_all = __reduce_min_sync(0xFFFFFFFFu, lo_all);
+    hi = __reduce_max_sync(0xFFFFFFFFu, hi);
     if (lane == 31) sc[w] = incl;
     if (lane == 0) {
-      gtw[w] = ka;
-      eqw[w] = ko;
+      gtw[w] = lo_full;
+      eqw[w] = lo_all;
+      sc[48 + w] = hi;
     }
     for (int b = tid; b < 2048; b += kMergeThreads) hl[b] = 0u;
     __syncthreads();
@@ -772,13 +780,17 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       run += cnt[j];
       if (j < per && l0 + j < nu) lstart[l0 + j + 1] = run;
     }
-    uint32_t aa = 0xFFFFFFFFu, oo = 0u;
+    lo_full = 0u;
+    lo_all = 0xFFFFFFFFu;
+    hi = 0u;
 #pragma unroll
     for (int w2 = 0; w2 < kMergeNW; ++w2) {
-      aa &= gtw[w2];
-      oo |= eqw[w2];
+      lo_full = max(lo_full, gtw[w2]);
+      lo_all = min(lo_all, eqw[w2]);
+      hi = max(hi, sc[48 + w2]);
     }
-    pbits = (aa ^ oo) == 0u ? 32u : static_cast<uint32_t>(__clz(aa ^ oo));
+    lo = lo_full != 0u ? lo_full : lo_all;
+    pbits = (lo ^ hi) == 0u ? 32u : static_cast<uint32_t>(__clz(lo ^ hi));
     __syncthreads();
   }
   const int total = static_cast<int>(lstart[nu]);
@@ -810,7 +822,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         const int p = b + j * kMergeThreads + tid;
         if (p < p1) {
           stage[p - p0] = v[j];
-          smem_red_add(&hl[merge_xform(v[j].x, pbits) >> 21], 1u);  // 2. level 1, below
+          const uint32_t t = merge_xform(v[j].x, pbits, lo);  // 2. level 1, below
+          if (t != 0u) smem_red_add(&hl[t >> 21], 1u);
         }
       }
     }
@@ -840,7 +853,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 
   // 2. Level 1: top 11 bits of the shifted keys (counted while staging, when staged).
   if (!staged)
-    for (int p = p0 + tid; p < p1; p += kMergeThreads) smem_red_add(&hl[merge_xform(get(p).x, pbits) >> 21], 1u);
+    for (int p = p0 + tid; p < p1; p += kMergeThreads) {
+      const uint32_t t = merge_xform(get(p).x, pbits, lo);
+      if (t != 0u) smem_red_add(&hl[t >> 21], 1u);
+    }
   cluster.sync();
   // The level-1 bin of the threshold without moving whole histograms: CTA r sums bins
   // [256 r, 256 r + 256) over the cluster (one remote word per thread and CTA) and publishes the
@@ -908,8 +924,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       uint32_t eqm = 0, t[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const bool in = p + j < s1;
-        t[j] = merge_xform(e[j].x, pbits);
+        t[j] = merge_xform(e[j].x, pbits, lo);
+        const bool in = p + j < s1 && t[j] != 0u;
         above += (in && (t[j] >> 21) > bin) ? 1u : 0u;
         eqm |= (in && (t[j] >> 21) == bin) ? (1u << j) : 0u;
       }
@@ -988,8 +1004,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
           for (int x = tid; x < m; x += kMergeThreads) count(cbuf[x] & 0x1FFFFFu);
         } else {
           for (int p = p0 + tid; p < p1; p += kMergeThreads) {
-            const uint32_t t = merge_xform(get(p).x, pbits);
-            if ((t >> 21) == bin) count(t & 0x1FFFFFu);
+            const uint32_t t = merge_xform(get(p).x, pbits, lo);
+            if (t != 0u && (t >> 21) == bin) count(t & 0x1FFFFFu);
           }
         }
         __syncthreads();
@@ -1018,8 +1034,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       for (int base = s0; base < s1; base += 32) {
         const int p = base + lane;
         if (p < s1) {
-          const uint32_t t = merge_xform(get(p).x, pbits);
-          if ((t >> 21) == bin) {
+          const uint32_t t = merge_xform(get(p).x, pbits, lo);
+          if (t != 0u && (t >> 21) == bin) {
             g += (t & 0x1FFFFFu) > low ? 1u : 0u;
             e += (t & 0x1FFFFFu) == low ? 1u : 0u;
           }
@@ -1078,7 +1094,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const bool in = p + j < s1;
-      const uint32_t t = merge_xform(e[j].x, pbits);
+      const uint32_t t = merge_xform(e[j].x, pbits, lo);  // thr >= 1: keys below lo never kept
       gtm |= (in && t > thr) ? (1u << j) : 0u;
       eqm |= (in && t == thr) ? (1u << j) : 0u;
     }
