@@ -680,8 +680,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int topk = mp.topk;
-  uint32_t* gtw = sc + 16;  // per warp: keys > thr (first a bound on the threshold)
-  uint32_t* eqw = sc + 32;  // per warp: keys == thr (first the lists' smallest key)
+  uint32_t* gtw = sc + 16;  // per warp: the largest smallest key of a full list
+  uint32_t* eqw = sc + 32;  // per warp: the smallest key of any list
   // Row setup: every CTA of the cluster reads the same row, so every early return below is
   // taken by the whole cluster.
   int first, nu, stride, kk;
@@ -796,26 +796,36 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   const int total = static_cast<int>(lstart[nu]);
   const int share = (total + kMergeG - 1) / kMergeG;
   const int p0 = min(total, rank * share), p1 = min(total, p0 + share);
-  // entry p of the row: list by binary search over the starts
-  auto entry = [&](int p) {
-    int lo = 0, hi = nu;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (static_cast<int>(lstart[mid]) <= p) lo = mid; else hi = mid;
+  // the list holding entry p (0 <= p < total): the last list starting at or before p, so
+  // lstart[li] <= p < lstart[li + 1]
+  auto list_of = [&](int p) {
+    int a = 0, b = nu;
+    while (b - a > 1) {
+      const int mid = (a + b) >> 1;
+      if (static_cast<int>(lstart[mid]) <= p) a = mid; else b = mid;
     }
-    return list_base(lo)[p - static_cast<int>(lstart[lo])];
+    return a;
   };
-  // The share is staged in shared memory with independent loads, twelve in flight per thread;
-  // a share too large for the stage (rows of more than kMergeG * kMergeStage candidates) is
-  // read from global memory in every pass instead.
+  auto entry = [&](int p) {
+    const int li = list_of(p);
+    return list_base(li)[p - static_cast<int>(lstart[li])];
+  };
+  // The share is staged in shared memory with independent loads, twelve in flight per thread
+  // (a thread's entries are kMergeThreads apart, so it walks its list index forward instead of
+  // searching for each); a share too large for the stage (rows of more than kMergeG *
+  // kMergeStage candidates) is read from global memory in every pass instead.
   const bool staged = p1 - p0 <= kMergeStage;
-  if (staged) {
+  if (staged && p0 + tid < p1) {
+    int li = list_of(p0 + tid);
     for (int b = p0; b < p1; b += 12 * kMergeThreads) {
       uint2 v[12];
 #pragma unroll
       for (int j = 0; j < 12; ++j) {
         const int p = b + j * kMergeThreads + tid;
-        if (p < p1) v[j] = entry(p);
+        if (p < p1) {
+          while (static_cast<int>(lstart[li + 1]) <= p) ++li;
+          v[j] = list_base(li)[p - static_cast<int>(lstart[li])];
+        }
       }
 #pragma unroll
       for (int j = 0; j < 12; ++j) {
@@ -846,10 +856,40 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       for (int j = 0; j < 4; ++j) e[j] = p + j < end ? entry(p + j) : make_uint2(0u, 0u);
     }
   };
-  // warp segments of this CTA's share (multiples of 4 entries), in token order
-  const int seg = ((p1 - p0 + kMergeNW - 1) / kMergeNW + 3) & ~3;
-  const int s0 = min(p1, p0 + w * seg), s1 = min(p1, s0 + seg);
-  const uint32_t lt = (1u << lane) - 1u;
+  // Each thread's run of the CTA's share, in token order (a multiple of 4 entries long except
+  // at the end). The passes below count over runs and turn the counts into list and output
+  // offsets with block scans.
+  const int2 trun = thread_run<kMergeThreads>(p1 - p0, tid);
+  const int ra = p0 + trun.x, rb = p0 + trun.y;
+  // exclusive prefix (x, y) and totals (z, w) over the CTA of two per-thread counts
+  auto scan2 = [&](uint32_t a, uint32_t b) {
+    uint32_t ia = a, ib = b;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t va = __shfl_up_sync(0xFFFFFFFFu, ia, off);
+      const uint32_t vb = __shfl_up_sync(0xFFFFFFFFu, ib, off);
+      if (lane >= off) {
+        ia += va;
+        ib += vb;
+      }
+    }
+    if (lane == 31) {
+      sc[2 * w] = ia;
+      sc[2 * w + 1] = ib;
+    }
+    __syncthreads();
+    uint32_t pa = 0, pb = 0, ta = 0, tb = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kMergeNW; ++w2) {
+      const uint32_t xa = sc[2 * w2], xb = sc[2 * w2 + 1];
+      pa += w2 < w ? xa : 0u;
+      pb += w2 < w ? xb : 0u;
+      ta += xa;
+      tb += xb;
+    }
+    __syncthreads();
+    return make_uint4(pa + ia - a, pb + ib - b, ta, tb);
+  };
 
   // 2. Level 1: top 11 bits of the shifted keys (counted while staging, when staged).
   if (!staged)
@@ -913,42 +953,32 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
     need = static_cast<uint32_t>(kk) - above_slice - r1.y;
     const uint32_t in_bin = ubuf[r1.x];  // the cluster's keys in the threshold bin
     const bool listed = hl[bin] <= static_cast<uint32_t>(kMergeCbuf);
-    // one pass: keys above the bin per warp, keys in the bin listed as (low 21 bits | warp << 21)
-    if (tid == 0) sc[48] = 0u;
-    __syncthreads();
-    uint32_t above = 0;
-    for (int base = s0; base < s1; base += 128) {
-      const int p = base + 4 * lane;
+    // The CTA's keys in the threshold bin (low 21 bits), listed in token order: a count over each
+    // run, a block scan, and a second walk of the run that writes them.
+    uint32_t inb = 0;
+    for (int p = ra; p < rb; p += 4) {
       uint2 e[4];
-      get4(p, s1, e);
-      uint32_t eqm = 0, t[4];
+      get4(p, rb, e);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        t[j] = merge_xform(e[j].x, pbits, lo);
-        const bool in = p + j < s1 && t[j] != 0u;
-        above += (in && (t[j] >> 21) > bin) ? 1u : 0u;
-        eqm |= (in && (t[j] >> 21) == bin) ? (1u << j) : 0u;
-      }
-      uint32_t pre = 0, tot = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t bb = __ballot_sync(0xFFFFFFFFu, (eqm >> j) & 1u);
-        pre += __popc(bb & lt);
-        tot += __popc(bb);
-      }
-      if (listed && tot != 0u) {
-        uint32_t slot = 0;
-        if (lane == 0) slot = atomicAdd(&sc[48], tot);
-        slot = __shfl_sync(0xFFFFFFFFu, slot, 0) + pre;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if ((eqm >> j) & 1u) cbuf[slot++] = (t[j] & 0x1FFFFFu) | (static_cast<uint32_t>(w) << 21);
+        const uint32_t t = merge_xform(e[j].x, pbits, lo);
+        inb += (p + j < rb && t != 0u && (t >> 21) == bin) ? 1u : 0u;
       }
     }
-    above = __reduce_add_sync(0xFFFFFFFFu, above);
-    if (lane == 0) gtw[w] = above;
-    __syncthreads();
-    const int m = static_cast<int>(sc[48]);
+    const uint4 ls = scan2(inb, 0u);
+    const int m = static_cast<int>(ls.z);
+    if (listed && inb != 0u) {
+      uint32_t slot = ls.x;
+      for (int p = ra; p < rb; p += 4) {
+        uint2 e[4];
+        get4(p, rb, e);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t t = merge_xform(e[j].x, pbits, lo);
+          if (p + j < rb && t != 0u && (t >> 21) == bin) cbuf[slot++] = t & 0x1FFFFFu;
+        }
+      }
+    }
     if (tid == 0) {
       pub[4] = static_cast<uint32_t>(m);
       pub[5] = listed ? 1u : 0u;
@@ -973,20 +1003,46 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
         for (int q = 1; q < kMergeG; ++q) r += static_cast<uint32_t>(u) >= base_of[q] ? 1 : 0;
         ubuf[u] = cluster.map_shared_rank(cbuf, r)[u - static_cast<int>(base_of[r])] & 0x1FFFFFu;
       }
-#pragma unroll 1
-      for (int level = 0; level < 2; ++level) {
-        const int nb = level == 0 ? 2048 : 1024;
-        for (int x = tid; x < 2048; x += kMergeThreads) hl[x] = 0u;
-        __syncthreads();
-        for (int x = tid; x < static_cast<int>(in_bin); x += kMergeThreads) {
-          const uint32_t c = ubuf[x];
-          if (level == 0) smem_red_add(&hl[c >> 10], 1u);
-          else if ((c >> 10) == (low >> 10)) smem_red_add(&hl[c & 1023u], 1u);
+      __syncthreads();
+      if (in_bin <= static_cast<uint32_t>(kMergeThreads)) {
+        // Rank selection: thread u holds gathered key u; the threshold's low bits are the key
+        // with fewer than `need` keys above it and at least `need` at or above it (equal keys
+        // all write the same values).
+        if (tid < static_cast<int>(in_bin)) {
+          const uint32_t c = ubuf[tid];
+          uint32_t gt = 0, ge = 0;
+          for (int x = 0; x < static_cast<int>(in_bin); ++x) {
+            const uint32_t d = ubuf[x];
+            gt += d > c ? 1u : 0u;
+            ge += d >= c ? 1u : 0u;
+          }
+          if (gt < need && need <= ge) {
+            sc[60] = c;
+            sc[61] = gt;
+          }
         }
         __syncthreads();
-        const uint2 r = find_bin<kMergeThreads>(hl, nb, need, sc, tid, 1);
-        need -= r.y;
-        low |= level == 0 ? (r.x << 10) : r.x;
+        low = sc[60];
+        need -= sc[61];
+      } else {
+        // Three radix levels of 8, 8 and 5 bits, over 256 bins (one per thread).
+        uint32_t pre = 0u;
+#pragma unroll 1
+        for (int level = 0; level < 3; ++level) {
+          const int sh = level == 0 ? 13 : (level == 1 ? 5 : 0);  // this level's digit
+          const int psh = level == 0 ? 21 : sh + (level == 1 ? 8 : 5);  // the digits found so far
+          hl[tid] = 0u;
+          __syncthreads();
+          for (int x = tid; x < static_cast<int>(in_bin); x += kMergeThreads) {
+            const uint32_t c = ubuf[x];
+            if ((c >> psh) == pre) smem_red_add(&hl[(c >> sh) & (level == 2 ? 31u : 255u)], 1u);
+          }
+          __syncthreads();
+          const uint2 r = find_bin<kMergeThreads>(hl, kMergeThreads, need, sc, tid, 1);
+          need -= r.y;
+          pre = (pre << (level == 2 ? 5 : 8)) | r.x;
+        }
+        low = pre;
       }
     } else {
       // Levels 2 and 3 through cluster sums (from the list, or from the share when it did not fit).
@@ -1017,119 +1073,58 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
       }
     }
     thr = (bin << 21) | low;
-    // per-warp counts of keys > thr and == thr
-    if (tid < kMergeNW) eqw[tid] = 0u;
-    __syncthreads();
-    if (listed) {
-      for (int x = tid; x < m; x += kMergeThreads) {
-        const uint32_t c = cbuf[x];
-        const uint32_t ww = c >> 21, lo = c & 0x1FFFFFu;
-        if (lo > low)
-          smem_red_add(&gtw[ww], 1u);
-        else if (lo == low)
-          smem_red_add(&eqw[ww], 1u);
-      }
-    } else {
-      uint32_t g = 0, e = 0;
-      for (int base = s0; base < s1; base += 32) {
-        const int p = base + lane;
-        if (p < s1) {
-          const uint32_t t = merge_xform(get(p).x, pbits, lo);
-          if (t != 0u && (t >> 21) == bin) {
-            g += (t & 0x1FFFFFu) > low ? 1u : 0u;
-            e += (t & 0x1FFFFFu) == low ? 1u : 0u;
-          }
-        }
-      }
-      g = __reduce_add_sync(0xFFFFFFFFu, g);
-      e = __reduce_add_sync(0xFFFFFFFFu, e);
-      if (lane == 0) {
-        gtw[w] += g;
-        eqw[w] = e;
-      }
-    }
-    __syncthreads();
-  } else {
-    // every candidate is kept
-    const uint32_t g = s1 > s0 ? static_cast<uint32_t>(s1 - s0) : 0u;
-    if (lane == 0) {
-      gtw[w] = g;
-      eqw[w] = 0u;
-    }
-    __syncthreads();
   }
-  // 3. Offsets: this CTA's place among the cluster's, then each warp's place in the CTA.
-  if (tid == 0) {
-    uint32_t g = 0, e = 0;
-    for (int w2 = 0; w2 < kMergeNW; ++w2) {
-      g += gtw[w2];
-      e += eqw[w2];
+  // Every candidate is kept when kk >= total: thr = 0 and need = 0 keep every key (all are at
+  // least lo then, and map to nonzero images).
+  // 3. Offsets: per thread, the keys above thr and equal to it; a block scan gives the thread's
+  // place in the CTA, the published totals the CTA's place in the cluster.
+  uint32_t g = 0, e = 0;
+  for (int p = ra; p < rb; p += 4) {
+    uint2 en[4];
+    get4(p, rb, en);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t t = merge_xform(en[j].x, pbits, lo);  // thr >= 1 when selecting: keys below lo never kept
+      g += (p + j < rb && t > thr) ? 1u : 0u;
+      e += (p + j < rb && t == thr) ? 1u : 0u;
     }
-    pub[2] = g;
-    pub[3] = e;
+  }
+  const uint4 cs = scan2(g, e);
+  if (tid == 0) {
+    pub[2] = cs.z;
+    pub[3] = cs.w;
   }
   cluster.sync();
   pull(2, 2);
   // That was the last read of another CTA's shared memory: arrive now, and wait for the others
   // only before leaving (no CTA exits while another may still read its published counts).
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
-  uint32_t out = 0, eq_before = 0;
+  uint32_t gb = cs.x, eb = cs.y;  // keys above thr / equal to it before this thread's run
   for (int r = 0; r < rank; ++r) {
-    out += rv[2 * r];
-    eq_before += rv[2 * r + 1];
+    gb += rv[2 * r];
+    eb += rv[2 * r + 1];
   }
-  out += min(eq_before, need);
-  for (int w2 = 0; w2 < w; ++w2) {
-    out += gtw[w2] + (eq_before >= need ? 0u : min(eqw[w2], need - eq_before));
-    eq_before += eqw[w2];
-  }
-  // 4. Output pass in token order, four entries per lane.
+  // 4. Output in token order: a kept key goes to (keys above thr before it) + min(keys equal to
+  // thr before it, need); the first `need` keys equal to thr are kept.
   int32_t* oi = mp.topk_idx + static_cast<int64_t>(row) * topk;
   float* ov = mp.topk_val != nullptr ? mp.topk_val + static_cast<int64_t>(row) * topk : nullptr;
-  for (int base = s0; base < s1; base += 128) {
-    const int p = base + 4 * lane;
-    uint2 e[4];
-    get4(p, s1, e);
-    uint32_t gtm = 0, eqm = 0;
+  if (g + min(e, need > eb ? need - eb : 0u) != 0u) {
+    for (int p = ra; p < rb; p += 4) {
+      uint2 en[4];
+      get4(p, rb, en);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool in = p + j < s1;
-      const uint32_t t = merge_xform(e[j].x, pbits, lo);  // thr >= 1: keys below lo never kept
-      gtm |= (in && t > thr) ? (1u << j) : 0u;
-      eqm |= (in && t == thr) ? (1u << j) : 0u;
-    }
-    uint32_t eq_lanes = 0, eq_chunk = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t bb = __ballot_sync(0xFFFFFFFFu, (eqm >> j) & 1u);
-      eq_lanes += __popc(bb & lt);
-      eq_chunk += __popc(bb);
-    }
-    uint32_t keepm = 0, rk = eq_before + eq_lanes;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool eq = (eqm >> j) & 1u;
-      keepm |= (((gtm >> j) & 1u) || (eq && rk < need)) ? (1u << j) : 0u;
-      rk += eq ? 1u : 0u;
-    }
-    uint32_t k_lanes = 0, k_chunk = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t bb = __ballot_sync(0xFFFFFFFFu, (keepm >> j) & 1u);
-      k_lanes += __popc(bb & lt);
-      k_chunk += __popc(bb);
-    }
-    uint32_t pos = out + k_lanes;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if ((keepm >> j) & 1u) {
-        oi[pos] = static_cast<int32_t>(e[j].y);
-        if (ov != nullptr) ov[pos] = key_to_float(e[j].x);
-        ++pos;
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t t = merge_xform(en[j].x, pbits, lo);
+        const bool gt = p + j < rb && t > thr, eq = p + j < rb && t == thr;
+        if (gt || (eq && eb < need)) {
+          const uint32_t pos = gb + min(eb, need);
+          oi[pos] = static_cast<int32_t>(en[j].y);
+          if (ov != nullptr) ov[pos] = key_to_float(en[j].x);
+        }
+        gb += gt ? 1u : 0u;
+        eb += eq ? 1u : 0u;
       }
     }
-    out += k_chunk;
-    eq_before += eq_chunk;
   }
   if (rank == 0)
     for (int e = kk + tid; e < topk; e += kMergeThreads) {

@@ -141,6 +141,34 @@ def test_decode_many_rows_merge():
         _check_decode(run, ref)
 
 
+@pytest.mark.parametrize("n,n_x,topk", [(3000, 500, 2048), (60000, 0, 2048), (20000, 300, 64)])
+def test_decode_exact_ties_lowest_index(n, n_x, topk):
+    # One sequence whose keys are copies of two vectors (n_x of one at random places, the rest of
+    # the other): its logits take two values, and the k-th key sits in a class of hundreds to
+    # tens of thousands of exactly equal logits. Equal keys are taken in token order, so the
+    # selection must be exactly the oracle's lowest indices. The sizes steer the merge through
+    # each way of resolving the threshold bin: a few thousand tied candidates (radix levels on
+    # the gathered bin), and more than the cluster can gather (levels through cluster sums, the
+    # share read from global memory).
+    case = synth.decode_case(f"ties_{n}_{n_x}_k{topk}", 60 + n_x, [n], 64, topk)
+    order = np.argsort(synth.Rng(61).uniform(n), kind="stable")
+    vx, vy = case.k_bf16[0].copy(), case.k_bf16[1].copy()
+    case.k_bf16[:] = vy
+    case.k_bf16[order[:n_x]] = vx
+    run = DecodeRun(case).run()
+    kv_p, kv_s, qp, qs = _oracle_side(case)
+    ref = oracle.row_logits(qp, qs, case.w, 0, kv_p, kv_s, case.layout.block_tables[0], 0, n)
+    vals = np.unique(ref)
+    assert len(vals) <= 2
+    if len(vals) == 2:
+        assert vals[1] - vals[0] > 10 * 1e-4 * (1 + abs(vals[1])), "classes too close to order exactly"
+    expect = np.sort(np.lexsort((np.arange(n), -ref))[:min(topk, n)])
+    got = run.topk_idx.cpu().numpy()[0]
+    assert np.array_equal(got[:len(expect)], expect), f"{int((got[:len(expect)] != expect).sum())} indices differ"
+    assert_topk_match(got, run.topk_val.cpu().numpy()[0], ref, topk, case.name)
+    assert int(run.status.item()) == 0
+
+
 def test_decode_config3_full():
     case = synth.decode_config(3)
     run = DecodeRun(case).run()
