@@ -7,7 +7,8 @@ the writer quantises the step's new key and query heads, the schedule is rebuilt
 decode scorer scores every cached key and selects each sequence's top-k. The step is captured
 once in CUDA graphs and replayed; an L2-sized buffer is rewritten between timed steps. The
 causal-prefill workload (4 prompts of 2634..4295 tokens in 512-row steps) is timed in the same
-run and reported in the line's "prefill" object.
+run and reported in the line's "prefill" object, and prefill over a staged flat cache (one
+16384-token prompt, identity page table) in "prefill_flat".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -350,15 +351,17 @@ def run_decode_e2e(bench: DecodeBench, steps: int, warmup: int):
     return statistics.mean(times), h2d, d2h
 
 
-def run_prefill(steps: int, warmup: int):
-    """Causal prefill of 4 prompts (2634..4295 tokens) in 512-row steps, all steps captured in one
-    graph; returns seconds per full prefill pass and the algorithmic FLOPs of a pass."""
+def run_prefill(steps: int, warmup: int, case=None):
+    """Causal prefill of a PrefillCase (default: 4 prompts of 2634..4295 tokens) in 512-row steps,
+    all steps captured in one graph; returns seconds per full prefill pass and the algorithmic
+    FLOPs of a pass."""
     import numpy as np
     import torch
 
     import synth
     import fp4_sparse_attention_mxfp4_gb300 as fx
-    case = synth.prefill_config("pad8")
+    if case is None:
+        case = synth.prefill_config("pad8")
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
     H, k = case.heads, case.topk
     kv_p = torch.full((case.layout.num_pages, 4, 64, 16), 0x77, dtype=torch.uint8, device="cuda")
@@ -555,6 +558,14 @@ def run_ours(args):
                         "64 heads, top-2048", "steps_per_pass": pf_steps, "ms_per_pass": pf_s * 1e3,
             "alg_flop_per_pass": pf_flops, "tflops": pf_flops / pf_s / 1e12,
             "peak_tflops": fp4_peak, "peak_source": f"{peak_kind} bf16_tflops x {FP4_OVER_BF16:g} (nominal FP4/bf16)",
+            "frac_fp4_peak": pf_flops / pf_s / 1e12 / fp4_peak, "status_ok": pf_ok}
+        import synth
+        pf_s, pf_flops, pf_steps, pf_ok = run_prefill(max(5, min(args.steps, 20)), 3, synth.prefill_flat_config())
+        line["prefill_flat"] = {
+            "workload": "causal prefill over a staged flat cache (identity page table): one 16384-token prompt, "
+                        "512-row steps with padding rows, 64 heads, top-2048; rows past 8192 keys merged from "
+                        "key chunks", "steps_per_pass": pf_steps, "ms_per_pass": pf_s * 1e3,
+            "alg_flop_per_pass": pf_flops, "tflops": pf_flops / pf_s / 1e12, "peak_tflops": fp4_peak,
             "frac_fp4_peak": pf_flops / pf_s / 1e12 / fp4_peak, "status_ok": pf_ok}
         if rank == 0 and world == 1:
             del bench

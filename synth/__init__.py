@@ -128,14 +128,16 @@ class PagedLayout:
 
 
 def paged_layout(rng: Rng, ctx_lens, spare: float = 0.125, pool_pages: int | None = None,
-                 width: int | None = None, fill: int = -1) -> PagedLayout:
-    """Random page tables: each sequence's pages drawn without replacement from one pool."""
+                 width: int | None = None, fill: int = -1, contiguous: bool = False) -> PagedLayout:
+    """Random page tables: each sequence's pages drawn without replacement from one pool. With
+    `contiguous`, sequence b takes the pages right after sequence b-1's instead (an identity
+    table per sequence over a flat, staged pool)."""
     ctx_lens = [int(c) for c in ctx_lens]
     need = [-(-c // PAGE) for c in ctx_lens]
     total = sum(need)
     num_pages = pool_pages if pool_pages is not None else max(total + int(math.ceil(spare * total)), 1)
     assert num_pages >= total
-    perm = rng.permutation(num_pages)
+    perm = np.arange(num_pages) if contiguous else rng.permutation(num_pages)
     width = width if width is not None else max(max(need, default=1), 1)
     bt = np.full((len(ctx_lens), width), fill, np.int32)
     seq_pages, at = [], 0
@@ -241,13 +243,13 @@ class PrefillCase:
 
 
 def prefill_case(name: str, seed: int, prompt_lens, heads: int, topk: int, budget: int = 512,
-                 real_per_step: int = 509, pad_to: int = 8) -> PrefillCase:
+                 real_per_step: int = 509, pad_to: int = 8, contiguous: bool = False) -> PrefillCase:
     """Chunked causal prefill: requests processed in order, `real_per_step` real tokens per step (a step
     may span requests), then padding rows up to the next multiple of `pad_to` (at most `budget` rows),
     folded into the step's last request with row_end 0. pad_to=1 disables padding."""
     rng = Rng(seed)
     L = np.asarray(prompt_lens, dtype=np.int32)
-    layout = paged_layout(rng.fork(1), L)
+    layout = paged_layout(rng.fork(1), L, spare=0.0 if contiguous else 0.125, contiguous=contiguous)
     total = int(L.sum())
     k = qk_bf16(rng.fork(2), (total,))
     q = qk_bf16(rng.fork(3), (total, heads))
@@ -276,6 +278,13 @@ def prefill_case(name: str, seed: int, prompt_lens, heads: int, topk: int, budge
                                  np.asarray([e for _, _, e in groups], np.int32), toks))
         t += n
     return PrefillCase(name, heads, topk, L, layout, k, q, w, steps)
+
+
+def prefill_flat_config() -> PrefillCase:
+    """Prefill over a staged, flat cache: one 16384-token prompt whose pages are consecutive (an
+    identity page table), 512-row steps with padding rows, 64 heads, topk 2048, seed 5. Rows past
+    8192 keys are scored in key chunks whose candidate lists are merged."""
+    return prefill_case("prefill_flat_1req_16384_h64_k2048", 5, [16384], 64, 2048, 512, 509, 8, contiguous=True)
 
 
 def prefill_config(pad_variant: str = "pad8") -> PrefillCase:

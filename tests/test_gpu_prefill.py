@@ -122,6 +122,22 @@ def test_prefill_workload_odd_total_sampled():
     _run_case(synth.prefill_config("odd"), rows_per_step=6, seed=6)
 
 
+def test_prefill_identity_table_small_full_check():
+    # two requests staged back to back in a flat pool: each request's page table is consecutive pages
+    case = synth.prefill_case("flat_small", 45, [150, 201], 64, 96, budget=64, real_per_step=61, pad_to=8,
+                              contiguous=True)
+    assert np.array_equal(case.layout.block_tables[1, :4], np.arange(3, 7))
+    _run_case(case)
+
+
+def test_prefill_identity_table_long_prompt_sampled():
+    """One 16384-token prompt over an identity page table: rows past 8192 keys are scored in key
+    chunks whose candidate lists are merged."""
+    case = synth.prefill_flat_config()
+    assert np.array_equal(case.layout.block_tables[0], np.arange(case.layout.num_pages))
+    _run_case(case, rows_per_step=4, seed=7)
+
+
 def test_prefill_bad_rows_flagged():
     case = synth.prefill_case("bad", 43, [100], 16, 32, budget=104, real_per_step=100, pad_to=8)
     run = PrefillRun(case)
