@@ -421,6 +421,69 @@ def run_prefill(steps: int, warmup: int, case=None):
     return statistics.mean(ms) / 1e3, flops, len(case.steps), ok
 
 
+def run_mtp(steps: int, warmup: int):
+    """Decode with two verify rows per sequence (16 x 131072 keys, next_n 2) through the prefill
+    call, captured in a graph and replayed with an L2 flush between calls. Returns seconds per
+    call, (query row, key) pairs scored per call, algorithmic bytes per call and the status."""
+    import numpy as np
+    import torch
+
+    import synth
+    import fp4_sparse_attention_mxfp4_gb300 as fx
+    case = synth.mtp_config()
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    B, H, k, n = case.batch, case.heads, case.topk, case.next_n
+    R = B * n
+    kv_p = torch.full((case.layout.num_pages, 4, 64, 16), 0x77, dtype=torch.uint8, device="cuda")
+    kv_s = torch.full((case.layout.num_pages, 4, 64), 0xFF, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = case.all_slots()
+    chunk = 1 << 20
+    for a in range(0, slots.size, chunk):
+        fx.idx_fp4_quant_and_cache(d(case.k_bf16[a:a + chunk].view(np.int16)), d(slots[a:a + chunk]), kv_p, kv_s,
+                                   status=status)
+    qp = torch.empty((R, H, 64), dtype=torch.uint8, device="cuda")
+    qs = torch.empty((R, H, 4), dtype=torch.uint8, device="cuda")
+    fx.idx_fp4_quant_and_cache(d(case.k_bf16[:0].view(np.int16)), d(slots[:0]), kv_p, kv_s,
+                               q_bf16=d(case.q_bf16.view(np.int16)), q_packed=qp, q_scale=qs, status=status)
+    w, bt, ctx = d(case.w), d(case.layout.block_tables), d(case.ctx_lens)
+    cu, re = d(case.cu_seqlens()), d(case.row_ends())
+    max_ctx = int(case.ctx_lens.max())
+    ws = torch.zeros(fx.idx_fp4_prefill_workspace_bytes(B, R, H, max_ctx, k), dtype=torch.uint8, device="cuda")
+    idx = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    val = torch.empty((R, k), dtype=torch.float32, device="cuda")
+
+    def call():
+        fx.idx_fp4_prefill_logits_topk(qp, qs, w, kv_p, kv_s, bt, ctx, cu, re, k, max_ctx, ws, idx, val,
+                                       status=status)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    flush = torch.empty((256 << 20) // 4, dtype=torch.int32, device="cuda")
+    for _ in range(warmup):
+        g.replay()
+        flush.fill_(1)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        g.replay()
+        b.record()
+        flush.fill_(1)
+    torch.cuda.synchronize()
+    sec = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
+    pairs = int(case.row_ends().astype(np.int64).sum())
+    alg = decode_alg_bytes(case.ctx_lens, H * n, k * n)  # keys once; n query rows' operands and outputs
+    return sec, pairs, alg, int(status.item()) == 0
+
+
 def oracle_decode_rate(case, threads: int, min_seconds: float = 8.0, max_reps: int = 5):
     """The oracle (fp64 scoring + exact sort top-k) on the given decode workload, host cores."""
     import numpy as np
@@ -560,6 +623,11 @@ def run_ours(args):
             "peak_tflops": fp4_peak, "peak_source": f"{peak_kind} bf16_tflops x {FP4_OVER_BF16:g} (nominal FP4/bf16)",
             "frac_fp4_peak": pf_flops / pf_s / 1e12 / fp4_peak, "status_ok": pf_ok}
         import synth
+        mt_s, mt_pairs, mt_alg, mt_ok = run_mtp(max(10, min(args.steps, 50)), 3)
+        line["decode_mtp"] = {
+            "workload": "decode with 2 verify rows per sequence (next_n 2) through the prefill call: 16 x 131072 "
+                        "keys, 64 heads, top-2048", "us_per_layer": mt_s * 1e6, "row_key_pairs_per_s": mt_pairs / mt_s,
+            "alg_bytes_per_call": mt_alg, "hbm_frac": mt_alg / mt_s / 1e9 / hbm, "status_ok": mt_ok}
         pf_s, pf_flops, pf_steps, pf_ok = run_prefill(max(5, min(args.steps, 20)), 3, synth.prefill_flat_config())
         line["prefill_flat"] = {
             "workload": "causal prefill over a staged flat cache (identity page table): one 16384-token prompt, "

@@ -280,6 +280,52 @@ def prefill_case(name: str, seed: int, prompt_lens, heads: int, topk: int, budge
     return PrefillCase(name, heads, topk, L, layout, k, q, w, steps)
 
 
+@dataclasses.dataclass
+class MtpCase:
+    """Decode with next_n query rows per sequence (speculative-decoding verify rows): row j of
+    sequence b sees keys [0, ctx_b - next_n + 1 + j)."""
+    name: str
+    heads: int
+    topk: int
+    next_n: int
+    ctx_lens: np.ndarray      # int32 [B], keys cached per sequence (including the step's next_n)
+    layout: PagedLayout
+    k_bf16: np.ndarray        # uint16 [sum ctx][128]
+    q_bf16: np.ndarray        # uint16 [B * next_n][H][128], rows of sequence b at b * next_n + j
+    w: np.ndarray             # f32 [B * next_n][H]
+
+    @property
+    def batch(self):
+        return len(self.ctx_lens)
+
+    def all_slots(self) -> np.ndarray:
+        return np.concatenate([self.layout.slots(b, 0, int(c)) for b, c in enumerate(self.ctx_lens)])
+
+    def row_ends(self) -> np.ndarray:
+        j = np.tile(np.arange(self.next_n), self.batch)
+        return (np.repeat(self.ctx_lens, self.next_n) - self.next_n + 1 + j).astype(np.int32)
+
+    def cu_seqlens(self) -> np.ndarray:
+        return (np.arange(self.batch + 1) * self.next_n).astype(np.int32)
+
+
+def mtp_case(name: str, seed: int, ctx_lens, heads: int, topk: int, next_n: int) -> MtpCase:
+    rng = Rng(seed)
+    ctx = np.asarray(ctx_lens, dtype=np.int32)
+    assert np.all(ctx >= next_n)
+    layout = paged_layout(rng.fork(1), ctx)
+    k = qk_bf16(rng.fork(2), (int(ctx.sum()),))
+    q = qk_bf16(rng.fork(3), (len(ctx) * next_n, heads))
+    w = head_weights(rng.fork(4), len(ctx) * next_n, heads)
+    return MtpCase(name, heads, topk, next_n, ctx, layout, k, q, w)
+
+
+def mtp_config() -> MtpCase:
+    """The long-context decode workload with two verify rows per sequence: 16 x 131072 keys,
+    next_n 2, 64 heads, topk 2048, seed 6."""
+    return mtp_case("mtp2_b16_ctx131072_h64_k2048", 6, [131072] * 16, 64, 2048, 2)
+
+
 def prefill_flat_config() -> PrefillCase:
     """Prefill over a staged, flat cache: one 16384-token prompt whose pages are consecutive (an
     identity page table), 512-row steps with padding rows, 64 heads, topk 2048, seed 5. Rows past
