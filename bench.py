@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -162,11 +163,22 @@ def gpu_index_for_smi(local_rank: int) -> str:
     return str(local_rank)
 
 
+_CODE_TOKENS = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'', re.S)
+
+
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed (string literals kept)."""
+    text = _CODE_TOKENS.sub(lambda m: " " if m.group(0).startswith("/") else m.group(0), text)
+    return " ".join(text.split())
+
+
 def scorer_source_hash() -> str:
+    """Hash of the scorer's code (comments and layout ignored): the committed ncu traffic figure is
+    used only while the code it was measured on is unchanged."""
     h = hashlib.sha256()
     for name in SCORER_SOURCES:
-        with open(os.path.join(ROOT, "fp4_sparse_attention_mxfp4_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "fp4_sparse_attention_mxfp4_gb300", "csrc", name)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

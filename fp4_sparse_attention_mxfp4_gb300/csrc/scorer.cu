@@ -386,12 +386,13 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
   } else {
     if constexpr (C::RESPLIT) warpgroup_regs_inc<C::EPI_REGS>();
     // ---------------- epilogue: head-weighted ReLU sum, row buffer, exact top-k ----------------
-    // Two groups of four warps (one per TMEM lane quarter) take alternate tiles; the epilogue also
-    // lays out each unit's query operand and weights, two units ahead.
+    // GROUPS groups of four warps (one per TMEM lane quarter; three groups for tiles up to 64
+    // columns, two for 128) take tiles in turn; the epilogue also lays out each unit's query
+    // operand and weights, two units ahead.
     const int e = warp - C::EPI_WARP0;
     const int grp = e >> 2;                 // tiles t with t % GROUPS == grp are this group's
     const int qtr = warp & 3;               // TMEM lane quarter of this warp
-    const int etid = e * 32 + lane;         // rank in the 256-thread epilogue group
+    const int etid = e * 32 + lane;         // rank among the epilogue threads (the first SEL_THREADS select)
     const int krow = qtr * 32 + lane;       // key row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(qtr * 32) << 16;
     uint32_t* lg_base = reinterpret_cast<uint32_t*>(smem + C::OFF_LG);
