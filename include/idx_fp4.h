@@ -29,6 +29,13 @@
  *   - Every call is asynchronous on `stream`, launches only kernels, and may be captured
  *     into a CUDA graph. Nothing is sized from device data, so a captured graph may be
  *     replayed after the device-side inputs (context lengths, row ends, tables) change.
+ *   - Kernels are launched with programmatic stream serialization: each waits for the
+ *     preceding grid in the stream to complete before it touches memory, then lets the next
+ *     kernel begin launching. Stream order is unchanged for ordinary kernels, copies and
+ *     events that follow a call. A caller's own kernel launched with programmatic stream
+ *     serialization right after a call must wait for its prerequisite grid
+ *     (cudaGridDependencySynchronize / griddepcontrol.wait) before it reads the call's
+ *     outputs, as such kernels must after any kernel.
  *   - Return value: IDX_FP4_OK, or an IDX_FP4_ERR_* code from host-side argument checks
  *     (nothing is launched then), or IDX_FP4_ERR_CUDA if a launch failed.
  *   - `status_dev` (device int32, nullable): kernels OR IDX_FP4_DEV_* bits into it when
@@ -169,6 +176,9 @@ size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_h
  *   max_ctx    bound on every row end, the value the workspace was sized with
  *   workspace  device, >= idx_fp4_prefill_workspace_bytes(num_requests, num_rows, num_heads, max_ctx, topk)
  * Rows longer than one unit's share are scored in key chunks and merged inside the call.
+ * Decode with next_n query rows per sequence (speculative-decoding verify rows) is this call
+ * with one request per sequence b of next_n rows, row j carrying row_end ctx_b - next_n + 1 + j.
+ * The index head count of the layout's own rows (not next_n) sets num_heads.
  *   topk_idx [num_rows][topk] (required), topk_val (nullable), logits_debug as for decode */
 int idx_fp4_prefill_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
                                 const uint8_t *kv_packed, const uint8_t *kv_scale, int64_t num_pages,
