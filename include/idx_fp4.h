@@ -178,7 +178,7 @@ size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_h
  * Rows longer than one unit's share are scored in key chunks and merged inside the call.
  * Decode with next_n query rows per sequence (speculative-decoding verify rows) is this call
  * with one request per sequence b of next_n rows, row j carrying row_end ctx_b - next_n + 1 + j.
- * The index head count of the layout's own rows (not next_n) sets num_heads.
+ * num_heads stays the index head count of one row.
  *   topk_idx [num_rows][topk] (required), topk_val (nullable), logits_debug as for decode */
 int idx_fp4_prefill_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
                                 const uint8_t *kv_packed, const uint8_t *kv_scale, int64_t num_pages,
