@@ -7,6 +7,7 @@ asynchronously on the current (or given) stream:
     idx_fp4_quant_and_cache        bf16 keys -> paged MXFP4 cache (and q -> plain MXFP4)
     idx_fp4_build_decode_schedule  once per decode step: the persistent-grid work table
     idx_fp4_decode_logits_topk     decode: score every cached key of each sequence, top-k
+    idx_fp4_decode_mtp_logits_topk decode with next_n verify rows per sequence (one key pass)
     idx_fp4_prefill_logits_topk    causal prefill: score keys [0, row_end) per row, top-k
 """
 from ._lib import (  # noqa: F401
@@ -16,12 +17,16 @@ from ._lib import (  # noqa: F401
     DEV_BAD_ROWS,
     DEV_BAD_SCHEDULE,
     DEV_BAD_SLOT,
+    DEV_SYNC,
     DEV_TIMEOUT,
     IDX_FP4_MAX_TOPK,
     IdxFp4Error,
     STATIC_SCRATCH_BYTES,
     idx_fp4_build_decode_schedule,
+    idx_fp4_build_decode_schedule_mtp,
     idx_fp4_decode_logits_topk,
+    idx_fp4_decode_mtp_logits_topk,
+    idx_fp4_decode_mtp_workspace_bytes,
     idx_fp4_decode_logits_topk_static,
     idx_fp4_decode_static_bytes,
     idx_fp4_decode_schedule_bytes,

@@ -29,6 +29,7 @@ DEV_BAD_ROWS = 0x08
 DEV_BAD_SCHEDULE = 0x10
 DEV_TIMEOUT = 0x20
 DEV_CAPACITY = 0x40
+DEV_SYNC = 0x80
 
 _lock = threading.Lock()
 _lib = None
@@ -45,6 +46,10 @@ SIGNATURES = {
     "idx_fp4_decode_workspace_bytes": (_SZ, [_I32, _I64, _I32]),
     "idx_fp4_decode_logits_topk": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _P, _SZ, _P,
                                           _SZ, _P, _P, _P, _I64, _P, _P]),
+    "idx_fp4_build_decode_schedule_mtp": (_I32, [_P, _I32, _I32, _I32, _I64, _P, _SZ, _P, _P]),
+    "idx_fp4_decode_mtp_workspace_bytes": (_SZ, [_I32, _I64, _I32, _I32]),
+    "idx_fp4_decode_mtp_logits_topk": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32, _P,
+                                              _SZ, _P, _SZ, _P, _P, _P, _I64, _P, _P]),
     "idx_fp4_prefill_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I64, _I32]),
     "idx_fp4_decode_static_bytes": (_SZ, [_I32, _I64, _I32]),
     "idx_fp4_decode_logits_topk_static": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I64, _P,
@@ -166,7 +171,65 @@ def idx_fp4_build_decode_schedule(ctx_lens, max_batch: int, max_ctx: int, sched,
 
 
 def idx_fp4_decode_workspace_bytes(max_batch: int, max_ctx: int, topk: int) -> int:
+    """Workspace bytes of the decode call (zero-fill the buffer once before its first use)."""
     return int(lib().idx_fp4_decode_workspace_bytes(int(max_batch), int(max_ctx), int(topk)))
+
+
+def idx_fp4_build_decode_schedule_mtp(ctx_lens, next_n: int, max_batch: int, max_ctx: int, sched, status=None,
+                                      stream=None):
+    """Decode schedule for next_n verify rows per sequence (ctx_lens: device int32 [B])."""
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    _need(sched, "sched", torch.uint8, 1)
+    if status is not None:
+        _need(status, "status", torch.int32)
+    code = lib().idx_fp4_build_decode_schedule_mtp(_ptr(ctx_lens), ctx_lens.shape[0], int(next_n), int(max_batch),
+                                                   int(max_ctx), _ptr(sched), sched.numel(), _ptr(status),
+                                                   _stream(stream))
+    _check("idx_fp4_build_decode_schedule_mtp", code)
+
+
+def idx_fp4_decode_mtp_workspace_bytes(max_batch: int, max_ctx: int, topk: int, next_n: int) -> int:
+    return int(lib().idx_fp4_decode_mtp_workspace_bytes(int(max_batch), int(max_ctx), int(topk), int(next_n)))
+
+
+def idx_fp4_decode_mtp_logits_topk(q_packed, q_scale, weights, kv_packed, kv_scale, block_tables, ctx_lens,
+                                   next_n: int, topk: int, sched, workspace, topk_idx, topk_val=None,
+                                   logits_debug=None, status=None, stream=None):
+    """Decode with next_n verify rows per sequence: q rows [B*next_n, H, ...]; row j of sequence b
+    sees keys [0, ctx_b - next_n + 1 + j). Writes topk_idx [B*next_n, k] and topk_val."""
+    _need(q_packed, "q_packed", torch.uint8, 3)
+    R, H = q_packed.shape[0], q_packed.shape[1]
+    _need(q_scale, "q_scale", torch.uint8, 3)
+    _need(weights, "weights", torch.float32, 2)
+    _need(kv_packed, "kv_packed", torch.uint8, 4)
+    _need(kv_scale, "kv_scale", torch.uint8, 3)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    _need(sched, "sched", torch.uint8, 1)
+    _need(workspace, "workspace", torch.uint8, 1)
+    _need(topk_idx, "topk_idx", torch.int32, 2)
+    B = ctx_lens.shape[0]
+    if R != B * int(next_n) or tuple(q_scale.shape) != (R, H, 4) or tuple(weights.shape) != (R, H) or \
+            q_packed.shape[2] != 64:
+        raise ValueError("q_packed [B*next_n,H,64], q_scale [B*next_n,H,4], weights [B*next_n,H] expected")
+    if block_tables.shape[0] < B or tuple(topk_idx.shape) != (R, topk):
+        raise ValueError("block_tables [>=B, W], topk_idx [B*next_n, topk] expected")
+    if topk_val is not None:
+        _need(topk_val, "topk_val", torch.float32, 2)
+        if tuple(topk_val.shape) != (R, topk):
+            raise ValueError("topk_val must be [B*next_n, topk]")
+    stride = 0
+    if logits_debug is not None:
+        _need(logits_debug, "logits_debug", torch.float32, 2)
+        stride = logits_debug.shape[1]
+    if status is not None:
+        _need(status, "status", torch.int32)
+    code = lib().idx_fp4_decode_mtp_logits_topk(
+        _ptr(q_packed), _ptr(q_scale), _ptr(weights), _ptr(kv_packed), _ptr(kv_scale), kv_packed.shape[0],
+        _ptr(block_tables), block_tables.shape[1], _ptr(ctx_lens), B, int(next_n), H, int(topk), _ptr(sched),
+        sched.numel(), _ptr(workspace), workspace.numel(), _ptr(topk_idx), _ptr(topk_val), _ptr(logits_debug),
+        stride, _ptr(status), _stream(stream))
+    _check("idx_fp4_decode_mtp_logits_topk", code)
 
 
 def idx_fp4_decode_logits_topk(q_packed, q_scale, weights, kv_packed, kv_scale, block_tables, ctx_lens, topk: int,
@@ -219,8 +282,8 @@ def idx_fp4_decode_logits_topk_static(q_packed, q_scale, weights, kv_packed, kv_
                                       topk: int, max_ctx: int, sched, topk_idx, topk_val=None, logits_debug=None,
                                       status=None, stream=None):
     """Decode scoring + top-k without a workspace argument, for callers that cannot allocate device
-    memory: the candidate lists go to a fixed 16 MiB array the library keeps on each GPU. Same
-    outputs as idx_fp4_decode_logits_topk. `max_ctx` is the bound the schedule was built with.
+    memory: the workspace is a fixed 16 MiB array the library keeps on each GPU. Same outputs as
+    idx_fp4_decode_logits_topk. The schedule must be built with max_batch = B and this `max_ctx`.
     Calls that overlap on the GPU share that array and race; the first call on a device should
     come before any stream capture."""
     _need(q_packed, "q_packed", torch.uint8, 3)

@@ -3,9 +3,11 @@
 // neither the device nor the stream.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "common.cuh"
+#include "decode_sched.cuh"
 #include "idx_fp4.h"
 
 namespace idxfp4 {
@@ -13,19 +15,20 @@ cudaError_t launch_quant_and_cache(const uint16_t* k, int64_t num_tokens, const 
                                    uint8_t* kv_scale, int64_t num_pages, const uint16_t* q, int64_t num_q_vec,
                                    uint8_t* q_packed, uint8_t* q_scale, int32_t* status, int num_sms,
                                    cudaStream_t stream);
-cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, int batch, int max_batch, int64_t max_ctx, int ctas,
-                                         int min_tiles, int64_t units_cap, void* sched, int32_t* status,
-                                         cudaStream_t stream);
+cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, int batch, int next_n, int max_batch,
+                                         int64_t max_ctx, int ctas, const DecodeCaps& caps, void* sched,
+                                         int32_t* status, cudaStream_t stream);
 cudaError_t launch_build_prefill_schedule(const int32_t* cu_seqlens, const int32_t* row_ends, const int32_t* ctx_lens,
                                           int num_requests, int num_rows, int rows_per_unit, int table_width,
                                           int64_t units_cap, int64_t slots_cap, void* workspace, int32_t* status,
                                           cudaStream_t stream);
+bool decode_shape_supported(int heads, int next_n);
 cudaError_t launch_decode(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
                           const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
-                          const int32_t* block_tables, int bt_stride, const int32_t* ctx_lens, int batch, int H,
-                          int topk, const void* sched, size_t sched_bytes, void* workspace, int64_t cand_slots,
-                          int32_t* topk_idx, float* topk_val, float* logits_debug, int64_t logits_stride,
-                          int32_t* status, int grid, cudaStream_t stream);
+                          const int32_t* block_tables, int bt_stride, const int32_t* ctx_lens, int batch, int heads,
+                          int next_n, int topk, const void* sched, size_t sched_bytes, void* workspace,
+                          size_t ws_bytes, int32_t* topk_idx, float* topk_val, float* logits_debug,
+                          int64_t logits_stride, int32_t* status, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
                            const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
                            const int32_t* block_tables, int bt_stride, const int32_t* row_ends, int num_rows, int H,
@@ -38,7 +41,6 @@ namespace {
 
 using namespace idxfp4;
 
-constexpr int kMinTilesPerCta = 8;      // a CTA's share is at least 1024 keys
 constexpr int64_t kMaxCtx = 1ll << 30;   // keys per sequence / row the sizing formulas accept
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -53,6 +55,63 @@ int device_ctas() {
 }
 
 int to_code(cudaError_t e) { return e == cudaSuccess ? IDX_FP4_OK : IDX_FP4_ERR_CUDA; }
+
+// Decode capacities for (max_batch, max_ctx); false for sizes the tables cannot index (more than
+// 2^31 - 1 tiles of 128 keys in all).
+bool decode_caps_for(int max_batch, int64_t max_ctx, DecodeCaps* caps) {
+  if (max_batch < 1 || max_batch > kMaxBatch || max_ctx < 0 || max_ctx > kMaxCtx) return false;
+  *caps = decode_caps(max_batch, max_ctx);
+  return caps->tiles_cap <= INT32_MAX && caps->units_cap <= INT32_MAX;
+}
+
+size_t decode_ws_bytes(int max_batch, int64_t max_ctx, int topk, int next_n) {
+  if (topk < 1 || topk > IDX_FP4_MAX_TOPK || next_n < 1 || next_n > kMaxNextN) return 0;
+  DecodeCaps caps;
+  if (!decode_caps_for(max_batch, max_ctx, &caps)) return 0;
+  return decode_ws_bytes_for(caps, max_batch, next_n, topk);
+}
+
+int build_schedule(const int32_t* ctx_lens_dev, int batch, int next_n, int max_batch, int64_t max_ctx, void* sched_dev,
+                   size_t sched_bytes, int32_t* status_dev, cudaStream_t stream) {
+  if (max_batch < 1 || max_batch > kMaxBatch || batch < 0 || batch > max_batch || max_ctx < 0 || max_ctx > kMaxCtx ||
+      next_n < 1 || next_n > kMaxNextN)
+    return IDX_FP4_ERR_ARG;
+  if (sched_dev == nullptr || !aligned16(sched_dev) || (batch > 0 && ctx_lens_dev == nullptr)) return IDX_FP4_ERR_ARG;
+  DecodeCaps caps;
+  if (!decode_caps_for(max_batch, max_ctx, &caps)) return IDX_FP4_ERR_ARG;
+  if (sched_bytes < decode_sched_bytes_for(max_batch, caps)) return IDX_FP4_ERR_CAPACITY;
+  const int ctas = device_ctas();
+  if (ctas <= 0) return IDX_FP4_ERR_CUDA;
+  return to_code(launch_build_decode_schedule(ctx_lens_dev, batch, next_n, max_batch, max_ctx, ctas, caps, sched_dev,
+                                              status_dev, stream));
+}
+
+int decode_call(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights, const uint8_t* kv_packed,
+                const uint8_t* kv_scale, int64_t num_pages, const int32_t* block_tables, int block_table_stride,
+                const int32_t* ctx_lens_dev, int batch, int num_heads, int next_n, int topk, const void* sched_dev,
+                size_t sched_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx, float* topk_val,
+                float* logits_debug, int64_t logits_stride, int32_t* status_dev, cudaStream_t stream) {
+  if (!heads_ok(num_heads) || topk < 1 || topk > IDX_FP4_MAX_TOPK || !decode_shape_supported(num_heads, next_n))
+    return IDX_FP4_ERR_SHAPE;
+  if (batch < 0 || batch > kMaxBatch) return IDX_FP4_ERR_ARG;
+  if (batch == 0) return IDX_FP4_OK;
+  if (q_packed == nullptr || q_scale == nullptr || weights == nullptr || kv_packed == nullptr ||
+      kv_scale == nullptr || block_tables == nullptr || ctx_lens_dev == nullptr || sched_dev == nullptr ||
+      workspace == nullptr || topk_idx == nullptr)
+    return IDX_FP4_ERR_ARG;
+  if (num_pages < 1 || block_table_stride < 1) return IDX_FP4_ERR_ARG;
+  if (logits_debug != nullptr && logits_stride < 1) return IDX_FP4_ERR_ARG;
+  if (!aligned16(q_packed) || !aligned16(q_scale) || !aligned16(weights) || !aligned16(kv_packed) ||
+      !aligned16(kv_scale) || !aligned16(sched_dev) || !aligned16(workspace))
+    return IDX_FP4_ERR_ARG;
+  if (sched_bytes < sizeof(DecodeSchedHeader)) return IDX_FP4_ERR_CAPACITY;
+  const int ctas = device_ctas();
+  if (ctas <= 0) return IDX_FP4_ERR_CUDA;
+  return to_code(launch_decode(q_packed, q_scale, weights, kv_packed, kv_scale, num_pages, block_tables,
+                               block_table_stride, ctx_lens_dev, batch, num_heads, next_n, topk, sched_dev,
+                               sched_bytes, workspace, workspace_bytes, topk_idx, topk_val, logits_debug,
+                               logits_stride, status_dev, ctas, stream));
+}
 
 }  // namespace
 
@@ -94,28 +153,28 @@ int idx_fp4_quant_and_cache(const uint16_t* k_bf16, int64_t num_tokens, const in
 }
 
 size_t idx_fp4_decode_schedule_bytes(int max_batch, int64_t max_ctx) {
-  if (max_batch < 1 || max_batch > kMaxBatch || max_ctx < 0 || max_ctx > kMaxCtx) return 0;
-  return decode_sched_bytes_for(max_batch, decode_units_cap(max_batch, max_ctx));
+  DecodeCaps caps;
+  if (!decode_caps_for(max_batch, max_ctx, &caps)) return 0;
+  return decode_sched_bytes_for(max_batch, caps);
 }
 
 int idx_fp4_build_decode_schedule(const int32_t* ctx_lens_dev, int batch, int max_batch, int64_t max_ctx,
                                   void* sched_dev, size_t sched_bytes, int32_t* status_dev, cudaStream_t stream) {
-  if (max_batch < 1 || max_batch > kMaxBatch || batch < 0 || batch > max_batch || max_ctx < 0 || max_ctx > kMaxCtx)
-    return IDX_FP4_ERR_ARG;
-  if (sched_dev == nullptr || !aligned16(sched_dev) || (batch > 0 && ctx_lens_dev == nullptr)) return IDX_FP4_ERR_ARG;
-  const int64_t units_cap = decode_units_cap(max_batch, max_ctx);
-  if (sched_bytes < decode_sched_bytes_for(max_batch, units_cap)) return IDX_FP4_ERR_CAPACITY;
-  const int ctas = device_ctas();
-  if (ctas <= 0) return IDX_FP4_ERR_CUDA;
-  return to_code(launch_build_decode_schedule(ctx_lens_dev, batch, max_batch, max_ctx, ctas, kMinTilesPerCta,
-                                              units_cap, sched_dev, status_dev, stream));
+  return build_schedule(ctx_lens_dev, batch, 1, max_batch, max_ctx, sched_dev, sched_bytes, status_dev, stream);
+}
+
+int idx_fp4_build_decode_schedule_mtp(const int32_t* ctx_lens_dev, int batch, int next_n, int max_batch,
+                                      int64_t max_ctx, void* sched_dev, size_t sched_bytes, int32_t* status_dev,
+                                      cudaStream_t stream) {
+  return build_schedule(ctx_lens_dev, batch, next_n, max_batch, max_ctx, sched_dev, sched_bytes, status_dev, stream);
 }
 
 size_t idx_fp4_decode_workspace_bytes(int max_batch, int64_t max_ctx, int topk) {
-  if (max_batch < 1 || max_batch > kMaxBatch || max_ctx < 0 || max_ctx > kMaxCtx || topk < 1 ||
-      topk > IDX_FP4_MAX_TOPK)
-    return 0;
-  return decode_workspace_bytes_for(decode_units_cap(max_batch, max_ctx), topk);
+  return decode_ws_bytes(max_batch, max_ctx, topk, 1);
+}
+
+size_t idx_fp4_decode_mtp_workspace_bytes(int max_batch, int64_t max_ctx, int topk, int next_n) {
+  return decode_ws_bytes(max_batch, max_ctx, topk, next_n);
 }
 
 int idx_fp4_decode_logits_topk(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
@@ -125,26 +184,22 @@ int idx_fp4_decode_logits_topk(const uint8_t* q_packed, const uint8_t* q_scale, 
                                void* workspace, size_t workspace_bytes, int32_t* topk_idx, float* topk_val,
                                float* logits_debug, int64_t logits_stride, int32_t* status_dev,
                                cudaStream_t stream) {
-  if (!heads_ok(num_heads) || topk < 1 || topk > IDX_FP4_MAX_TOPK) return IDX_FP4_ERR_SHAPE;
-  if (batch < 0 || batch > kMaxBatch) return IDX_FP4_ERR_ARG;
-  if (batch == 0) return IDX_FP4_OK;
-  if (q_packed == nullptr || q_scale == nullptr || weights == nullptr || kv_packed == nullptr ||
-      kv_scale == nullptr || block_tables == nullptr || ctx_lens_dev == nullptr || sched_dev == nullptr ||
-      workspace == nullptr || topk_idx == nullptr)
-    return IDX_FP4_ERR_ARG;
-  if (num_pages < 1 || block_table_stride < 1) return IDX_FP4_ERR_ARG;
-  if (logits_debug != nullptr && logits_stride < 1) return IDX_FP4_ERR_ARG;
-  if (!aligned16(q_packed) || !aligned16(q_scale) || !aligned16(weights) || !aligned16(kv_packed) ||
-      !aligned16(kv_scale) || !aligned16(sched_dev) || !aligned16(workspace))
-    return IDX_FP4_ERR_ARG;
-  if (sched_bytes < decode_sched_bytes_for(batch, 0)) return IDX_FP4_ERR_CAPACITY;
-  const int64_t cand_slots = static_cast<int64_t>(workspace_bytes / (sizeof(uint2) * cand_slot_entries(topk)));
-  const int ctas = device_ctas();
-  if (ctas <= 0) return IDX_FP4_ERR_CUDA;
-  return to_code(launch_decode(q_packed, q_scale, weights, kv_packed, kv_scale, num_pages, block_tables,
-                               block_table_stride, ctx_lens_dev, batch, num_heads, topk, sched_dev, sched_bytes,
-                               workspace, cand_slots, topk_idx, topk_val, logits_debug, logits_stride, status_dev,
-                               ctas, stream));
+  return decode_call(q_packed, q_scale, weights, kv_packed, kv_scale, num_pages, block_tables, block_table_stride,
+                     ctx_lens_dev, batch, num_heads, 1, topk, sched_dev, sched_bytes, workspace, workspace_bytes,
+                     topk_idx, topk_val, logits_debug, logits_stride, status_dev, stream);
+}
+
+int idx_fp4_decode_mtp_logits_topk(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
+                                   const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
+                                   const int32_t* block_tables, int block_table_stride, const int32_t* ctx_lens_dev,
+                                   int batch, int next_n, int num_heads, int topk, const void* sched_dev,
+                                   size_t sched_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
+                                   float* topk_val, float* logits_debug, int64_t logits_stride, int32_t* status_dev,
+                                   cudaStream_t stream) {
+  if (next_n < 1 || next_n > kMaxNextN) return IDX_FP4_ERR_SHAPE;
+  return decode_call(q_packed, q_scale, weights, kv_packed, kv_scale, num_pages, block_tables, block_table_stride,
+                     ctx_lens_dev, batch, num_heads, next_n, topk, sched_dev, sched_bytes, workspace,
+                     workspace_bytes, topk_idx, topk_val, logits_debug, logits_stride, status_dev, stream);
 }
 
 size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_heads, int64_t max_ctx, int topk) {

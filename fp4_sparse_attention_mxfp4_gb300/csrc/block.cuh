@@ -1,0 +1,146 @@
+// Block-wide primitives of the exact top-k: scans, radix histogram searches and an exact
+// selection over keys listed in token order. Every block-wide step synchronises on one named
+// barrier over the participating threads (the whole CTA in the decode kernel's selection phase).
+//
+// Keys are the order-preserving 32-bit images of fp32 logits (ordered_key): a larger logit has a
+// larger key, equal logits equal keys. Selecting the kk largest keys with ties going to the lower
+// token index is then: find the threshold key T (the kk-th largest) and the number `need` of keys
+// equal to T that are kept, and keep every key above T plus the first `need` keys equal to T in
+// token order. T is found radix-wise, 12 + 10 + 10 bits, with the first level's histogram often
+// known beforehand.
+#pragma once
+#include <cstdint>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace idxfp4 {
+
+struct Blk {
+  int tid, nt;          // thread rank and count (nt a multiple of 32, at most 1024)
+  uint32_t bar;         // named barrier over the nt threads
+  uint32_t* sc;         // shared scratch, at least 96 words
+  __device__ __forceinline__ void sync() const { named_barrier_sync(bar, static_cast<uint32_t>(nt)); }
+  __device__ __forceinline__ int lane() const { return tid & 31; }
+  __device__ __forceinline__ int warp() const { return tid >> 5; }
+  __device__ __forceinline__ int nw() const { return nt >> 5; }
+};
+
+// Exclusive prefix (thread order) of two per-thread counts; totals to *ta, *tb.
+__device__ __forceinline__ uint2 blk_scan2(const Blk& B, uint32_t a, uint32_t b, uint32_t* ta, uint32_t* tb) {
+  const int lane = B.lane(), w = B.warp();
+  uint32_t ia = a, ib = b;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t va = __shfl_up_sync(0xFFFFFFFFu, ia, off);
+    const uint32_t vb = __shfl_up_sync(0xFFFFFFFFu, ib, off);
+    if (lane >= off) {
+      ia += va;
+      ib += vb;
+    }
+  }
+  if (lane == 31) {
+    B.sc[2 * w] = ia;
+    B.sc[2 * w + 1] = ib;
+  }
+  B.sync();
+  uint32_t pa = 0, pb = 0, sa = 0, sb = 0;
+  for (int w2 = 0; w2 < B.nw(); ++w2) {
+    const uint32_t xa = B.sc[2 * w2], xb = B.sc[2 * w2 + 1];
+    if (w2 < w) {
+      pa += xa;
+      pb += xb;
+    }
+    sa += xa;
+    sb += xb;
+  }
+  B.sync();
+  if (ta != nullptr) *ta = sa;
+  if (tb != nullptr) *tb = sb;
+  return make_uint2(pa + ia - a, pb + ib - b);
+}
+
+// Bin of the need-th largest element (1 <= need <= total) of hist[0, nb), searching from the top:
+// returns (bin, elements in the bins above it) to every thread.
+__device__ __forceinline__ uint2 blk_find_bin(const Blk& B, const uint32_t* hist, int nb, uint32_t need) {
+  const int per = (nb + B.nt - 1) / B.nt;
+  const int b0 = min(nb, B.tid * per), b1 = min(nb, b0 + per);
+  uint32_t s = 0;
+  for (int b = b0; b < b1; ++b) s += hist[b];
+  uint32_t total = 0;
+  const uint32_t pre = blk_scan2(B, s, 0u, &total, nullptr).x;
+  uint32_t above = total - pre - s;  // elements in the bins of later threads
+  for (int b = b1 - 1; b >= b0; --b) {
+    const uint32_t c = hist[b];
+    if (above < need && need <= above + c) {
+      B.sc[64] = static_cast<uint32_t>(b);
+      B.sc[65] = above;
+    }
+    above += c;
+  }
+  B.sync();
+  const uint2 r = make_uint2(B.sc[64], B.sc[65]);
+  B.sync();
+  return r;
+}
+
+__device__ __forceinline__ void blk_zero(const Blk& B, uint32_t* p, int n) {
+  for (int i = B.tid; i < n; i += B.nt) p[i] = 0u;
+}
+
+// The contiguous run of [0, n) that thread tid owns in run-based passes (runs in thread order).
+__device__ __forceinline__ int2 blk_run(const Blk& B, int n) {
+  const int per = (n + B.nt - 1) / B.nt;
+  const int r0 = min(n, B.tid * per);
+  return make_int2(r0, min(n, r0 + per));
+}
+
+// Threshold of an exact top-kk over n candidates whose first-level bin is known: `bin` holds the
+// kk-th largest key, and `need` (>= 1) of its keys are among the kk. Finds the low 20 bits of T from
+// the keys in `bin`, listed into `list` when they fit list_cap, else counted straight from the
+// source in each level. Returns (T, keys equal to T that are kept). key(p) gives candidate p's key.
+// *consistent is false when the bin holds fewer than `need` keys (counts that do not belong to
+// these candidates); T then keeps nothing from the bin.
+template <class KeyAt>
+__device__ __forceinline__ uint2 blk_resolve(const Blk& B, KeyAt key, int n, uint32_t bin, uint32_t need,
+                                             uint32_t* hist, uint32_t* list, int list_cap, bool* consistent) {
+  const int2 run = blk_run(B, n);
+  uint32_t cnt = 0;
+  for (int p = run.x; p < run.y; ++p) cnt += (key(p) >> kL1Shift) == bin ? 1u : 0u;
+  uint32_t in_bin = 0;
+  uint32_t o = blk_scan2(B, cnt, 0u, &in_bin, nullptr).x;
+  *consistent = need >= 1u && need <= in_bin;
+  if (!*consistent) return make_uint2((bin << kL1Shift) | 0xFFFFFu, 0u);
+  const bool listed = in_bin <= static_cast<uint32_t>(list_cap);
+  if (listed && cnt != 0u)
+    for (int p = run.x; p < run.y; ++p) {
+      const uint32_t k = key(p);
+      if ((k >> kL1Shift) == bin) list[o++] = k;
+    }
+  B.sync();
+  uint32_t low = 0u;
+#pragma unroll 1
+  for (int level = 0; level < 2; ++level) {
+    const int shift = level == 0 ? 10 : 0;
+    blk_zero(B, hist, 1024);
+    B.sync();
+    auto count = [&](uint32_t k) {
+      if ((k >> kL1Shift) != bin) return;
+      const uint32_t l = k & 0xFFFFFu;
+      if (level == 0) smem_red_add(&hist[l >> 10], 1u);
+      else if ((l >> 10) == (low >> 10)) smem_red_add(&hist[l & 1023u], 1u);
+    };
+    if (listed) {
+      for (int i = B.tid; i < static_cast<int>(in_bin); i += B.nt) count(list[i]);
+    } else {
+      for (int p = B.tid; p < n; p += B.nt) count(key(p));
+    }
+    B.sync();
+    const uint2 r = blk_find_bin(B, hist, 1024, need);
+    need -= r.y;
+    low |= r.x << shift;
+  }
+  return make_uint2((bin << kL1Shift) | low, need);
+}
+
+}  // namespace idxfp4

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 #include <utility>
 
 #include "idx_fp4.h"
@@ -23,18 +24,18 @@ constexpr int kMaxBatch = 4096;                    // sequences (decode) / reque
 constexpr int kMaxPrefillRows = 8192;              // query rows per prefill call
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: a bound, never reached in normal runs
 
-// Keys one unit scores per query row: the unit's logits live in shared memory (4 B per key and
-// row). Decode units carry one row, prefill units up to two.
+// Keys one prefill unit scores per query row: the unit's logits live in shared memory (4 B per
+// key and row); a unit carries up to two rows.
 __host__ __device__ constexpr int unit_key_cap(int rows) { return rows == 1 ? 16384 : 8192; }
 
 // Row permutation of the scale plane inside a page: the 64 rows viewed as 4 x 16 and
 // transposed ("Use the index scale plane's own row order when staging FP4 prefill under DCP").
 __host__ __device__ constexpr int scale_slot(int row) { return (row % 16) * 4 + row / 16; }
 
-// One unit of scorer work: `nq` query rows sharing one page table, scored against keys
+// One unit of prefill scorer work: `nq` query rows sharing one page table, scored against keys
 // [kb, ke). kb is a multiple of kTileKeys and ke - kb <= unit_key_cap(rows per unit).
 struct Unit {
-  int32_t row;    // first query row (decode: the sequence)
+  int32_t row;    // first query row
   int32_t table;  // row of block_tables
   int32_t kb, ke;
   int32_t nq;
@@ -44,80 +45,15 @@ struct Unit {
 };
 static_assert(sizeof(Unit) == 32, "Unit is 32 bytes");
 
-constexpr uint32_t kDecodeMagic = 0x44534332u;   // "DSC2"
 constexpr uint32_t kPrefillMagic = 0x50465332u;  // "PFS2"
 
 __host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Decode schedule, at a fixed address the caller owns (CUDA-graph stable):
-//   header | cta_first[kMaxCtas] | cta_count[kMaxCtas] | seq_first[max_batch] | seq_units[max_batch] |
-//   seq_ctx[max_batch] | (pad to 32) | units[units_cap]
-// Units are stored in token order, so a sequence's units (and candidate slots) are consecutive
-// and so are each CTA's.
-struct DecodeSchedHeader {
-  uint32_t magic;
-  int32_t ctas;         // persistent grid the schedule was built for
-  int32_t batch;
-  int32_t max_batch;
-  int32_t num_units;
-  int32_t total_tiles;
-  int32_t tiles_per_range;
-  int32_t units_cap;
-};
-
-struct DecodeSchedView {
-  DecodeSchedHeader* hdr;
-  int32_t* cta_first;
-  int32_t* cta_count;
-  int32_t* seq_first;
-  int32_t* seq_units;
-  int32_t* seq_ctx;
-  Unit* units;
-};
-
-// Units a decode schedule can hold: tile ranges of at most unit_key_cap(1) keys (their number a
-// multiple of the grid), plus one more unit per sequence boundary inside a range.
-__host__ __device__ inline int64_t decode_units_cap(int max_batch, int64_t max_ctx) {
-  const int64_t tiles = static_cast<int64_t>(max_batch) * ((max_ctx + kTileKeys - 1) / kTileKeys);
-  const int64_t per = unit_key_cap(1) / kTileKeys;
-  return (tiles + per - 1) / per + kMaxCtas + max_batch;
-}
-
-__host__ __device__ inline size_t decode_units_offset(int max_batch) {
-  return round_up(sizeof(DecodeSchedHeader) + 2 * sizeof(int32_t) * kMaxCtas + 3 * sizeof(int32_t) * max_batch, 32);
-}
-
-__host__ __device__ inline size_t decode_sched_bytes_for(int max_batch, int64_t units_cap) {
-  return decode_units_offset(max_batch) + sizeof(Unit) * static_cast<size_t>(units_cap);
-}
-
-__host__ __device__ inline DecodeSchedView decode_sched_view(void* base, int max_batch) {
-  DecodeSchedView v;
-  char* p = static_cast<char*>(base);
-  v.hdr = reinterpret_cast<DecodeSchedHeader*>(p);
-  p += sizeof(DecodeSchedHeader);
-  v.cta_first = reinterpret_cast<int32_t*>(p);
-  p += sizeof(int32_t) * kMaxCtas;
-  v.cta_count = reinterpret_cast<int32_t*>(p);
-  p += sizeof(int32_t) * kMaxCtas;
-  v.seq_first = reinterpret_cast<int32_t*>(p);
-  p += sizeof(int32_t) * max_batch;
-  v.seq_units = reinterpret_cast<int32_t*>(p);
-  p += sizeof(int32_t) * max_batch;
-  v.seq_ctx = reinterpret_cast<int32_t*>(p);
-  v.units = reinterpret_cast<Unit*>(static_cast<char*>(base) + decode_units_offset(max_batch));
-  return v;
-}
-
-// Candidate slots (decode units of split sequences, prefill rows split into key chunks): slot s
+// Candidate slots (prefill rows split into key chunks): slot s
 // is a 16-byte header (entry count, smallest key, largest key, 0), then up to k
 // (ordered key, token index) entries in token order; an odd count is followed by one (0, -1) pad entry so each list
 // is a whole number of 16-byte pairs. Key 0 is below every logit's key and never selected.
 __host__ __device__ inline size_t cand_slot_entries(int topk) { return round_up(static_cast<size_t>(topk) + 2, 2); }
-
-__host__ __device__ inline size_t decode_workspace_bytes_for(int64_t units_cap, int topk) {
-  return sizeof(uint2) * cand_slot_entries(topk) * static_cast<size_t>(units_cap);
-}
 
 // Prefill workspace: header | row_merge[num_rows] (first slot, number of lists, clamped row end,
 // 0) | (pad to 32) | units[units_cap] | candidate slots[slots_cap]. Row r of a split row group has
@@ -164,6 +100,12 @@ __host__ __device__ inline size_t prefill_workspace_bytes_for(int num_requests, 
   return prefill_slots_offset(num_rows, units) + sizeof(uint2) * cand_slot_entries(topk) * static_cast<size_t>(slots);
 }
 
+// Radix levels of the exact top-k: the first takes the top 12 bits of an ordered key, the next
+// two 10 bits each.
+constexpr int kL1Bits = 12;
+constexpr int kL1Bins = 1 << kL1Bits;
+constexpr int kL1Shift = 32 - kL1Bits;
+
 // Order-preserving map fp32 -> uint32 (a larger float maps to a larger integer). Adding
 // +0.0f first folds -0 into +0 so that equal values compare equal.
 __device__ __forceinline__ uint32_t ordered_key(float f) {
@@ -191,26 +133,58 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Launch with programmatic stream serialization (plus a cluster shape when cluster_x > 1).
+// With `cooperative`, the grid is launched as a cooperative grid: all its CTAs are resident at
+// once (the launch fails otherwise), which kernels whose CTAs wait on each other rely on.
 template <class... KArgs, class... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                              int cluster_x, Args&&... args) {
+                              int cluster_x, bool cooperative, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[3];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = cluster_x > 1 ? 2 : 1;
+  cfg.numAttrs = n;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Opt a kernel into `bytes` of dynamic shared memory on the current device, once per device and
+// kernel (so that a launch inside stream capture is only a launch). Thread-safe.
+template <auto Kernel>
+inline cudaError_t set_smem_once(size_t bytes) {
+  static std::mutex m;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        static_cast<int>(bytes));
+  std::lock_guard<std::mutex> lock(m);
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace idxfp4

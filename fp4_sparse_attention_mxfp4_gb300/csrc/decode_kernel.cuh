@@ -1,0 +1,1043 @@
+// Decode: every cached key of each sequence scored against the sequence's query row(s) on tcgen05
+// block-scaled MXFP4 MMA, head-weighted ReLU reduction, and the exact top-k, in one persistent,
+// cooperative kernel.
+//
+// Method ("Score a DSA sparse indexer in FP4", squashed commit message and PR body):
+//   logit[q, t] = sum_h w[q, h] * relu(q_h . k_t), keys read in place from the paged two-plane FP4
+//   index region; a row's top-k is bounded by its context. With next_n verify rows per sequence
+//   (speculative decoding; on the pages the draft folds its batch x next_n verify rows back onto the
+//   batch's sequences and rebuilds the schedule for them), row j of a sequence sees keys
+//   [0, ctx - next_n + 1 + j) and all rows share one pass over the keys.
+//
+// GB300 design (the pages' kernels target MI355X MFMA; this is a fresh design):
+//   * Stream. CTA c takes the tile range the schedule gives it (at most cap_tiles(next_n) tiles of
+//     128 keys). Twelve stage warps each own one stage of a 12-stage ring: a warp issues its tile's
+//     eight 1 KB group-chunk bulk copies (cp.async.bulk; a page's chunk g lands at g * 2048 +
+//     page * 1024, the canonical no-swizzle K-major operand), loads the two pages' scale words,
+//     rebuilds them in the tensor core's scale layout, and issues the tile's two tcgen05.mma
+//     kind::mxf4 block_scale MMAs (M = 128 keys, N = next_n * H query heads, K = 64 each) into one
+//     of several TMEM accumulators. Three epilogue groups of four warps (one per TMEM lane quarter)
+//     read the accumulators with tcgen05.ld, form each key's logits in a fixed order and store their
+//     order-preserving 32-bit images in a shared-memory row buffer. Nothing else happens in the
+//     stream, so the bulk copies run at the rate of the memory system.
+//   * Select. Then every warp of the CTA works on the row buffer. A sequence whose keys all sit in
+//     this CTA is selected here (radix passes over the buffer). The units of a longer sequence
+//     publish the non-empty bins of their 12-bit key histograms (only bins at or above their own
+//     k-th key's bin), wait until every unit of the sequence has published, and each finds the
+//     sequence's threshold bin from the published counts. Each then writes only its keys at or
+//     above that bin (about k plus one bin's worth over the whole sequence, instead of k per unit)
+//     at its offset in the sequence's candidate array, and takes a ticket; the last unit to finish
+//     resolves the exact threshold inside the bin and writes the top-k in token order. The logits
+//     never reach global memory (unless a debug buffer is passed).
+//   * The grid is the SM count, launched cooperatively so that every CTA is resident while units
+//     wait on each other's histograms; every wait is bounded and reports a timeout in the status
+//     word instead of hanging.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "block.cuh"
+#include "common.cuh"
+#include "decode_sched.cuh"
+#include "ptx.cuh"
+
+namespace idxfp4 {
+
+// Arguments of one decode call (device pointers owned by the caller).
+struct DecodeParams {
+  const uint8_t* q_packed;
+  const uint8_t* q_scale;
+  const float* weights;
+  const uint8_t* kv_packed;
+  const uint8_t* kv_scale;
+  int64_t num_pages;
+  const int32_t* block_tables;
+  int bt_stride;
+  const int32_t* ctx_lens;
+  const void* sched;
+  size_t sched_bytes;
+  int batch;
+  int topk;
+  void* workspace;
+  size_t ws_bytes;
+  int32_t* topk_idx;
+  float* topk_val;
+  float* logits_debug;
+  int64_t logits_stride;
+  int32_t* status;
+};
+
+namespace {
+
+constexpr uint32_t kEpiBarrier = 1;    // the epilogue warps, during the stream
+constexpr uint32_t kSelBarrier = 2;    // the epilogue warps, during the selection
+constexpr uint32_t kRoundBarrier = 3;  // every warp of the CTA: a round's range is published
+
+template <int H, int Q>
+struct DecodeCfg {
+  static constexpr int N = H * Q;
+  static_assert(N % 16 == 0 && N <= 128, "MMA N dimension: next_n * heads, a multiple of 16 up to 128");
+  static constexpr int GROUPS = 3;                 // epilogue groups (tiles t with t % GROUPS == g)
+  static constexpr int ACC = N <= 64 ? 6 : 3;      // TMEM accumulators
+  static constexpr int STAGES = 12;                // tiles in flight; one stage warp per stage
+  static constexpr int EPI_WARP0 = STAGES;
+  static constexpr int EPI_WARPS = 4 * GROUPS;
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
+  static constexpr int THREADS = (STAGES + EPI_WARPS) * 32;
+  // Registers: the launch gives 65536 / THREADS each; during the stream the stage warpgroups give
+  // some back and the epilogue warpgroups take them (a tile's 64 accumulator columns in flight).
+  static constexpr uint32_t LAUNCH_REGS = (65536u / static_cast<uint32_t>(THREADS)) / 8u * 8u;
+  static constexpr uint32_t STAGE_REGS = 56u;
+  static constexpr uint32_t EPI_REGS =
+      (LAUNCH_REGS * (STAGES + EPI_WARPS) - STAGE_REGS * STAGES) / EPI_WARPS / 8u * 8u;
+  static_assert(STAGES % 4 == 0 && EPI_WARPS % 4 == 0, "roles are whole warpgroups");
+  static_assert(STAGE_REGS * STAGES + EPI_REGS * EPI_WARPS <= LAUNCH_REGS * (STAGES + EPI_WARPS),
+                "the re-split fits the registers the block is launched with");
+  static constexpr int CAP = decode_cap_tiles(Q) * kTileKeys;  // row-buffer keys per query row
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t SFA_COL = ACC * N;
+  static constexpr uint32_t SFB_COL = SFA_COL + 4 * STAGES;
+  static_assert(ACC % GROUPS == 0, "tiles sharing an accumulator belong to one epilogue group");
+  static_assert(SFB_COL + 8 <= TMEM_COLS, "accumulators and scale chunks fit the allocation");
+  // shared memory (offsets from a 1024-byte aligned base)
+  static constexpr uint32_t OFF_PACKED = 0;                         // [STAGES][4][128][16]
+  static constexpr uint32_t OFF_SFA = OFF_PACKED + STAGES * 8192;   // [STAGES][512]
+  static constexpr uint32_t OFF_QB = OFF_SFA + STAGES * 512;        // [2][4][N][16]
+  static constexpr uint32_t OFF_SFB = OFF_QB + 2 * N * 64;          // [2][512]
+  static constexpr uint32_t OFF_W = OFF_SFB + 2 * 512;              // [2][N]
+  static constexpr uint32_t OFF_LG = OFF_W + 2 * N * 4;             // [Q][CAP] ordered keys
+  static constexpr uint32_t OFF_SCR = OFF_LG + Q * CAP * 4;         // [128] block scratch
+  static constexpr int REL_RING = STAGES / ACC + 2;
+  static_assert(STAGES % ACC == 0, "a stage warp keeps to one accumulator");
+  // full[STAGES], empty[STAGES], acc_full[ACC], acc_rel[ACC * REL_RING], q_ready[2], q_free[2]
+  static constexpr uint32_t NUM_BARS = 2 * STAGES + ACC + ACC * REL_RING + 4;
+  static constexpr uint32_t BAR_QREADY = 2 * STAGES + ACC + ACC * REL_RING;
+  static constexpr uint32_t BAR_QFREE = BAR_QREADY + 2;
+  static constexpr uint32_t OFF_BAR = OFF_SCR + 128 * 4;
+  static constexpr uint32_t OFF_KS = OFF_BAR + NUM_BARS * 8;  // KernelShared
+  static constexpr uint32_t SMEM_BYTES = OFF_KS + 128;
+  static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM");
+  static_assert(OFF_LG % 16 == 0 && OFF_QB % 128 == 0, "operand and row-buffer alignment");
+  // The selection phase reuses the stage area (free once the stream has ended), in words:
+  static constexpr int P_WORDS = static_cast<int>(OFF_QB / 4);
+  static constexpr int P_HIST = 0;                    // [kL1Bins] histogram
+  static constexpr int P_LIST = P_HIST + kL1Bins;     // [4096] keys of the threshold bin
+  static constexpr int LIST_CAP = 4096;
+  static constexpr int P_UCNT = P_LIST + LIST_CAP;    // [1024 + 1] per-unit counts / offsets
+  static constexpr int P_UOFF = P_UCNT + 1028;        // [1024 + 1] per-unit record offsets
+  static constexpr int P_REC = P_UOFF + 1028;         // [RCAP] staged (record, unit) pairs
+  static constexpr int RCAP = 2048;
+  static constexpr int P_SOFF = P_WORDS - 1040;       // [1024 + 1] segment offsets of a sequence merge
+  static constexpr int P_CAND = P_LIST + LIST_CAP;    // the merge's staged candidates (after the records)
+  static constexpr int CCAP = (P_SOFF - P_CAND) / 2 / 128 * 128;
+  static_assert(P_REC + 2 * RCAP <= P_SOFF && CCAP >= 4096, "selection areas fit the stage area");
+};
+
+
+// ---- cross-CTA synchronisation in global memory ----------------------------------------------
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ uint32_t ldcg_u32(const uint32_t* p) { return __ldcg(p); }
+__device__ __forceinline__ uint2 ldcg_u2(const uint2* p) { return __ldcg(p); }
+
+// ---- stream phase -------------------------------------------------------------------------------
+
+struct RangeIter {
+  const DecodeUnit* units;
+  int first, count;
+  __device__ __forceinline__ DecodeUnit at(int i) const { return units[first + i]; }
+};
+
+__device__ __forceinline__ int dunit_tiles(const DecodeUnit& u) {
+  return u.ke > u.kb ? (u.ke - u.kb + kTileKeys - 1) / kTileKeys : 0;
+}
+
+struct Cursor {
+  int i, j, nt;
+  DecodeUnit u;
+};
+
+// Move `steps` tiles forward (skipping units without tiles); false once past the range's last tile.
+__device__ __forceinline__ bool cursor_advance(Cursor& c, int steps, const RangeIter& it) {
+  while (c.i < it.count && (steps > 0 || c.j >= c.nt)) {
+    const int left = c.nt - c.j;
+    if (steps < left) {
+      c.j += steps;
+      steps = 0;
+    } else {
+      steps -= left;
+      ++c.i;
+      c.j = 0;
+      if (c.i < it.count) {
+        c.u = it.at(c.i);
+        c.nt = dunit_tiles(c.u);
+      }
+    }
+  }
+  return c.i < it.count;
+}
+
+// Bounded wait: a timeout raises the CTA's abort flag and the status bit; later waits return at once.
+__device__ __forceinline__ bool wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
+  if (*abort_flag) return false;
+  if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
+  *abort_flag = 1;
+  set_status(status, IDX_FP4_DEV_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             int32_t* status) {
+  return mbar_try_wait(bar, parity) || wait_slow(bar, parity, abort_flag, status);
+}
+
+// Page id of the tile at cursor c for lane 0 (the tile's first page) and lane 1 (its second, or -1
+// when the tile holds one page). A logical page outside the table gives -2 and is not read.
+__device__ __forceinline__ int tile_page(const DecodeParams& p, const Cursor& c, int lane) {
+  const int lp = c.u.kb / kPage + 2 * c.j + lane;
+  const bool needed = lane == 0 || (lane == 1 && c.u.kb + c.j * kTileKeys + kPage < c.u.ke);
+  if (!needed) return -1;
+  if (lp < 0 || lp >= p.bt_stride) return -2;
+  return p.block_tables[static_cast<int64_t>(c.u.seq) * p.bt_stride + lp];
+}
+
+// Per-CTA state in shared memory. Every role re-reads it, so that little stays live in registers
+// across the warp-role branches (whose register budgets differ).
+struct RoundInfo {
+  int uf, ul;   // the round's units [uf, ul)
+  int tiles;    // tiles this CTA streamed in earlier rounds (ring and accumulator phases)
+  int units;    // units this CTA streamed in earlier rounds (query-buffer phases)
+};
+
+struct KernelShared {
+  DecodeSchedHeader h;  // the schedule's header
+  uint32_t tmem;        // TMEM base address
+  int abort;            // a bounded wait gave up: later waits return at once
+  RoundInfo round[2];   // round r in slot r & 1 (written before round r's start barrier, read after it;
+                        // slot r & 1 is rewritten only after every warp has passed round r + 1's)
+};
+static_assert(sizeof(KernelShared) <= 128, "fits its slot");
+
+__device__ __forceinline__ DecodeSchedView sched_view(const DecodeParams& p, const DecodeSchedHeader& h) {
+  return decode_sched_view(const_cast<void*>(p.sched), h.max_batch, h.ranges_cap, h.units_cap);
+}
+
+// Stage warp `ps`: streams the tiles t of this round's range with (st.tiles + t) % STAGES == ps
+// through its stage and issues their MMAs.
+template <int H, int Q>
+__device__ __forceinline__ void stream_stage_warp(const DecodeParams& p, uint8_t* smem, int slot, int ps, int lane) {
+  using C = DecodeCfg<H, Q>;
+  constexpr int N = C::N, ACC = C::ACC, STAGES = C::STAGES;
+  KernelShared* ks = reinterpret_cast<KernelShared*>(smem + C::OFF_KS);
+  volatile int* abort_flag = &ks->abort;
+  const uint32_t tmem = ks->tmem;
+  const RoundInfo st = ks->round[slot];
+  const RangeIter it{sched_view(p, ks->h).units, st.uf, st.ul - st.uf};
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + STAGES;
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint64_t* acc_rel = acc_full + ACC;
+  uint64_t* q_ready = bars + C::BAR_QREADY;
+  uint64_t* q_free = bars + C::BAR_QFREE;
+  const uint64_t pol = policy_evict_first();
+  uint8_t* stage = smem + C::OFF_PACKED + ps * 8192;
+  uint8_t* sfa_s = smem + C::OFF_SFA + ps * 512;
+  const uint64_t a_desc = smem_desc(smem_addr(stage), 2048, 128);
+  const uint32_t sfa_t = tmem + C::SFA_COL + 4u * static_cast<uint32_t>(ps);
+  const uint32_t idesc0 = mxf4_idesc(128, N, 0), idesc2 = mxf4_idesc(128, N, 2);
+  // The scale plane's 16x4 row transpose puts rows l%16 + 16*b of a page at byte b of word l%16 of
+  // each group's 64 bytes: lane l takes byte l/16 (rows l, l+64 of the tile) and byte 2 + l/16 (rows
+  // l+32, l+96); tile row m goes to TMEM lane m%32, column m/32 of the scale chunk.
+  const uint32_t sel_lo = static_cast<uint32_t>(lane >> 4), sel_hi = sel_lo + 2u;
+  const uint32_t perm_lo = sel_lo | ((sel_lo + 4u) << 4), perm_hi = sel_hi | ((sel_hi + 4u) << 4);
+  const int j0 = ((ps - st.tiles) % STAGES + STAGES) % STAGES;  // this warp's first tile of the round
+  Cursor c{0, 0, 0, DecodeUnit{}};
+  bool have = it.count > 0;
+  if (have) {
+    c.u = it.at(0);
+    c.nt = dunit_tiles(c.u);
+    have = cursor_advance(c, j0, it);
+  }
+  int entry = have ? tile_page(p, c, lane) : -1;
+  int f = st.tiles + j0;      // CTA-wide tile number (ring and accumulator phases)
+  // Query operands: this warp waits for every unit's operand in order (so that each parity wait
+  // names an unambiguous phase) and frees each unit's buffer once its tiles lie behind it.
+  int qnext = 0;              // next unit of the round whose operand this warp has waited for
+  int qfreed = 0;             // units of the round whose buffer this warp has freed
+  int last_f = -1;
+  while (have) {
+    int pid0 = __shfl_sync(0xFFFFFFFFu, entry, 0);
+    int pid1 = __shfl_sync(0xFFFFFFFFu, entry, 1);
+    const bool has1 = pid1 != -1;
+    if ((pid0 == -2 || pid1 == -2) && lane == 0) set_status(p.status, IDX_FP4_DEV_BAD_CTX);
+    if (pid0 < 0 || pid0 >= p.num_pages) {
+      if (lane == 0 && pid0 != -2) set_status(p.status, IDX_FP4_DEV_BAD_PAGE);
+      pid0 = 0;
+    }
+    if (has1 && (pid1 < 0 || pid1 >= p.num_pages)) {
+      if (lane == 0 && pid1 != -2) set_status(p.status, IDX_FP4_DEV_BAD_PAGE);
+      pid1 = 0;
+    }
+    // the stage's previous tile has been consumed by its MMAs
+    if (lane == 0) {
+      bounded_wait(&empty_bar[ps], ((f / STAGES) & 1) ^ 1, abort_flag, p.status);
+      mbar_arrive_expect_tx(&full_bar[ps], (has1 ? 2u : 1u) * kPageBytes);
+    }
+    __syncwarp();
+    if (lane < 8 && (lane < 4 || has1)) {
+      const int pg = lane >> 2, k = lane & 3;
+      const int64_t pid = pg == 0 ? pid0 : pid1;
+      bulk_load_evict_first(stage + k * 2048 + pg * 1024, p.kv_packed + pid * kPageBytes + k * 1024, 1024,
+                            &full_bar[ps], pol);
+    }
+    uint32_t w0[4], w1[4];
+    {
+      const uint32_t* s0 = reinterpret_cast<const uint32_t*>(p.kv_scale + static_cast<int64_t>(pid0) * kPageScaleBytes) + (lane & 15);
+      const uint32_t* s1 = reinterpret_cast<const uint32_t*>(p.kv_scale + static_cast<int64_t>(has1 ? pid1 : 0) * kPageScaleBytes) + (lane & 15);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        w0[g] = __ldg(s0 + 16 * g);
+        w1[g] = has1 ? __ldg(s1 + 16 * g) : 0x7F7F7F7Fu;
+      }
+    }
+    Cursor nc = c;
+    const bool next = cursor_advance(nc, STAGES, it);
+    const int next_entry = next ? tile_page(p, nc, lane) : -1;
+    {
+      const uint32_t c0 = __byte_perm(__byte_perm(w0[0], w0[1], perm_lo), __byte_perm(w0[2], w0[3], perm_lo), 0x5410);
+      const uint32_t c1 = __byte_perm(__byte_perm(w0[0], w0[1], perm_hi), __byte_perm(w0[2], w0[3], perm_hi), 0x5410);
+      const uint32_t c2 = __byte_perm(__byte_perm(w1[0], w1[1], perm_lo), __byte_perm(w1[2], w1[3], perm_lo), 0x5410);
+      const uint32_t c3 = __byte_perm(__byte_perm(w1[0], w1[1], perm_hi), __byte_perm(w1[2], w1[3], perm_hi), 0x5410);
+      *reinterpret_cast<uint4*>(sfa_s + lane * 16) = make_uint4(c0, c1, c2, c3);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      bounded_wait(&full_bar[ps], (f / STAGES) & 1, abort_flag, p.status);
+      // in order: wait for unit x's operand, and free it at once when this tile lies past unit x
+      // (the operand of unit x + 2 is only prepared once every stage warp has freed unit x)
+      while (qnext <= c.i) {
+        const int un = st.units + qnext;
+        bounded_wait(&q_ready[un & 1], (un >> 1) & 1, abort_flag, p.status);
+        ++qnext;
+        for (; qfreed < qnext && qfreed < c.i; ++qfreed) mbar_arrive(&q_free[(st.units + qfreed) & 1]);
+      }
+      const int a = f % ACC, jf = f / ACC;
+      if (jf >= 1)  // the accumulator's previous tile has been read out
+        bounded_wait(&acc_rel[a * C::REL_RING + (jf - 1) % C::REL_RING],
+                     static_cast<uint32_t>((jf - 1) / C::REL_RING) & 1u, abort_flag, p.status);
+      tc_fence_after_sync();
+      const int par = (st.units + c.i) & 1;
+      const uint32_t qb = smem_addr(smem + C::OFF_QB + par * (N * 64));
+      const uint32_t sfb = tmem + C::SFB_COL + 4u * static_cast<uint32_t>(par);
+      const uint32_t d = tmem + static_cast<uint32_t>(a * N);
+      tmem_copy_sf_chunk(sfa_t, smem_addr(sfa_s));
+      mma_mxf4(d, a_desc, smem_desc(qb, N * 16, 128), idesc0, sfa_t, sfb, 0u);
+      mma_mxf4(d, a_desc + (4096 >> 4), smem_desc(qb + 2 * N * 16, N * 16, 128), idesc2, sfa_t, sfb, 1u);
+      tc_commit(&empty_bar[ps]);
+      tc_commit(&acc_full[a]);
+    }
+    __syncwarp();
+    last_f = f;
+    c = nc;
+    have = next;
+    entry = next_entry;
+    f += STAGES;
+  }
+  // This warp's last copies and MMAs are done before the stage area is reused; the operands of the
+  // round's remaining units are waited for (their scale copies into TMEM completed) and freed.
+  if (lane == 0) {
+    if (last_f >= 0) {
+      mbar_wait(&full_bar[ps], (last_f / STAGES) & 1, kWaitLimitNs);
+      mbar_wait(&empty_bar[ps], (last_f / STAGES) & 1, kWaitLimitNs);
+    }
+    for (; qfreed < it.count; ++qfreed) {
+      if (qfreed >= qnext) {
+        const int un = st.units + qfreed;
+        bounded_wait(&q_ready[un & 1], (un >> 1) & 1, abort_flag, p.status);
+        qnext = qfreed + 1;
+      }
+      mbar_arrive(&q_free[(st.units + qfreed) & 1]);
+    }
+  }
+  __syncwarp();
+}
+
+// Query heads of unit i (rows seq * Q .. seq * Q + Q - 1) -> canonical K-major [4 chunks][N][16 B]
+// operand, query scales -> the tensor core's scale layout (row n at line n%32, word n/32), weights
+// -> plain floats; one thread then copies the scales to TMEM and commits q_ready. The buffers of
+// parity un & 1 are free: the unit that used them last has been fully read out.
+template <int H, int Q>
+__device__ __forceinline__ void prep_query(const DecodeParams& p, const DecodeUnit& u, int un, uint8_t* smem,
+                                           uint32_t tmem, int etid) {
+  using C = DecodeCfg<H, Q>;
+  constexpr int N = C::N;
+  uint64_t* q_ready = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + C::BAR_QREADY;
+  uint64_t* q_free = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + C::BAR_QFREE;
+  const int par = un & 1;
+  // every stage warp is past unit un - 2, the buffers' previous user
+  if (un >= 2) {
+    const int prev = un - 2;
+    if (!mbar_try_wait(&q_free[prev & 1], (prev >> 1) & 1)) {
+      volatile int* abort_flag = &reinterpret_cast<KernelShared*>(smem + C::OFF_KS)->abort;
+      wait_slow(&q_free[prev & 1], (prev >> 1) & 1, abort_flag, p.status);
+    }
+  }
+  uint8_t* qb = smem + C::OFF_QB + par * (N * 64);
+  uint8_t* sfb = smem + C::OFF_SFB + par * 512;
+  float* wq = reinterpret_cast<float*>(smem + C::OFF_W) + par * N;
+  const int64_t row0 = static_cast<int64_t>(u.seq) * Q;
+  const uint8_t* qsrc = p.q_packed + row0 * H * 64;
+  for (int cc = etid; cc < 4 * N; cc += C::EPI_THREADS) {
+    const int g = cc / N, n = cc % N;
+    *reinterpret_cast<uint4*>(qb + g * N * 16 + n * 16) = __ldg(reinterpret_cast<const uint4*>(qsrc + n * 64 + g * 16));
+  }
+  for (int n = etid; n < 128; n += C::EPI_THREADS) {
+    uint32_t wv = 0x7F7F7F7Fu;
+    if (n < N) wv = __ldg(reinterpret_cast<const uint32_t*>(p.q_scale + (row0 * H + n) * 4));
+    *reinterpret_cast<uint32_t*>(sfb + (n & 31) * 16 + (n >> 5) * 4) = wv;
+  }
+  for (int x = etid; x < N; x += C::EPI_THREADS) wq[x] = __ldg(p.weights + row0 * H + x);
+  fence_proxy_async_smem();
+  named_barrier_sync(kEpiBarrier, C::EPI_THREADS);
+  if (etid == 0) {
+    tc_fence_after_sync();
+    tmem_copy_sf_chunk(tmem + C::SFB_COL + 4u * static_cast<uint32_t>(par), smem_addr(sfb));
+    tc_commit(&q_ready[par]);
+  }
+}
+
+// Head-weighted ReLU sum of one query row for this thread's key (TMEM lane): heads h of row r sit in
+// accumulator columns r * H + h. Fixed summation order (deterministic).
+template <int H>
+__device__ __forceinline__ float row_logit(uint32_t col, const float* wr) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f, s5 = 0.f, s6 = 0.f, s7 = 0.f;
+  if constexpr (H == 16) {
+    float v[16];
+    tmem_load_x16(col, v);
+#pragma unroll
+    for (int h = 0; h < 16; h += 8) {
+      const float4 wa = *reinterpret_cast<const float4*>(wr + h);
+      const float4 wb = *reinterpret_cast<const float4*>(wr + h + 4);
+      s0 = fmaf(wa.x, fmaxf(v[h], 0.f), s0);
+      s1 = fmaf(wa.y, fmaxf(v[h + 1], 0.f), s1);
+      s2 = fmaf(wa.z, fmaxf(v[h + 2], 0.f), s2);
+      s3 = fmaf(wa.w, fmaxf(v[h + 3], 0.f), s3);
+      s4 = fmaf(wb.x, fmaxf(v[h + 4], 0.f), s4);
+      s5 = fmaf(wb.y, fmaxf(v[h + 5], 0.f), s5);
+      s6 = fmaf(wb.z, fmaxf(v[h + 6], 0.f), s6);
+      s7 = fmaf(wb.w, fmaxf(v[h + 7], 0.f), s7);
+    }
+  } else if constexpr (H % 64 == 0) {
+    // packed pairs: heads (h, h+1) share one fma.rn.f32x2
+    unsigned long long p01 = 0ull, p23 = 0ull, p45 = 0ull, p67 = 0ull;
+#pragma unroll
+    for (int cc = 0; cc < H; cc += 64) {
+      float v[64];
+      tmem_load_2x32(col + cc, col + cc + 32, v);
+#pragma unroll
+      for (int h = 0; h < 64; h += 8) {
+        const float4 wa = *reinterpret_cast<const float4*>(wr + cc + h);
+        const float4 wb = *reinterpret_cast<const float4*>(wr + cc + h + 4);
+        fma2(p01, wa.x, wa.y, fmaxf(v[h], 0.f), fmaxf(v[h + 1], 0.f));
+        fma2(p23, wa.z, wa.w, fmaxf(v[h + 2], 0.f), fmaxf(v[h + 3], 0.f));
+        fma2(p45, wb.x, wb.y, fmaxf(v[h + 4], 0.f), fmaxf(v[h + 5], 0.f));
+        fma2(p67, wb.z, wb.w, fmaxf(v[h + 6], 0.f), fmaxf(v[h + 7], 0.f));
+      }
+    }
+    const float2 a01 = unpack2(p01), a23 = unpack2(p23), a45 = unpack2(p45), a67 = unpack2(p67);
+    s0 = a01.x; s1 = a01.y; s2 = a23.x; s3 = a23.y;
+    s4 = a45.x; s5 = a45.y; s6 = a67.x; s7 = a67.y;
+  } else {
+#pragma unroll
+    for (int cc = 0; cc < H; cc += 32) {
+      float v[32];
+      tmem_load_x32(col + cc, v);
+#pragma unroll
+      for (int h = 0; h < 32; h += 8) {
+        const float4 wa = *reinterpret_cast<const float4*>(wr + cc + h);
+        const float4 wb = *reinterpret_cast<const float4*>(wr + cc + h + 4);
+        s0 = fmaf(wa.x, fmaxf(v[h], 0.f), s0);
+        s1 = fmaf(wa.y, fmaxf(v[h + 1], 0.f), s1);
+        s2 = fmaf(wa.z, fmaxf(v[h + 2], 0.f), s2);
+        s3 = fmaf(wa.w, fmaxf(v[h + 3], 0.f), s3);
+        s4 = fmaf(wb.x, fmaxf(v[h + 4], 0.f), s4);
+        s5 = fmaf(wb.y, fmaxf(v[h + 5], 0.f), s5);
+        s6 = fmaf(wb.z, fmaxf(v[h + 6], 0.f), s6);
+        s7 = fmaf(wb.w, fmaxf(v[h + 7], 0.f), s7);
+      }
+    }
+  }
+  return ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+}
+
+// Epilogue warp (group grp, TMEM lane quarter qtr): logits of the tiles t with (st.tiles + t) %
+// GROUPS == grp into the row buffer; the query operands of the round's units, two units ahead.
+template <int H, int Q>
+__device__ __forceinline__ void stream_epilogue_warp(const DecodeParams& p, uint8_t* smem, int slot, int e, int lane) {
+  using C = DecodeCfg<H, Q>;
+  constexpr int N = C::N, ACC = C::ACC;
+  KernelShared* ks = reinterpret_cast<KernelShared*>(smem + C::OFF_KS);
+  volatile int* abort_flag = &ks->abort;
+  const uint32_t tmem = ks->tmem;
+  const DecodeSchedView v = sched_view(p, ks->h);
+  const int32_t* seq_ctx = v.seq_ctx;
+  const RoundInfo st = ks->round[slot];
+  const RangeIter it{v.units, st.uf, st.ul - st.uf};
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* acc_full = bars + 2 * C::STAGES;
+  uint64_t* acc_rel = acc_full + ACC;
+  const int grp = e >> 2;
+  const int qtr = (C::EPI_WARP0 + e) & 3;  // TMEM lane quarter = warp id % 4
+  const int etid = e * 32 + lane;
+  const int krow = qtr * 32 + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(qtr * 32) << 16;
+  uint32_t* lg = reinterpret_cast<uint32_t*>(smem + C::OFF_LG);
+  if (it.count > 0) prep_query<H, Q>(p, it.at(0), st.units, smem, tmem, etid);
+  if (it.count > 1) prep_query<H, Q>(p, it.at(1), st.units + 1, smem, tmem, etid);
+  int t0 = st.tiles;  // CTA-wide number of the unit's first tile
+  for (int i = 0; i < it.count; ++i) {
+    const DecodeUnit u = it.at(i);
+    const float* wsm = reinterpret_cast<const float*>(smem + C::OFF_W) + ((st.units + i) & 1) * N;
+    const int ctx = seq_ctx[u.seq];
+    const int ntiles = dunit_tiles(u);
+    for (int j = ((grp - t0) % C::GROUPS + C::GROUPS) % C::GROUPS; j < ntiles; j += C::GROUPS) {
+      const int tt = t0 + j;
+      const int a = tt % ACC;
+      bounded_wait(&acc_full[a], static_cast<uint32_t>(tt / ACC) & 1u, abort_flag, p.status);
+      tc_fence_after_sync();
+      float logit[Q];
+#pragma unroll
+      for (int r = 0; r < Q; ++r) logit[r] = row_logit<H>(tmem + lane_base + a * N + r * H, wsm + r * H);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_rel[a * C::REL_RING + (tt / ACC) % C::REL_RING]);
+      const int key = u.kb + j * kTileKeys + krow;
+      const int at = u.buf + j * kTileKeys + krow;  // < CAP: a range holds at most CAP keys
+#pragma unroll
+      for (int r = 0; r < Q; ++r) {
+        const bool valid = key < ctx - Q + 1 + r;
+        if (at < C::CAP) lg[r * C::CAP + at] = valid ? ordered_key(logit[r]) : 0u;
+        if (valid && p.logits_debug != nullptr && key < p.logits_stride)
+          p.logits_debug[(static_cast<int64_t>(u.seq) * Q + r) * p.logits_stride + key] = logit[r];
+      }
+    }
+    t0 += ntiles;
+    if (i + 2 < it.count) {
+      named_barrier_sync(kEpiBarrier, C::EPI_THREADS);  // every group is done with unit i's operand
+      prep_query<H, Q>(p, it.at(i + 2), st.units + i + 2, smem, tmem, etid);
+    }
+  }
+}
+
+// ---- selection phase ----------------------------------------------------------------------------
+
+__device__ __forceinline__ int clampi(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+// Keep every candidate (all) or those above T plus the first `need` equal to T, in token order:
+// out(position, key, token) for each kept candidate, positions dense from 0.
+template <class KeyAt, class TokAt, class Out>
+__device__ __forceinline__ void blk_emit(const Blk& B, KeyAt key, TokAt tok, int n, bool all, uint32_t T,
+                                         uint32_t need, Out out) {
+  const int2 run = blk_run(B, n);
+  uint32_t gt = 0, eq = 0;
+  if (all) {
+    gt = static_cast<uint32_t>(run.y - run.x);
+  } else {
+    for (int x = run.x; x < run.y; ++x) {
+      const uint32_t k = key(x);
+      gt += k > T ? 1u : 0u;
+      eq += k == T ? 1u : 0u;
+    }
+  }
+  const uint2 pre = blk_scan2(B, gt, eq, nullptr, nullptr);
+  uint32_t pos = pre.x + min(pre.y, need), eqr = pre.y;
+  if (gt + eq != 0u)
+    for (int x = run.x; x < run.y; ++x) {
+      const uint32_t k = key(x);
+      const bool eqk = !all && k == T;
+      const bool keep = all || k > T || (eqk && eqr < need);
+      if (keep) out(pos++, k, tok(x));
+      eqr += eqk ? 1u : 0u;
+    }
+}
+
+// Exact top-kk of n candidates in token order (first-level bin unknown: counted here).
+template <class KeyAt, class TokAt, class Out>
+__device__ __forceinline__ void blk_select(const Blk& B, KeyAt key, TokAt tok, int n, int kk, uint32_t* hist,
+                                           uint32_t* list, int list_cap, Out out) {
+  if (kk <= 0 || n <= 0) return;
+  if (kk >= n) {
+    blk_emit(B, key, tok, n, true, 0u, 0u, out);
+    return;
+  }
+  blk_zero(B, hist, kL1Bins);
+  B.sync();
+  for (int x = B.tid; x < n; x += B.nt) smem_red_add(&hist[key(x) >> kL1Shift], 1u);
+  B.sync();
+  const uint2 r = blk_find_bin(B, hist, kL1Bins, static_cast<uint32_t>(kk));
+  bool consistent = true;
+  const uint2 tn = blk_resolve(B, key, n, r.x, static_cast<uint32_t>(kk) - r.y, hist, list, list_cap, &consistent);
+  blk_emit(B, key, tok, n, false, tn.x, tn.y, out);
+}
+
+// Where a segment row's selection goes: the final output row (then padded to topk with -1 / -inf),
+// or the segment's list when its sequence has several segments.
+struct RowOut {
+  int32_t* idx;
+  float* val;      // nullable
+  uint2* list;     // non-null: a segment list instead
+  uint32_t limit;  // positions past the row's k are never written
+  __device__ __forceinline__ void operator()(uint32_t pos, uint32_t key, int tok) const {
+    if (pos >= limit) return;
+    if (list != nullptr) {
+      list[pos] = make_uint2(key, static_cast<uint32_t>(tok));
+    } else {
+      idx[pos] = tok;
+      if (val != nullptr) val[pos] = key_to_float(key);
+    }
+  }
+};
+
+__device__ __forceinline__ void pad_row(const Blk& B, const DecodeParams& p, int64_t row, int from) {
+  int32_t* oi = p.topk_idx + row * p.topk;
+  float* ov = p.topk_val != nullptr ? p.topk_val + row * p.topk : nullptr;
+  for (int x = from + B.tid; x < p.topk; x += B.nt) {
+    oi[x] = -1;
+    if (ov != nullptr) ov[x] = -__int_as_float(0x7f800000);
+  }
+}
+
+// Bounded wait by one thread until *ctr >= target; the answer is shared with the block.
+__device__ __forceinline__ bool blk_wait_count(const Blk& B, uint32_t* ctr, uint32_t target, volatile int* abort_flag,
+                                               int32_t* status) {
+  if (B.tid == 0) {
+    bool ok = *abort_flag == 0;
+    if (ok && ld_acquire_gpu(ctr) < target) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_gpu(ctr) < target) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          ok = false;
+          *abort_flag = 1;
+          set_status(status, IDX_FP4_DEV_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __threadfence();
+    B.sc[72] = ok ? 1u : 0u;
+  }
+  B.sync();
+  const bool ok = B.sc[72] != 0u;
+  B.sync();
+  return ok;
+}
+
+// Ticket after this CTA's writes for a segment row: true for the CTA that arrives last.
+__device__ __forceinline__ bool blk_ticket(const Blk& B, uint32_t* ctr, uint32_t count) {
+  B.sync();
+  if (B.tid == 0) {
+    __threadfence();
+    const uint32_t old = atom_add_acq_rel_gpu(ctr, 1u);
+    __threadfence();
+    B.sc[73] = old + 1u == count ? 1u : 0u;
+  }
+  B.sync();
+  const bool last = B.sc[73] != 0u;
+  B.sync();
+  return last;
+}
+
+struct SegCtx {
+  DecodeSeg sg;
+  int seg_id, q, row_end, kk;
+  int64_t out_row;
+};
+
+// Exact top-k of a sequence row over its segments' lists (a sequence spanning several rounds).
+template <int H, int Q>
+__device__ void merge_sequence(const DecodeParams& p, const DecodeSchedView& v, const DecodeWs& ws, int seq, int q,
+                               uint8_t* smem, const Blk& B) {
+  using C = DecodeCfg<H, Q>;
+  uint32_t* P = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* off = P + C::P_SOFF;
+  const int nseg = v.seq_nseg[seq], s0 = v.seq_seg0[seq];
+  const int ctx = v.seq_ctx[seq];
+  const int row_end = clampi(ctx - Q + 1 + q, 0, ctx);
+  if (B.tid == 0) {
+    uint32_t o = 0;
+    for (int s = 0; s < nseg && s < 1024; ++s) {
+      off[s] = o;
+      const DecodeSeg sg = v.segs[s0 + s];
+      o += static_cast<uint32_t>(min(p.topk, clampi(row_end - sg.kb, 0, sg.ke - sg.kb)));
+    }
+    off[min(nseg, 1024)] = o;
+  }
+  B.sync();
+  const int ns = min(nseg, 1024);
+  const int M = static_cast<int>(off[ns]);
+  auto at = [&](int x) {
+    int lo = 0, hi = ns - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (static_cast<int>(off[mid]) <= x) lo = mid; else hi = mid - 1;
+    }
+    return ws.seglists + (static_cast<int64_t>(s0 + lo) * Q + q) * p.topk + (x - static_cast<int>(off[lo]));
+  };
+  uint2* cand = reinterpret_cast<uint2*>(P + C::P_CAND);
+  const bool staged = M <= C::CCAP;
+  if (staged) {
+    for (int x = B.tid; x < M; x += B.nt) cand[x] = ldcg_u2(at(x));
+    B.sync();
+  }
+  auto key = [&](int x) { return staged ? cand[x].x : ldcg_u2(at(x)).x; };
+  auto tok = [&](int x) { return static_cast<int>(staged ? cand[x].y : ldcg_u2(at(x)).y); };
+  const int64_t row = static_cast<int64_t>(seq) * Q + q;
+  const int kk = min(p.topk, row_end);
+  RowOut out{p.topk_idx + row * p.topk, p.topk_val != nullptr ? p.topk_val + row * p.topk : nullptr, nullptr,
+             static_cast<uint32_t>(kk)};
+  blk_select(B, key, tok, M, kk, P + C::P_HIST, P + C::P_LIST, C::LIST_CAP, out);
+  pad_row(B, p, row, kk);
+  if (B.tid == 0) ws.seqsync[(static_cast<int64_t>(seq) * Q + q) * 4] = 0u;
+  B.sync();
+}
+
+// Writes a segment row's selection: to the final row, or to the segment list followed by the
+// sequence's ticket (the last segment to finish merges the lists).
+template <int H, int Q, class KeyAt, class TokAt>
+__device__ void finish_segment(const DecodeParams& p, const DecodeSchedView& v, const DecodeWs& ws, const SegCtx& s,
+                               KeyAt key, TokAt tok, int n, bool known, uint32_t bin, uint32_t above, uint8_t* smem,
+                               const Blk& B) {
+  using C = DecodeCfg<H, Q>;
+  uint32_t* P = reinterpret_cast<uint32_t*>(smem);
+  const int seq = s.sg.seq;
+  const int nseg = v.seq_nseg[seq];
+  RowOut out{p.topk_idx + s.out_row * p.topk, p.topk_val != nullptr ? p.topk_val + s.out_row * p.topk : nullptr,
+             nseg > 1 ? ws.seglists + (static_cast<int64_t>(s.seg_id) * Q + s.q) * p.topk : nullptr,
+             static_cast<uint32_t>(max(s.kk, 0))};
+  if (known && s.kk < n && s.kk > 0) {
+    bool consistent = true;
+    const uint2 tn = blk_resolve(B, key, n, bin, static_cast<uint32_t>(s.kk) - above, P + C::P_HIST, P + C::P_LIST,
+                                 C::LIST_CAP, &consistent);
+    if (!consistent && B.tid == 0) set_status(p.status, IDX_FP4_DEV_SYNC);
+    blk_emit(B, key, tok, n, false, tn.x, tn.y, out);
+  } else {
+    blk_select(B, key, tok, n, s.kk, P + C::P_HIST, P + C::P_LIST, C::LIST_CAP, out);
+  }
+  if (nseg <= 1) {
+    pad_row(B, p, s.out_row, s.kk);
+    B.sync();
+    return;
+  }
+  if (blk_ticket(B, &ws.seqsync[(static_cast<int64_t>(seq) * Q + s.q) * 4], static_cast<uint32_t>(nseg)))
+    merge_sequence<H, Q>(p, v, ws, seq, s.q, smem, B);
+}
+
+// Selection of one round's units of this CTA (the row buffer holds their logits).
+template <int H, int Q>
+__device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, const Blk& B) {
+  using C = DecodeCfg<H, Q>;
+  KernelShared* ks = reinterpret_cast<KernelShared*>(smem + C::OFF_KS);
+  volatile int* abort_flag = &ks->abort;
+  const DecodeSchedView v = sched_view(p, ks->h);
+  const DecodeWs ws = decode_ws_view(p.workspace, decode_caps_of(ks->h), ks->h.max_batch, Q);
+  const int uf = ks->round[slot].uf, ul = ks->round[slot].ul;
+  uint32_t* P = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* hist = P + C::P_HIST;
+  const uint32_t* lg = reinterpret_cast<const uint32_t*>(smem + C::OFF_LG);
+  const int topk = p.topk;
+  auto seg_ctx = [&](const DecodeUnit& u, int q) {
+    SegCtx s;
+    s.sg = v.segs[u.seg];
+    s.seg_id = u.seg;
+    s.q = q;
+    s.row_end = v.seq_ctx[u.seq] - Q + 1 + q;
+    s.kk = min(topk, clampi(s.row_end - s.sg.kb, 0, s.sg.ke - s.sg.kb));
+    s.out_row = static_cast<int64_t>(u.seq) * Q + q;
+    return s;
+  };
+  auto sync_word = [&](const SegCtx& s, int k) { return &ws.sync[(static_cast<int64_t>(s.seg_id) * Q + s.q) * 4 + k]; };
+  auto rec_base = [&](int unit, int q) {
+    return ws.records + q * ws.rec_stride + static_cast<int64_t>(v.units[unit].tile0) * kTileKeys + unit;
+  };
+  auto cand_base = [&](const SegCtx& s) { return ws.cands + s.q * ws.cand_stride + static_cast<int64_t>(s.sg.tile0) * kTileKeys; };
+
+  // Merge of a segment row by its last unit: the candidates (every key at or above the threshold
+  // bin, or every key of the row when `all`) in token order at the segment's candidate array.
+  auto merge_segment = [&](const SegCtx& s, int M, bool all, uint32_t bin, uint32_t above) {
+    const uint2* src = cand_base(s);
+    uint2* cand = reinterpret_cast<uint2*>(P + C::P_CAND);
+    const bool staged = M <= C::CCAP;
+    if (staged) {
+      for (int x = B.tid; x < M; x += B.nt) cand[x] = ldcg_u2(src + x);
+      B.sync();
+    }
+    auto key = [&](int x) { return staged ? cand[x].x : ldcg_u2(src + x).x; };
+    auto tok = [&](int x) { return static_cast<int>(staged ? cand[x].y : ldcg_u2(src + x).y); };
+    if (B.tid == 0) {
+      *sync_word(s, 0) = 0u;  // every unit has passed its wait on the published histograms
+      *sync_word(s, 1) = 0u;
+      if (M < s.kk) set_status(p.status, IDX_FP4_DEV_SYNC);
+    }
+    finish_segment<H, Q>(p, v, ws, s, key, tok, M, !all, bin, above, smem, B);
+  };
+
+  // Phase A: selections that need nobody else, and the published histograms of longer segments.
+  for (int i = uf; i < ul; ++i) {
+    const DecodeUnit u = v.units[i];
+    for (int q = 0; q < Q; ++q) {
+      const SegCtx s = seg_ctx(u, q);
+      const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
+      const uint32_t* keys = lg + q * C::CAP + u.buf;
+      auto key = [&](int x) { return keys[x]; };
+      auto tok = [&](int x) { return u.kb + x; };
+      if (s.sg.nunits == 1) {
+        finish_segment<H, Q>(p, v, ws, s, key, tok, un, false, 0u, 0u, smem, B);
+      } else if (s.kk >= clampi(s.row_end - s.sg.kb, 0, s.sg.ke - s.sg.kb)) {
+        // every key of the segment row is selected: each unit writes its keys at their place
+        uint2* dst = cand_base(s) + (u.kb - s.sg.kb);
+        for (int x = B.tid; x < un; x += B.nt) dst[x] = make_uint2(keys[x], static_cast<uint32_t>(u.kb + x));
+        if (blk_ticket(B, sync_word(s, 1), static_cast<uint32_t>(s.sg.nunits))) merge_segment(s, s.kk, true, 0u, 0u);
+      } else {
+        // histogram of the unit row; publish the bins from the unit's own k-th key's bin up
+        blk_zero(B, hist, kL1Bins);
+        B.sync();
+        for (int x = B.tid; x < un; x += B.nt) smem_red_add(&hist[keys[x] >> kL1Shift], 1u);
+        B.sync();
+        const uint32_t bu = un >= s.kk ? blk_find_bin(B, hist, kL1Bins, static_cast<uint32_t>(s.kk)).x : 0u;
+        const int nb = kL1Bins - static_cast<int>(bu);
+        const int per = (nb + B.nt - 1) / B.nt;
+        const int b0 = static_cast<int>(bu) + min(nb, B.tid * per), b1 = static_cast<int>(bu) + min(nb, B.tid * per + per);
+        uint32_t cnt = 0;
+        for (int b = b0; b < b1; ++b) cnt += hist[b] != 0u ? 1u : 0u;
+        uint32_t total = 0;
+        uint32_t o = blk_scan2(B, cnt, 0u, &total, nullptr).x;
+        uint32_t* rec = rec_base(i, q);
+        for (int b = b0; b < b1; ++b)
+          if (hist[b] != 0u) rec[1 + o++] = (static_cast<uint32_t>(b) << 17) | hist[b];
+        if (B.tid == 0) rec[0] = total;
+        blk_ticket(B, sync_word(s, 0), 0u);  // publish (the count is never the last one's)
+      }
+    }
+  }
+
+  // Phase B: the threshold bin of each longer segment from every unit's published bins, this unit's
+  // candidates, and the merge by the last unit.
+  for (int i = uf; i < ul; ++i) {
+    const DecodeUnit u = v.units[i];
+    for (int q = 0; q < Q; ++q) {
+      const SegCtx s = seg_ctx(u, q);
+      if (s.sg.nunits == 1 || s.kk >= clampi(s.row_end - s.sg.kb, 0, s.sg.ke - s.sg.kb)) continue;
+      const int nu = s.sg.nunits, fu = s.sg.first_unit;
+      if (!blk_wait_count(B, sync_word(s, 0), static_cast<uint32_t>(nu), abort_flag, p.status)) continue;
+      // record counts of every unit -> offsets (a contiguous chunk of units per thread)
+      uint32_t* uoff = P + C::P_UOFF;
+      uint32_t* ucnt = P + C::P_UCNT;
+      const int cper = (nu + B.nt - 1) / B.nt;
+      const int c0 = min(nu, B.tid * cper), c1 = min(nu, c0 + cper);
+      uint32_t mine = 0;
+      // (a count is at most the unit's keys and the number of bins: anything else could only be a
+      // workspace that was not zero-filled, and is clamped so that every read stays in the unit's area)
+      for (int j = c0; j < c1; ++j) {
+        const DecodeUnit uj = v.units[fu + j];
+        const uint32_t cap = static_cast<uint32_t>(min(kL1Bins, max(uj.ke - uj.kb, 0)));
+        const uint32_t c = min(ldcg_u32(rec_base(fu + j, q)), cap);
+        uoff[j] = c;
+        mine += c;
+      }
+      uint32_t R = 0;
+      uint32_t run = blk_scan2(B, mine, 0u, &R, nullptr).x;
+      for (int j = c0; j < c1; ++j) {
+        const uint32_t c = uoff[j];
+        uoff[j] = run;
+        run += c;
+      }
+      if (B.tid == 0) uoff[nu] = R;
+      blk_zero(B, hist, kL1Bins);
+      blk_zero(B, ucnt, nu);
+      B.sync();
+      auto unit_of = [&](int f) {
+        int lo = 0, hi = nu - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (static_cast<int>(uoff[mid]) <= f) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+      };
+      uint2* recs = reinterpret_cast<uint2*>(P + C::P_REC);
+      const bool staged = static_cast<int>(R) <= C::RCAP;
+      auto record = [&](int f) {
+        if (staged) return recs[f];
+        const int j = unit_of(f);
+        return make_uint2(ldcg_u32(rec_base(fu + j, q) + 1 + (f - static_cast<int>(uoff[j]))), static_cast<uint32_t>(j));
+      };
+      for (int f = B.tid; f < static_cast<int>(R); f += B.nt) {
+        const int j = unit_of(f);
+        const uint32_t r = ldcg_u32(rec_base(fu + j, q) + 1 + (f - static_cast<int>(uoff[j])));
+        if (staged) recs[f] = make_uint2(r, static_cast<uint32_t>(j));
+        smem_red_add(&hist[(r >> 17) & (kL1Bins - 1)], r & 0x1FFFFu);
+      }
+      B.sync();
+      const uint2 tb = blk_find_bin(B, hist, kL1Bins, static_cast<uint32_t>(s.kk));
+      const uint32_t bstar = tb.x, above = tb.y;
+      for (int f = B.tid; f < static_cast<int>(R); f += B.nt) {
+        const uint2 r = record(f);
+        if (((r.x >> 17) & (kL1Bins - 1)) >= bstar) smem_red_add(&ucnt[r.y], r.x & 0x1FFFFu);
+      }
+      B.sync();
+      // this unit's offset in the segment's candidate array, and the array's length
+      mine = 0;
+      for (int j = c0; j < c1; ++j) mine += ucnt[j];
+      uint32_t M = 0;
+      run = blk_scan2(B, mine, 0u, &M, nullptr).x;
+      for (int j = c0; j < c1; ++j) {
+        const uint32_t c = ucnt[j];
+        ucnt[j] = run;
+        run += c;
+      }
+      B.sync();
+      const uint32_t my_off = ucnt[i - fu];
+      // this unit's keys at or above the threshold bin, in token order
+      const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
+      const uint32_t* keys = lg + q * C::CAP + u.buf;
+      const int2 kr = blk_run(B, un);
+      uint32_t c = 0;
+      for (int x = kr.x; x < kr.y; ++x) c += (keys[x] >> kL1Shift) >= bstar ? 1u : 0u;
+      uint32_t o = my_off + blk_scan2(B, c, 0u, nullptr, nullptr).x;
+      // (offsets past the segment's own keys can only come from inconsistent counts: not written)
+      uint2* dst = cand_base(s);
+      const uint32_t seg_keys = static_cast<uint32_t>(s.sg.ke - s.sg.kb);
+      if (c != 0u)
+        for (int x = kr.x; x < kr.y; ++x) {
+          const uint32_t k = keys[x];
+          if ((k >> kL1Shift) >= bstar) {
+            if (o < seg_keys) dst[o] = make_uint2(k, static_cast<uint32_t>(u.kb + x));
+            ++o;
+          }
+        }
+      if (blk_ticket(B, sync_word(s, 1), static_cast<uint32_t>(nu)))
+        merge_segment(s, static_cast<int>(min(M, seg_keys)), false, bstar, above);
+    }
+  }
+}
+
+template <int H, int Q>
+__global__ void __launch_bounds__(DecodeCfg<H, Q>::THREADS, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DecodeCfg<H, Q>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  KernelShared* ks = reinterpret_cast<KernelShared*>(smem + C::OFF_KS);
+  if (threadIdx.x == 0) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    for (int s = 0; s < 2 * C::STAGES + C::ACC; ++s) mbar_init(&bars[s], 1);  // full, empty, acc_full
+    for (int x = 0; x < C::ACC * C::REL_RING; ++x) mbar_init(&bars[2 * C::STAGES + C::ACC + x], 4);
+    mbar_init(&bars[C::BAR_QREADY], 1);
+    mbar_init(&bars[C::BAR_QREADY + 1], 1);
+    mbar_init(&bars[C::BAR_QFREE], C::STAGES);
+    mbar_init(&bars[C::BAR_QFREE + 1], C::STAGES);
+    ks->abort = 0;
+    mbar_fence_init();
+  }
+  pdl_wait();
+  pdl_trigger();
+
+  // The schedule must belong to this call and the workspace must hold its layout (checks uniform
+  // across the grid; nothing is allocated yet).
+  {
+    const DecodeSchedHeader h = *static_cast<const DecodeSchedHeader*>(p.sched);
+    const DecodeCaps caps = decode_caps_of(h);
+    const bool ok = (smem_addr(smem) & 1023u) == 0u && h.magic == kDecodeMagic &&
+                    h.ctas == static_cast<int>(gridDim.x) && h.batch == p.batch && h.next_n == Q &&
+                    h.max_batch >= h.batch && decode_sched_bytes_for(h.max_batch, caps) <= p.sched_bytes;
+    if (!ok) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) set_status(p.status, IDX_FP4_DEV_BAD_SCHEDULE);
+      return;
+    }
+    const bool ws_ok = decode_ws_bytes_for(caps, h.max_batch, Q, p.topk) <= p.ws_bytes;
+    const DecodeSchedView v = sched_view(p, h);
+    // Rows with no keys (or nothing to run) come out empty; the schedule must match the contexts.
+    for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+      if (threadIdx.x == 0 && p.ctx_lens[b] >= 0 && p.ctx_lens[b] != v.seq_ctx[b])
+        set_status(p.status, IDX_FP4_DEV_BAD_SCHEDULE);
+      if (v.seq_nseg[b] == 0 || !ws_ok || h.ok == 0)
+        for (int x = threadIdx.x; x < Q * p.topk; x += C::THREADS) {
+          const int64_t at = static_cast<int64_t>(b) * Q * p.topk + x;
+          p.topk_idx[at] = -1;
+          if (p.topk_val != nullptr) p.topk_val[at] = -__int_as_float(0x7f800000);
+        }
+    }
+    if (!ws_ok) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) set_status(p.status, IDX_FP4_DEV_CAPACITY);
+      return;
+    }
+    if (h.ok == 0 || h.rounds == 0) return;
+    if (threadIdx.x == 0) ks->h = h;
+  }
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  if (warp == C::EPI_WARP0) tmem_alloc(&ks->tmem, C::TMEM_COLS);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  // Rounds: the epilogue warps publish each round's range and, after the round's stream, run its
+  // selection; the stage warps stream each round's tiles. Register budgets are set once per role.
+  const int rounds = ks->h.rounds;
+  if (warp < C::STAGES) {
+    warpgroup_regs_dec<C::STAGE_REGS>();
+    for (int r = 0; r < rounds; ++r) {
+      named_barrier_sync(kRoundBarrier, C::THREADS);
+      if (ks->round[r & 1].uf < ks->round[r & 1].ul) stream_stage_warp<H, Q>(p, smem, r & 1, warp, lane);
+    }
+  } else {
+    warpgroup_regs_inc<C::EPI_REGS>();
+    const int etid = static_cast<int>(threadIdx.x) - C::EPI_WARP0 * 32;
+    const Blk B{etid, C::EPI_THREADS, kSelBarrier, reinterpret_cast<uint32_t*>(smem + C::OFF_SCR)};
+    int tiles = 0, units = 0;  // streamed in earlier rounds (kept by every epilogue thread alike)
+    for (int r = 0; r < rounds; ++r) {
+      const int slot = r & 1;
+      const DecodeSchedView v = sched_view(p, ks->h);
+      const int ri = r * ks->h.ctas + static_cast<int>(blockIdx.x);
+      const int uf = v.range_first[ri], ul = v.range_first[ri + 1];
+      if (etid == 0) ks->round[slot] = RoundInfo{uf, ul, tiles, units};
+      fence_proxy_async_smem();  // the selection's writes to the stage area precede the bulk copies
+      named_barrier_sync(kRoundBarrier, C::THREADS);
+      if (uf >= ul) continue;
+      stream_epilogue_warp<H, Q>(p, smem, slot, warp - C::EPI_WARP0, lane);
+      B.sync();  // every tile is read out: the stage area is free and the row buffer complete
+      select_round<H, Q>(p, smem, slot, B);
+      for (int i = uf; i < ul; ++i) tiles += dunit_tiles(v.units[i]);
+      units += ul - uf;
+      B.sync();
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == C::EPI_WARP0) {
+    tc_fence_after_sync();
+    tmem_dealloc(ks->tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+template <int H, int Q>
+static cudaError_t launch_decode_t(const DecodeParams& p, int grid, cudaStream_t stream) {
+  using C = DecodeCfg<H, Q>;
+  cudaError_t e = set_smem_once<decode_kernel<H, Q>>(C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_kernel<H, Q>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, 1, true, p);
+}
+
+
+}  // namespace idxfp4

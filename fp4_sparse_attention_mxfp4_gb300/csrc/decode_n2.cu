@@ -1,0 +1,15 @@
+// Decode kernel instantiations for 2 query rows per sequence.
+#include "decode_kernel.cuh"
+
+namespace idxfp4 {
+
+cudaError_t launch_decode_n2(const DecodeParams& p, int heads, int grid, cudaStream_t stream) {
+  switch (heads) {
+    case 16: return launch_decode_t<16, 2>(p, grid, stream);
+    case 32: return launch_decode_t<32, 2>(p, grid, stream);
+    case 64: return launch_decode_t<64, 2>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace idxfp4

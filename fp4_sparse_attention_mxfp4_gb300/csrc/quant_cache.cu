@@ -108,7 +108,7 @@ cudaError_t launch_quant_and_cache(const uint16_t* k, int64_t num_tokens, const 
   const int64_t blocks_needed = (vecs + 7) / 8;  // 8 warps per block
   const int blocks = static_cast<int>(blocks_needed < static_cast<int64_t>(num_sms) * 16 ? blocks_needed
                                                                                           : static_cast<int64_t>(num_sms) * 16);
-  return launch_pdl(quant_and_cache_kernel, dim3(blocks), dim3(256), 0, stream, 1, k, num_tokens, slots, kv_packed,
+  return launch_pdl(quant_and_cache_kernel, dim3(blocks), dim3(256), 0, stream, 1, false, k, num_tokens, slots, kv_packed,
                     kv_scale, num_pages, q, num_q_vec, q_packed, q_scale, status);
 }
 

@@ -1,33 +1,29 @@
-// Scorer: MXFP4 keys x MXFP4 query heads on tcgen05 block-scaled MMA, fused head-weighted
-// ReLU reduction, fused exact top-k. Shared by decode (one query row per unit) and prefill
-// (up to two rows of one request per unit).
+// Prefill scorer: MXFP4 keys x MXFP4 query heads on tcgen05 block-scaled MMA, fused head-weighted
+// ReLU reduction, fused exact top-k, for up to two query rows of one request per unit.
 //
 // Method ("Score a DSA sparse indexer in FP4", squashed commit message and PR body):
 //   logit[q, t] = sum_h w[q, h] * relu(q_h . k_t), keys read in place from the paged two-plane
-//   FP4 index region; the decode top-k is bounded by the row's context and the prefill top-k by
-//   the row's [0, row_end) range.
+//   FP4 index region; the prefill top-k is bounded by the row's [0, row_end) range.
 //
 // GB300 design (the pages' kernels target MI355X MFMA; this is a fresh design):
 //   * A 128-key tile (two pages) is the MMA M dimension, query rows x heads the N dimension:
 //     D[128 x N] = K[128 x 128] . Q^T, as two K=64 tcgen05.mma kind::mxf4 block-scaled MMAs
 //     accumulating fp32 in TMEM. TMEM lane = key, so the head sum is thread-local.
-//   * Eight producer warps each own one stage of an 8-stage ring and fill it with 1-D bulk TMA
-//     copies (cp.async.bulk), the ten copies of a tile spread over ten lanes: a page's four 1 KB
-//     group chunks land interleaved with the tile's other page, which makes the stage a canonical
-//     no-swizzle K-major operand (LBO 2048 B between 32-dim chunks, SBO 128 B between 8-key
-//     groups). Bulk copies issued by one warp are processed one after another, so the stream
-//     rate grows with the number of issuing warps; eight reach the HBM copy rate.
-//   * One MMA warp rebuilds each stage's scale bytes from the cache's 16x4-transposed order into
-//     the tensor core's scale-factor layout (key m at lane m%32, column m/32), copies them to
+//   * Twelve stage warps each own one stage of a 12-stage ring and fill it with 1-D bulk copies
+//     (cp.async.bulk): a page's four 1 KB group chunks land interleaved with the tile's other page,
+//     which makes the stage a canonical no-swizzle K-major operand (LBO 2048 B between 32-dim
+//     chunks, SBO 128 B between 8-key groups). The same warp rebuilds the tile's scale bytes from
+//     the cache's 16x4-transposed order into the tensor core's scale-factor layout, copies them to
 //     TMEM with tcgen05.cp and issues the MMAs; tcgen05.commit frees the stage and hands the
 //     accumulator to the epilogue.
-//   * Four epilogue warps (one per TMEM lane quarter) read the accumulator with tcgen05.ld, form
-//     each key's logit in a fixed order, store its order-preserving key in a shared-memory row
-//     buffer and count it in a per-warp histogram. At the end of a unit an exact radix select
-//     finds the k-th key and a stable pass writes the selected keys in token order. The logit
-//     row never reaches global memory (unless a debug buffer is passed).
-//   * Persistent grid, one CTA per SM; every on-chip wait is bounded and reports a timeout in the
-//     status word instead of hanging.
+//   * Epilogue groups of four warps (one per TMEM lane quarter) read the accumulator with
+//     tcgen05.ld, form each key's logit in a fixed order, store its order-preserving key in a
+//     shared-memory row buffer and count it in a packed histogram. At the end of a unit an exact
+//     radix select finds the k-th key and a stable pass writes the selected keys in token order.
+//     The logit row never reaches global memory (unless a debug buffer is passed).
+//   * Rows longer than one unit's share are scored in key chunks whose candidate lists are merged
+//     by a cluster kernel. Persistent grid, one CTA per SM; every on-chip wait is bounded and
+//     reports a timeout in the status word instead of hanging.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -107,13 +103,8 @@ struct ScorerParams {
   int64_t num_pages;
   const int32_t* block_tables;
   int bt_stride;
-  // unit list: decode (sched != nullptr) uses the schedule's per-CTA table; prefill strides
-  // over the workspace's unit list by the grid
-  const void* sched;
-  size_t sched_bytes;
-  const PrefillSchedHeader* prefill;
-  int expect_batch;
-  const int32_t* row_ends;       // prefill per-row key ends (nullptr: the unit's ke)
+  const PrefillSchedHeader* prefill;  // the call's unit list, strided over by the grid
+  const int32_t* row_ends;       // per-row key ends
   int topk;
   int32_t* topk_idx;
   float* topk_val;
@@ -122,7 +113,6 @@ struct ScorerParams {
   float* logits_debug;
   int64_t logits_stride;
   int32_t* status;
-  int stream_once;               // 1: keys are read once (decode) -> L2 evict-first
 };
 
 struct UnitIter {
@@ -132,30 +122,19 @@ struct UnitIter {
   __device__ __forceinline__ Unit at(int i) const { return units[first + i * stride]; }
 };
 
-// This CTA's units; `ok` is false when the schedule does not belong to this call.
+// This CTA's units (every gridDim-th of the call's list); `ok` is false when the workspace holds
+// no unit list of this call.
 __device__ __forceinline__ UnitIter unit_range(const ScorerParams& p) {
   UnitIter it{};
   const int c = blockIdx.x;
-  if (p.sched != nullptr) {
-    const DecodeSchedHeader* h = static_cast<const DecodeSchedHeader*>(p.sched);
-    it.ok = h->magic == kDecodeMagic && h->ctas == static_cast<int>(gridDim.x) && h->batch == p.expect_batch &&
-            h->max_batch >= h->batch && decode_sched_bytes_for(h->max_batch, h->units_cap) <= p.sched_bytes;
-    if (!it.ok) return it;
-    const DecodeSchedView v = decode_sched_view(const_cast<void*>(p.sched), h->max_batch);
-    it.units = v.units;
-    it.first = v.cta_first[c];
-    it.count = v.cta_count[c];
-    it.stride = 1;
-  } else {
-    it.ok = p.prefill->magic == kPrefillMagic;
-    if (!it.ok) return it;
-    const int n = p.prefill->num_units;
-    it.units = reinterpret_cast<const Unit*>(reinterpret_cast<const char*>(p.prefill) +
-                                             prefill_units_offset(p.prefill->num_rows));
-    it.first = c;
-    it.count = c < n ? (n - c + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 0;
-    it.stride = gridDim.x;
-  }
+  it.ok = p.prefill->magic == kPrefillMagic;
+  if (!it.ok) return it;
+  const int n = p.prefill->num_units;
+  it.units = reinterpret_cast<const Unit*>(reinterpret_cast<const char*>(p.prefill) +
+                                           prefill_units_offset(p.prefill->num_rows));
+  it.first = c;
+  it.count = c < n ? (n - c + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) : 0;
+  it.stride = gridDim.x;
   return it;
 }
 
@@ -210,7 +189,7 @@ __device__ __forceinline__ int load_tile_page(const ScorerParams& p, const Curso
   const int lp = c.u.kb / kPage + 2 * c.j + lane;
   const bool needed = lane == 0 || (lane == 1 && c.u.kb + c.j * kTileKeys + kPage < c.u.ke);
   if (!needed) return -1;
-  if (lp >= p.bt_stride) return -2;
+  if (lp < 0 || lp >= p.bt_stride) return -2;
   return p.block_tables[static_cast<int64_t>(c.u.table) * p.bt_stride + lp];
 }
 
@@ -274,7 +253,6 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
     // instruction occupies its issuing warp or thread for a long time; one stage per warp also
     // keeps every wait on a barrier this warp alone advances.
     const int ps = warp;
-    const uint64_t pol = policy_evict_first();
     uint8_t* stage = smem + C::OFF_PACKED + ps * 8192;
     uint8_t* sfa_s = smem + C::OFF_SFA + ps * 512;
     const uint64_t a_desc = smem_desc(smem_addr(stage), 2048, 128);
@@ -321,10 +299,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         const int64_t pid = pg == 0 ? pid0 : pid1;
         uint8_t* dst = stage + k * 2048 + pg * 1024;
         const uint8_t* src = p.kv_packed + pid * kPageBytes + k * 1024;
-        if (p.stream_once)
-          bulk_load_evict_first(dst, src, 1024, &full_bar[ps], pol);
-        else
-          bulk_load(dst, src, 1024, &full_bar[ps]);
+        bulk_load(dst, src, 1024, &full_bar[ps]);
       }
       // scale bytes: plain loads, in flight together with the bulk copies
       uint32_t w0[4], w1[4];
@@ -443,7 +418,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
 #pragma unroll
       for (int r = 0; r < Q; ++r) {
         int ee = 0;
-        if (r < u.nq) ee = p.row_ends != nullptr ? min(max(p.row_ends[u.row + r], 0), u.ke) : u.ke;
+        if (r < u.nq) ee = min(max(p.row_ends[u.row + r], 0), u.ke);
         end[r] = ee;
       }
       const int ntiles = unit_tiles(u);
@@ -616,8 +591,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
 }
 
 // ---------------------------------------------------------------------------------------------
-// Merge of split rows (decode sequences spread over several units, prefill rows cut into key
-// chunks). A row's candidate lists (each exactly its unit's top-min(k, keys), in token order)
+// Merge of split prefill rows (rows cut into key chunks). A row's candidate lists (each exactly its unit's top-min(k, keys), in token order)
 // are merged by one cluster of kMergeG CTAs: CTA r takes the r-th share of the lists'
 // concatenation and streams it from L2 in every pass. Each CTA counts its share into local
 // radix histograms; the cluster sums them through distributed shared memory, so every CTA
@@ -625,7 +599,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
 // counts of the CTAs before it, which keeps the output in token order. Keys are first shifted
 // past the bits that all the row's candidates share, so that the first radix level spreads
 // them over its bins (the candidates are the top of the row and would otherwise fill a few
-// bins). Also writes the all-padding output of decode sequences with no keys.
+// bins).
 constexpr int kMergeG = 8;               // CTAs per row (one cluster)
 constexpr int kMergeThreads = 256;
 constexpr int kMergeNW = kMergeThreads / 32;
@@ -641,11 +615,7 @@ constexpr size_t kMergeSmem =
     (2 * kMergeStage + 2048 + 2048 + kMergeCbuf + kMergeUnion + kMergeMaxLists + 1 + 64 + 64 + 8) * 4;
 
 struct MergeParams {
-  const void* sched;                 // decode: the schedule, else nullptr
-  size_t sched_bytes;
-  const int32_t* ctx_lens;
-  int batch;
-  const PrefillSchedHeader* prefill; // prefill: the workspace header, else nullptr
+  const PrefillSchedHeader* prefill; // the workspace header
   int topk;
   const uint2* cand;
   int64_t cand_slots;
@@ -685,36 +655,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
   uint32_t* eqw = sc + 32;  // per warp: the smallest key of any list
   // Row setup: every CTA of the cluster reads the same row, so every early return below is
   // taken by the whole cluster.
-  int first, nu, stride, kk;
-  if (mp.sched != nullptr) {
-    const DecodeSchedHeader* h = static_cast<const DecodeSchedHeader*>(mp.sched);
-    if (h->magic != kDecodeMagic || h->batch != mp.batch || h->max_batch < mp.batch ||
-        decode_sched_bytes_for(h->max_batch, h->units_cap) > mp.sched_bytes)
-      return;  // flagged by the scorer
-    const DecodeSchedView v = decode_sched_view(const_cast<void*>(mp.sched), h->max_batch);
-    const int ctx = v.seq_ctx[row];
-    nu = v.seq_units[row];
-    first = v.seq_first[row];
-    stride = 1;
-    kk = min(topk, ctx);
-    if (rank == 0 && tid == 0 && mp.ctx_lens[row] >= 0 && mp.ctx_lens[row] != ctx)
-      set_status(mp.status, IDX_FP4_DEV_BAD_SCHEDULE);
-    if (nu == 0) {
-      if (rank == 0)
-        for (int e = tid; e < topk; e += kMergeThreads) {
-          mp.topk_idx[static_cast<int64_t>(row) * topk + e] = -1;
-          if (mp.topk_val != nullptr) mp.topk_val[static_cast<int64_t>(row) * topk + e] = -__int_as_float(0x7f800000);
-        }
-      return;
-    }
-  } else {
-    if (mp.prefill->magic != kPrefillMagic) return;
-    const int4 rm = reinterpret_cast<const int4*>(mp.prefill + 1)[row];
-    first = rm.x;
-    nu = rm.y;
-    stride = mp.prefill->rows_per_unit;
-    kk = min(topk, rm.z);
-  }
+  if (mp.prefill->magic != kPrefillMagic) return;
+  const int4 rm = reinterpret_cast<const int4*>(mp.prefill + 1)[row];
+  const int first = rm.x, nu = rm.y, stride = mp.prefill->rows_per_unit;
+  const int kk = min(topk, rm.z);
   if (nu <= 1) return;  // written by the scorer
   if (nu > kMergeMaxLists) {
     if (rank == 0 && tid == 0) set_status(mp.status, IDX_FP4_DEV_CAPACITY);
@@ -1136,41 +1080,18 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const __grid_const
 }
 
 cudaError_t launch_merge(const MergeParams& mp, int rows, cudaStream_t stream) {
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = set_smem_once<merge_kernel>(kMergeSmem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMergeSmem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
   return launch_pdl(merge_kernel, dim3(static_cast<unsigned>(rows) * kMergeG), dim3(kMergeThreads), kMergeSmem, stream,
-                    kMergeG, mp);
-}
-
-// The shared-memory opt-in is set once per device (so that a launch inside stream capture is
-// only a launch).
-template <class Kernel>
-cudaError_t ensure_smem(Kernel k, size_t bytes, bool (&configured)[64]) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
-  return cudaSuccess;
+                    kMergeG, false, mp);
 }
 
 template <int H, int Q>
 cudaError_t launch_scorer_t(const ScorerParams& p, int grid, cudaStream_t stream) {
   using C = ScorerCfg<H, Q>;
-  static bool configured[64] = {};
-  cudaError_t e = ensure_smem(scorer_kernel<H, Q>, C::SMEM_BYTES, configured);
+  cudaError_t e = set_smem_once<scorer_kernel<H, Q>>(C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return launch_pdl(scorer_kernel<H, Q>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, 1, p);
+  return launch_pdl(scorer_kernel<H, Q>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, 1, false, p);
 }
 
 template <int Q>
@@ -1184,52 +1105,6 @@ cudaError_t launch_scorer_h(int H, const ScorerParams& p, int grid, cudaStream_t
 }
 
 }  // namespace
-
-cudaError_t launch_decode(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
-                          const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
-                          const int32_t* block_tables, int bt_stride, const int32_t* ctx_lens, int batch, int H,
-                          int topk, const void* sched, size_t sched_bytes, void* workspace, int64_t cand_slots,
-                          int32_t* topk_idx, float* topk_val, float* logits_debug, int64_t logits_stride,
-                          int32_t* status, int grid, cudaStream_t stream) {
-  ScorerParams p{};
-  p.q_packed = q_packed;
-  p.q_scale = q_scale;
-  p.weights = weights;
-  p.kv_packed = kv_packed;
-  p.kv_scale = kv_scale;
-  p.num_pages = num_pages;
-  p.block_tables = block_tables;
-  p.bt_stride = bt_stride;
-  p.sched = sched;
-  p.sched_bytes = sched_bytes;
-  p.prefill = nullptr;
-  p.expect_batch = batch;
-  p.row_ends = nullptr;
-  p.topk = topk;
-  p.topk_idx = topk_idx;
-  p.topk_val = topk_val;
-  p.cand = static_cast<uint2*>(workspace);
-  p.cand_slots = cand_slots;
-  p.logits_debug = logits_debug;
-  p.logits_stride = logits_stride;
-  p.status = status;
-  p.stream_once = 1;
-  cudaError_t e = H == 128 ? launch_scorer_t<128, 1>(p, grid, stream) : launch_scorer_h<1>(H, p, grid, stream);
-  if (e != cudaSuccess) return e;
-  MergeParams mp{};
-  mp.sched = sched;
-  mp.sched_bytes = sched_bytes;
-  mp.ctx_lens = ctx_lens;
-  mp.batch = batch;
-  mp.prefill = nullptr;
-  mp.topk = topk;
-  mp.cand = p.cand;
-  mp.cand_slots = cand_slots;
-  mp.topk_idx = topk_idx;
-  mp.topk_val = topk_val;
-  mp.status = status;
-  return launch_merge(mp, batch, stream);
-}
 
 cudaError_t launch_prefill(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
                            const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
@@ -1247,7 +1122,6 @@ cudaError_t launch_prefill(const uint8_t* q_packed, const uint8_t* q_scale, cons
   p.num_pages = num_pages;
   p.block_tables = block_tables;
   p.bt_stride = bt_stride;
-  p.sched = nullptr;
   p.prefill = hdr;
   p.row_ends = row_ends;
   p.topk = topk;
@@ -1258,11 +1132,9 @@ cudaError_t launch_prefill(const uint8_t* q_packed, const uint8_t* q_scale, cons
   p.logits_debug = logits_debug;
   p.logits_stride = logits_stride;
   p.status = status;
-  p.stream_once = 0;
   cudaError_t e = H == 128 ? launch_scorer_t<128, 1>(p, grid, stream) : launch_scorer_h<2>(H, p, grid, stream);
   if (e != cudaSuccess || slots_cap == 0) return e;
   MergeParams mp{};
-  mp.sched = nullptr;
   mp.prefill = hdr;
   mp.topk = topk;
   mp.cand = p.cand;

@@ -1,7 +1,7 @@
 // Decode for callers that cannot allocate device memory.
 //
-// The regular decode call takes a caller-owned workspace for the candidate lists of sequences
-// that are split across CTAs. Some callers have no way to provide one: code that runs where
+// The regular decode call takes a caller-owned workspace for the exchange between the CTAs that
+// share a sequence (published histograms, candidate lists, a few counters). Some callers have no way to provide one: code that runs where
 // cudaMalloc is not allowed (inside an allocator hook or a custom memory pool that must not
 // re-enter itself, in an embedding runtime that owns every device allocation, or on a path
 // that must never block on the allocator). For them this file keeps that workspace in a fixed
@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "decode_sched.cuh"
 #include "idx_fp4.h"
 
 namespace idxfp4 {
@@ -24,7 +25,7 @@ namespace {
 constexpr size_t kStaticScratchBytes = IDX_FP4_STATIC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
-// Candidate slots of the decode calls made through idx_fp4_decode_logits_topk_static.
+// Workspace of the decode calls made through idx_fp4_decode_logits_topk_static (zero at load).
 static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mutex;
@@ -47,30 +48,13 @@ cudaError_t scratch_on_current_device(void** out) {
   return cudaSuccess;
 }
 
-// Upper bound on the units (and so candidate slots) of a schedule built for `batch` sequences of
-// at most `max_ctx` keys on a grid of `ctas`: each range of at most 128 tiles contributes one,
-// plus one per CTA range end and one per sequence boundary.
-int64_t units_bound(int batch, int64_t max_ctx, int ctas) {
-  const int64_t tiles = static_cast<int64_t>(batch) * ((max_ctx + kTileKeys - 1) / kTileKeys);
-  const int64_t per = unit_key_cap(1) / kTileKeys;
-  return (tiles + per - 1) / per + ctas + batch;
-}
-
 }  // namespace
 }  // namespace idxfp4
 
 extern "C" {
 
 size_t idx_fp4_decode_static_bytes(int batch, int64_t max_ctx, int topk) {
-  using namespace idxfp4;
-  if (batch < 1 || batch > kMaxBatch || max_ctx < 0 || max_ctx > (int64_t{1} << 30) || topk < 1 ||
-      topk > IDX_FP4_MAX_TOPK)
-    return 0;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  const int ctas = sms < kMaxCtas ? sms : kMaxCtas;
-  return decode_workspace_bytes_for(units_bound(batch, max_ctx, ctas), topk);
+  return idx_fp4_decode_workspace_bytes(batch, max_ctx, topk);
 }
 
 int idx_fp4_decode_logits_topk_static(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
@@ -85,16 +69,20 @@ int idx_fp4_decode_logits_topk_static(const uint8_t* q_packed, const uint8_t* q_
   if (batch < 0 || batch > kMaxBatch || max_ctx < 0 || max_ctx > (int64_t{1} << 30)) return IDX_FP4_ERR_ARG;
   if (batch == 0) return IDX_FP4_OK;
   const size_t need = idx_fp4_decode_static_bytes(batch, max_ctx, topk);
-  if (need == 0) return IDX_FP4_ERR_CUDA;
+  if (need == 0) return IDX_FP4_ERR_ARG;
   if (need > kStaticScratchBytes) return IDX_FP4_ERR_CAPACITY;
   void* scratch = nullptr;
   if (scratch_on_current_device(&scratch) != cudaSuccess) return IDX_FP4_ERR_CUDA;
-  // Nothing in the scratch needs to start at zero: every candidate list the merge reads is
-  // written earlier in the same call.
+  // The layout is the regular call's for a schedule built with (batch, max_ctx). Its
+  // synchronisation words must start at zero: a call leaves them at zero, but one that gave up
+  // waiting may not, so they are cleared on the stream first (a memset, not an allocation).
+  const DecodeCaps caps = decode_caps(batch, max_ctx);
+  if (cudaMemsetAsync(scratch, 0, decode_ws_sync_bytes(caps, batch, 1), stream) != cudaSuccess)
+    return IDX_FP4_ERR_CUDA;
   return idx_fp4_decode_logits_topk(q_packed, q_scale, weights, kv_packed, kv_scale, num_pages, block_tables,
                                     block_table_stride, ctx_lens_dev, batch, num_heads, topk, sched_dev,
-                                    sched_bytes, scratch, kStaticScratchBytes, topk_idx, topk_val, logits_debug,
-                                    logits_stride, status_dev, stream);
+                                    sched_bytes, scratch, need, topk_idx, topk_val, logits_debug, logits_stride,
+                                    status_dev, stream);
 }
 
 }  // extern "C"

@@ -24,11 +24,18 @@
  *
  * Conventions for every call
  *   - Pointers marked "device" are device pointers owned by the caller; the library
- *     keeps no global state and allocates no memory. Host sizing functions say how large
- *     the caller's schedule and workspace buffers must be.
- *   - Every call is asynchronous on `stream`, launches only kernels, and may be captured
- *     into a CUDA graph. Nothing is sized from device data, so a captured graph may be
- *     replayed after the device-side inputs (context lengths, row ends, tables) change.
+ *     allocates no memory. Host sizing functions (which query nothing on the device) say how
+ *     large the caller's schedule and workspace buffers must be. The one exception to
+ *     "no device state of its own" is idx_fp4_decode_logits_topk_static (end of this file):
+ *     a fixed array on every GPU that loads the library, whose first call per device must
+ *     come before any stream capture, and whose overlapping calls race. On the host the
+ *     library caches, per device and kernel, that the kernel's shared-memory attribute was
+ *     set (under a lock), and the static array's device address.
+ *   - Every other call is asynchronous on `stream`, launches only kernels, and may be
+ *     captured into a CUDA graph. Nothing is sized from device data, so a captured graph may
+ *     be replayed after the device-side inputs (context lengths, row ends, tables) change.
+ *     The decode scorer is a cooperative launch of one CTA per SM (its CTAs exchange
+ *     histograms through the workspace and wait for each other, boundedly).
  *   - Kernels are launched with programmatic stream serialization: each waits for the
  *     preceding grid in the stream to complete before it touches memory, then lets the next
  *     kernel begin launching. Stream order is unchanged for ordinary kernels, copies and
@@ -91,6 +98,8 @@ extern "C" {
 #define IDX_FP4_DEV_TIMEOUT 0x20      /* a bounded on-chip wait gave up (results undefined) */
 #define IDX_FP4_DEV_CAPACITY 0x40     /* the schedule or workspace was sized for smaller contexts than
                                          the call met (affected rows come out as -1) */
+#define IDX_FP4_DEV_SYNC 0x80         /* decode: the CTAs sharing a sequence saw inconsistent counts (a
+                                         workspace not zero-filled, or calls overlapping on it) */
 
 #define IDX_FP4_MAX_TOPK 2048
 #define IDX_FP4_MAX_BATCH 4096        /* sequences per decode call, requests per prefill call */
@@ -114,8 +123,9 @@ int idx_fp4_quant_and_cache(const uint16_t *k_bf16, int64_t num_tokens, const in
                             int64_t num_q_rows, int num_heads, uint8_t *q_packed, uint8_t *q_scale,
                             int32_t *status_dev, cudaStream_t stream);
 
-/* Bytes of the decode schedule buffer for up to `max_batch` sequences of up to `max_ctx` keys
- * (host; queries nothing on the device; 0 for invalid arguments). */
+/* Bytes of the decode schedule buffer for up to `max_batch` sequences of up to `max_ctx` keys,
+ * for any next_n and any GPU of up to 1024 SMs (host only; 0 for invalid arguments, or when
+ * max_batch * ceil(max_ctx / 128) exceeds 2^31 - 1). */
 size_t idx_fp4_decode_schedule_bytes(int max_batch, int64_t max_ctx);
 
 /* Build the decode CTA schedule once per step, before the layers; every decode call of the
@@ -127,14 +137,20 @@ size_t idx_fp4_decode_schedule_bytes(int max_batch, int64_t max_ctx);
  *   batch <= max_batch; max_ctx bounds every context (larger sets IDX_FP4_DEV_BAD_CTX and the
  *   sequence is treated as empty)
  *   sched_dev     device buffer of sched_bytes >= idx_fp4_decode_schedule_bytes(max_batch, max_ctx)
- * The schedule targets the current device's SM count; use it on that device. Each CTA gets an
- * equal block of tile ranges of at most 16384 keys; a sequence spread over several ranges is
- * merged inside idx_fp4_decode_logits_topk. */
+ * The schedule targets the current device's SM count; use it on that device. All sequences'
+ * 128-key tiles are laid end to end and cut into rounds of one equal range per SM, a range
+ * holding at most 16384 keys (one query row per sequence); a sequence spread over several
+ * ranges is selected jointly by the CTAs holding it, inside idx_fp4_decode_logits_topk. */
 int idx_fp4_build_decode_schedule(const int32_t *ctx_lens_dev, int batch, int max_batch, int64_t max_ctx,
                                   void *sched_dev, size_t sched_bytes, int32_t *status_dev, cudaStream_t stream);
 
-/* Bytes of the decode workspace (candidate lists of sequences split across CTAs) for schedules
- * built with (max_batch, max_ctx) and the given topk (host; 0 for invalid arguments). */
+/* Bytes of the decode workspace for schedules built with (max_batch, max_ctx) and the given topk
+ * (host only; 0 for invalid arguments). The workspace holds the exchange between the CTAs that
+ * share a sequence: each unit's published histogram bins, the sequence's candidate keys (at most
+ * 8 bytes per key of the batch) and a few counters. It must be zero-filled before its first use;
+ * every call leaves its counters at zero again, except a call that reports IDX_FP4_DEV_TIMEOUT,
+ * after which the caller zero-fills the workspace again. Calls that share a workspace must not
+ * overlap on the GPU. */
 size_t idx_fp4_decode_workspace_bytes(int max_batch, int64_t max_ctx, int topk);
 
 /* Decode: one query row per sequence b scores keys [0, ctx_lens[b]) through block_tables[b]
@@ -147,7 +163,8 @@ size_t idx_fp4_decode_workspace_bytes(int max_batch, int64_t max_ctx, int topk);
  *   ctx_lens_dev   the vector the schedule was built from (checked against it)
  *   sched_dev/sched_bytes   from idx_fp4_build_decode_schedule for this batch
  *   workspace      device, >= idx_fp4_decode_workspace_bytes(max_batch, max_ctx, topk) for the
- *                  schedule's sizes (a smaller one sets IDX_FP4_DEV_CAPACITY)
+ *                  schedule's sizes, zero-filled before first use (a smaller one sets
+ *                  IDX_FP4_DEV_CAPACITY and every row comes out empty)
  *   topk_idx [batch][topk] (device, required), topk_val [batch][topk] (nullable)
  *   logits_debug   nullable device float [batch][logits_stride]: every scored logit (testing) */
 int idx_fp4_decode_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
@@ -157,6 +174,34 @@ int idx_fp4_decode_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, 
                                void *workspace, size_t workspace_bytes, int32_t *topk_idx, float *topk_val,
                                float *logits_debug, int64_t logits_stride, int32_t *status_dev,
                                cudaStream_t stream);
+
+/* ---- Decode with next_n query rows per sequence (speculative-decoding verify rows) --------
+ * ("Score a DSA sparse indexer in FP4", squashed commit message: the MTP draft folds its
+ * batch x next_n verify rows back onto the batch's sequences and rebuilds the decode schedule for
+ * them.) Sequence b carries rows b * next_n + j, j < next_n; row j sees keys
+ * [0, ctx_lens[b] - next_n + 1 + j), so the last row sees the whole context and every row a key
+ * pass shared with the others: the keys are streamed once for all next_n rows.
+ * next_n is 1, 2 or 4 with next_n * num_heads <= 128 (else IDX_FP4_ERR_SHAPE; larger shapes go
+ * through idx_fp4_prefill_logits_topk, one request per sequence).
+ *   Schedule: idx_fp4_build_decode_schedule_mtp with the same next_n (a range holds at most
+ *   12288 keys for next_n 2, 6144 for 4), into a buffer of idx_fp4_decode_schedule_bytes.
+ *   Workspace: idx_fp4_decode_mtp_workspace_bytes, zero-filled before first use.
+ *   q_packed [batch * next_n][H][64], q_scale [batch * next_n][H][4], weights [batch * next_n][H];
+ *   topk_idx / topk_val [batch * next_n][topk]; logits_debug [batch * next_n][logits_stride].
+ * Everything else as for idx_fp4_decode_logits_topk, which is this call with next_n = 1. */
+int idx_fp4_build_decode_schedule_mtp(const int32_t *ctx_lens_dev, int batch, int next_n, int max_batch,
+                                      int64_t max_ctx, void *sched_dev, size_t sched_bytes, int32_t *status_dev,
+                                      cudaStream_t stream);
+
+size_t idx_fp4_decode_mtp_workspace_bytes(int max_batch, int64_t max_ctx, int topk, int next_n);
+
+int idx_fp4_decode_mtp_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
+                                   const uint8_t *kv_packed, const uint8_t *kv_scale, int64_t num_pages,
+                                   const int32_t *block_tables, int block_table_stride, const int32_t *ctx_lens_dev,
+                                   int batch, int next_n, int num_heads, int topk, const void *sched_dev,
+                                   size_t sched_bytes, void *workspace, size_t workspace_bytes, int32_t *topk_idx,
+                                   float *topk_val, float *logits_debug, int64_t logits_stride, int32_t *status_dev,
+                                   cudaStream_t stream);
 
 /* Bytes of the prefill workspace (the call's unit table, and candidate lists for rows longer
  * than one unit's 8192-key (64-head) / 16384-key (128-head) share) for rows of up to max_ctx
@@ -176,9 +221,9 @@ size_t idx_fp4_prefill_workspace_bytes(int num_requests, int num_rows, int num_h
  *   max_ctx    bound on every row end, the value the workspace was sized with
  *   workspace  device, >= idx_fp4_prefill_workspace_bytes(num_requests, num_rows, num_heads, max_ctx, topk)
  * Rows longer than one unit's share are scored in key chunks and merged inside the call.
- * Decode with next_n query rows per sequence (speculative-decoding verify rows) is this call
- * with one request per sequence b of next_n rows, row j carrying row_end ctx_b - next_n + 1 + j.
- * num_heads stays the index head count of one row.
+ * Decode with next_n query rows per sequence can also be run as this call, with one request per
+ * sequence b of next_n rows, row j carrying row_end ctx_b - next_n + 1 + j (num_heads stays the
+ * index head count of one row); idx_fp4_decode_mtp_logits_topk is the decode-shaped form.
  *   topk_idx [num_rows][topk] (required), topk_val (nullable), logits_debug as for decode */
 int idx_fp4_prefill_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,
                                 const uint8_t *kv_packed, const uint8_t *kv_scale, int64_t num_pages,
@@ -192,22 +237,26 @@ int idx_fp4_prefill_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale,
  * The pages have no counterpart of this call; it is here for callers that cannot allocate
  * device memory (code running inside an allocator or memory-pool hook, an embedding runtime
  * that owns every device allocation, or a path that must never wait on the allocator). It does
- * what idx_fp4_decode_logits_topk does, with the candidate workspace taken from a fixed array
- * of IDX_FP4_STATIC_SCRATCH_BYTES (16 MiB) that the library holds on every GPU it is loaded
- * on until the process exits. It allocates nothing.
+ * what idx_fp4_decode_logits_topk does, with the workspace taken from a fixed array of
+ * IDX_FP4_STATIC_SCRATCH_BYTES (16 MiB) that the library holds on every GPU it is loaded on
+ * until the process exits. It allocates nothing.
  *   Arguments as for idx_fp4_decode_logits_topk, minus workspace/workspace_bytes, plus
- *   max_ctx: the bound the schedule was built with (every ctx_lens[b] <= max_ctx).
- *   Returns IDX_FP4_ERR_CAPACITY, launching nothing, when the candidate lists such a schedule
- *   may need (idx_fp4_decode_static_bytes) exceed the array: split the batch or use the
- *   workspace call.
+ *   max_ctx: the bound the schedule was built with (every ctx_lens[b] <= max_ctx). The schedule
+ *   must be built with max_batch = batch and this max_ctx (else IDX_FP4_DEV_CAPACITY is set and
+ *   every row comes out empty).
+ *   Returns IDX_FP4_ERR_CAPACITY, launching nothing, when the workspace such a schedule needs
+ *   (idx_fp4_decode_static_bytes) exceeds the array: split the batch or use the workspace call.
  * The first call on a device looks up the array's device address (and may load the library's
  * device code); make that first call before any stream capture. All calls on a device share
  * the one array, so calls that overlap on the GPU (other streams, other host threads) race and
- * must be serialised by the caller. Nothing in the array needs to start at zero. */
+ * must be serialised by the caller. Each call first clears the array's synchronisation words
+ * on `stream` (cudaMemsetAsync); everything else it reads is written earlier in the same call.
+ * The cached device address does not survive cudaDeviceReset: do not use this call afterwards
+ * in the same process. */
 #define IDX_FP4_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 
-/* Scratch bytes idx_fp4_decode_logits_topk_static needs for this batch on the current device
- * (host + a device attribute query; 0 for invalid arguments or a failed query). */
+/* Scratch bytes idx_fp4_decode_logits_topk_static needs for this batch (host only; the same as
+ * idx_fp4_decode_workspace_bytes(batch, max_ctx, topk); 0 for invalid arguments). */
 size_t idx_fp4_decode_static_bytes(int batch, int64_t max_ctx, int topk);
 
 int idx_fp4_decode_logits_topk_static(const uint8_t *q_packed, const uint8_t *q_scale, const float *weights,

@@ -26,7 +26,7 @@
 //   magnitude within the E2M1 range, elements rounded to nearest with ties to the
 //   even code) is the workload's stated quantiser.
 //
-// Readings taken where the pages are silent (each is listed in the design doc):
+// Readings taken where the pages are silent:
 //   R1  Nibble order: element 2i in bits 0..3, element 2i+1 in bits 4..7 of byte i.
 //   R2  The sign bit of a code is set iff the input is negative, so a small negative
 //       value that rounds to zero encodes as -0 (code 8).

@@ -231,45 +231,66 @@ def test_decode_schedule_mismatch_flagged():
     assert int(run.status.item()) & fx.DEV_BAD_SCHEDULE
 
 
+def parse_decode_schedule(buf, max_batch):
+    """The decode schedule's tables, read on the host (header, per-range first unit, per-sequence
+    context / first segment / segment count, units, segments)."""
+    s = buf.cpu().numpy().view(np.int32)
+    keys = ["magic", "ctas", "batch", "max_batch", "next_n", "rounds", "per", "num_units", "num_segs", "units_cap",
+            "segs_cap", "ranges_cap", "total_tiles", "tiles_cap", "ok", "pad"]
+    h = dict(zip(keys, (int(x) for x in s[:16])))
+    o = 16
+    range_first = s[o:o + h["ranges_cap"] + 1]
+    o += h["ranges_cap"] + 1
+    seq_ctx, seq_seg0, seq_nseg = (s[o + i * max_batch:o + (i + 1) * max_batch] for i in range(3))
+    uoff = ((o + 3 * max_batch) * 4 + 31) // 32 * 32 // 4
+    units = s[uoff:uoff + 8 * h["units_cap"]].reshape(-1, 8)
+    segs = s[uoff + 8 * h["units_cap"]:uoff + 8 * (h["units_cap"] + h["segs_cap"])].reshape(-1, 8)
+    return h, range_first, seq_ctx, seq_seg0, seq_nseg, units, segs
+
+
 def test_decode_schedule_invariants():
-    """Units of every sequence partition [0, ctx) exactly, each CTA's share is at most the
-    per-CTA tile count, and no CTA exists past the work."""
-    from fp4_sparse_attention_mxfp4_gb300 import _lib  # noqa: F401
+    """Units of every sequence partition [0, ctx) exactly in token order; each CTA range holds at
+    most one row buffer of tiles; segments group a sequence's units per round with consecutive unit
+    indices; sequences without keys have no segment."""
     ctx = np.array([131072, 5, 0, 70000, 128, 129, 1, 262144], np.int32)
-    t = dev(ctx)
     sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(16, 262144), dtype=torch.uint8, device="cuda")
-    fx.idx_fp4_build_decode_schedule(t, 16, 262144, sched)
+    fx.idx_fp4_build_decode_schedule(dev(ctx), 16, 262144, sched)
     torch.cuda.synchronize()
-    s = sched.cpu().numpy().view(np.int32)
-    magic, ctas, batch, max_batch, num_units, total_tiles, per, units_cap = s[:8]
-    assert batch == 8 and max_batch == 16
-    assert ctas == torch.cuda.get_device_properties(0).multi_processor_count
-    cta_first = s[8:8 + 1024]
-    cta_count = s[8 + 1024:8 + 2048]
-    off = 8 + 2048
-    seq_first, seq_units, seq_ctx = s[off:off + 16], s[off + 16:off + 32], s[off + 32:off + 48]
-    uoff = ((off + 48) * 4 + 31) // 32 * 32 // 4
-    units = s[uoff:uoff + 8 * num_units].reshape(num_units, 8)
-    assert total_tiles == sum(-(-int(c) // 128) for c in ctx)
+    h, range_first, seq_ctx, seq_seg0, seq_nseg, units, segs = parse_decode_schedule(sched, 16)
+    assert h["magic"] == 0x44534333 and h["ok"] == 1 and h["batch"] == 8 and h["max_batch"] == 16
+    assert h["ctas"] == torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = [-(-int(c) // 128) for c in ctx]
+    assert h["total_tiles"] == sum(tiles)
     assert np.array_equal(seq_ctx[:8], ctx)
+    per, ctas, rounds = h["per"], h["ctas"], h["rounds"]
+    assert 1 <= per <= 128 and rounds * ctas * per >= h["total_tiles"]
+    starts = np.concatenate([[0], np.cumsum(tiles)])
     covered = {b: [] for b in range(8)}
-    for c in range(ctas):
-        tiles = 0
-        for ui in range(cta_first[c], cta_first[c] + cta_count[c]):
-            row, table, kb, ke, nq, slot = units[ui][:6]
-            covered[row].append((kb, ke, ui))
-            tiles += -(-(ke - kb) // 128)
-            assert kb % 128 == 0 and nq == 1 and table == row and ke - kb <= 16384
-            assert (slot == -1) == (seq_units[row] == 1)
-        assert tiles <= per * (-(-total_tiles // (ctas * 128)))
-    assert cta_first[ctas - 1] + cta_count[ctas - 1] == num_units
+    for i in range(rounds * ctas):
+        lo = i * per
+        for ui in range(range_first[i], range_first[i + 1]):
+            seq, kb, ke, buf, seg, uidx, tile0 = units[ui][:7]
+            covered[seq].append((kb, ke, ui, seg, uidx))
+            assert tile0 == starts[seq] + kb // 128 and kb % 128 == 0
+            assert lo <= tile0 and tile0 + -(-(ke - kb) // 128) <= lo + per
+            assert buf == (tile0 - lo) * 128 and buf + (ke - kb) <= per * 128
+    assert range_first[rounds * ctas] == h["num_units"]
+    nsegs = 0
     for b in range(8):
         r = sorted(covered[b])
-        assert len(r) == seq_units[b]
         if ctx[b] == 0:
-            assert r == []
+            assert r == [] and seq_nseg[b] == 0
             continue
         assert r[0][0] == 0 and r[-1][1] == ctx[b]
         assert all(r[i][1] == r[i + 1][0] for i in range(len(r) - 1))
-        assert seq_first[b] == r[0][2]
-        assert [x[2] for x in r] == list(range(seq_first[b], seq_first[b] + seq_units[b]))
+        assert seq_nseg[b] >= 1
+        for k in range(seq_nseg[b]):
+            sid = seq_seg0[b] + k
+            sseq, first, nunits, skb, ske, rank = segs[sid][:6]
+            mine = [x for x in r if x[3] == sid]
+            assert sseq == b and rank == k and nunits == len(mine) and first == mine[0][2]
+            assert [x[4] for x in mine] == list(range(nunits))
+            assert [x[2] for x in mine] == list(range(first, first + nunits))
+            assert skb == mine[0][0] and ske == mine[-1][1]
+        nsegs += int(seq_nseg[b])
+    assert nsegs == h["num_segs"]
