@@ -56,6 +56,12 @@ int device_ctas() {
 
 int to_code(cudaError_t e) { return e == cudaSuccess ? IDX_FP4_OK : IDX_FP4_ERR_CUDA; }
 
+// The decode grid: one CTA per SM, at most 256 (a sequence's segment then spans at most 256 CTAs).
+int decode_ctas() {
+  const int c = device_ctas();
+  return c > 256 ? 256 : c;
+}
+
 // Decode capacities for (max_batch, max_ctx); false for sizes the tables cannot index (more than
 // 2^31 - 1 tiles of 128 keys in all).
 bool decode_caps_for(int max_batch, int64_t max_ctx, DecodeCaps* caps) {
@@ -80,7 +86,7 @@ int build_schedule(const int32_t* ctx_lens_dev, int batch, int next_n, int max_b
   DecodeCaps caps;
   if (!decode_caps_for(max_batch, max_ctx, &caps)) return IDX_FP4_ERR_ARG;
   if (sched_bytes < decode_sched_bytes_for(max_batch, caps)) return IDX_FP4_ERR_CAPACITY;
-  const int ctas = device_ctas();
+  const int ctas = decode_ctas();
   if (ctas <= 0) return IDX_FP4_ERR_CUDA;
   return to_code(launch_build_decode_schedule(ctx_lens_dev, batch, next_n, max_batch, max_ctx, ctas, caps, sched_dev,
                                               status_dev, stream));
@@ -105,7 +111,7 @@ int decode_call(const uint8_t* q_packed, const uint8_t* q_scale, const float* we
       !aligned16(kv_scale) || !aligned16(sched_dev) || !aligned16(workspace))
     return IDX_FP4_ERR_ARG;
   if (sched_bytes < sizeof(DecodeSchedHeader)) return IDX_FP4_ERR_CAPACITY;
-  const int ctas = device_ctas();
+  const int ctas = decode_ctas();
   if (ctas <= 0) return IDX_FP4_ERR_CUDA;
   return to_code(launch_decode(q_packed, q_scale, weights, kv_packed, kv_scale, num_pages, block_tables,
                                block_table_stride, ctx_lens_dev, batch, num_heads, next_n, topk, sched_dev,

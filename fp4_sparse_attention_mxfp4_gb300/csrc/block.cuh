@@ -143,4 +143,130 @@ __device__ __forceinline__ uint2 blk_resolve(const Blk& B, KeyAt key, int n, uin
   return make_uint2((bin << kL1Shift) | low, need);
 }
 
+// Bin of the need-th largest element (1 <= need <= total) of hist[0, NB) (NB = 1024 or 4096,
+// 16-byte aligned), searched by one warp without block barriers. The bins form 32 groups: a
+// coalesced pass sums each group (the lanes reading one group reduce over shuffles) and leaves
+// group g's sum in lane g; a suffix scan over the lanes finds the group, and the warp splits that
+// group's bins, SUB per lane. Returns (bin, elements in the bins above it) in every lane.
+template <int NB>
+__device__ __forceinline__ uint2 warp_find_bin(const uint32_t* hist, uint32_t need, int lane) {
+  static_assert(NB == 1024 || NB == 4096, "32 groups of 32 or 128 bins");
+  constexpr int PER = NB / 32;      // bins per group
+  constexpr int G = PER / 4;        // lanes reading one group (16 bytes each)
+  constexpr int GCNT = 32 / G;      // groups per pass
+  constexpr int SUB = PER / 32;     // bins per lane inside the found group
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist);
+  uint32_t mine = 0;  // lane g: the sum of group g
+#pragma unroll
+  for (int it = 0; it < NB / 128; ++it) {
+    const uint4 v = h4[it * 32 + lane];
+    uint32_t x = v.x + v.y + v.z + v.w;
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+    const int gfirst = it * GCNT;
+    const uint32_t y = __shfl_sync(0xFFFFFFFFu, x, ((lane - gfirst) & (GCNT - 1)) * G);
+    if (lane >= gfirst && lane < gfirst + GCNT) mine = y;
+  }
+  uint32_t suf = mine;  // elements in groups >= lane
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suf, off);
+    if (lane + off < 32) suf += t;
+  }
+  const unsigned m = __ballot_sync(0xFFFFFFFFu, suf - mine < need && need <= suf);
+  const int L = m != 0u ? 31 - __clz(m) : 0;
+  const uint32_t above_l = __shfl_sync(0xFFFFFFFFu, suf - mine, L);
+  uint32_t c[SUB], s2 = 0;
+  if constexpr (SUB == 4) {
+    const uint4 v = h4[L * 32 + lane];
+    c[0] = v.x;
+    c[1] = v.y;
+    c[2] = v.z;
+    c[3] = v.w;
+  } else {
+    c[0] = hist[L * PER + lane];
+  }
+#pragma unroll
+  for (int k = 0; k < SUB; ++k) s2 += c[k];
+  uint32_t suf2 = s2;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suf2, off);
+    if (lane + off < 32) suf2 += t;
+  }
+  const uint32_t a2 = above_l + suf2 - s2;
+  const unsigned m2 = __ballot_sync(0xFFFFFFFFu, a2 < need && need <= a2 + s2);
+  const int L2 = m2 != 0u ? 31 - __clz(m2) : 0;
+  uint32_t bin = 0, ab = 0;
+  if (lane == L2) {
+    uint32_t a = a2;
+#pragma unroll
+    for (int k = SUB - 1; k >= 0; --k) {
+      if (a < need && need <= a + c[k]) {
+        bin = static_cast<uint32_t>(L * PER + lane * SUB + k);
+        ab = a;
+      }
+      a += c[k];
+    }
+  }
+  return make_uint2(__shfl_sync(0xFFFFFFFFu, bin, L2), __shfl_sync(0xFFFFFFFFu, ab, L2));
+}
+
+// Element e of a 16-byte vector of keys.
+__device__ __forceinline__ uint32_t vec_lane(const uint4& v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+// Bin of the need-th largest element (1 <= need <= total) of a two-level histogram, by one warp:
+// coarse[c] sums fine[c * FPER, (c + 1) * FPER), CB coarse bins (32 or 64). The warp finds the
+// coarse bin from the top, then the fine bin inside it (each lane holding CB / 32 and FPER / 32
+// bins). Returns (fine bin, elements above it) in every lane.
+template <int CB, int FPER>
+__device__ __forceinline__ uint2 warp_find_bin2(const uint32_t* fine, const uint32_t* coarse, uint32_t need, int lane) {
+  static_assert((CB == 32 || CB == 64) && (FPER == 32 || FPER == 64), "one or two bins per lane");
+  constexpr int CPL = CB / 32, FPL = FPER / 32;
+  auto search = [&](const uint32_t* h, int per, uint32_t above0, uint32_t& at_above) {
+    uint32_t c[2] = {0u, 0u}, s = 0;
+    for (int k = 0; k < per; ++k) {
+      c[k] = h[lane * per + k];
+      s += c[k];
+    }
+    uint32_t suf = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suf, off);
+      if (lane + off < 32) suf += t;
+    }
+    const uint32_t a = above0 + suf - s;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, a < need && need <= a + s);
+    const int L = m != 0u ? 31 - __clz(m) : 0;
+    int bin = 0;
+    uint32_t ab = 0;
+    if (lane == L) {
+      uint32_t x = a;
+      for (int k = per - 1; k >= 0; --k) {
+        if (x < need && need <= x + c[k]) {
+          bin = lane * per + k;
+          ab = x;
+        }
+        x += c[k];
+      }
+    }
+    at_above = __shfl_sync(0xFFFFFFFFu, ab, L);
+    return __shfl_sync(0xFFFFFFFFu, bin, L);
+  };
+  uint32_t a1 = 0, a2 = 0;
+  const int cb = search(coarse, CPL, 0u, a1);
+  const int fb = search(fine + cb * FPER, FPL, a1, a2);
+  return make_uint2(static_cast<uint32_t>(cb * FPER + fb), a2);
+}
+
+// The run of [0, n) that thread tid owns in run-based passes over 16-byte aligned keys: a multiple
+// of 4 long (except the last), runs in thread order.
+__device__ __forceinline__ int2 blk_run4(const Blk& B, int n) {
+  const int per = (((n + B.nt - 1) / B.nt) + 3) & ~3;
+  const int r0 = min(n, B.tid * per);
+  return make_int2(r0, min(n, r0 + per));
+}
+
 }  // namespace idxfp4

@@ -71,8 +71,11 @@ struct DecodeParams {
 namespace {
 
 constexpr uint32_t kEpiBarrier = 1;    // the epilogue warps, during the stream
-constexpr uint32_t kSelBarrier = 2;    // the epilogue warps, during the selection
-constexpr uint32_t kRoundBarrier = 3;  // every warp of the CTA: a round's range is published
+constexpr uint32_t kSelBarrier0 = 2;   // selection group 0 (the stage warps), during the selection
+constexpr uint32_t kSelBarrier1 = 3;   // selection group 1 (the epilogue warps), during the selection
+constexpr uint32_t kAllBarrier = 4;    // every warp of the CTA
+constexpr int kDecodeMaxCtas = 256;    // the decode grid: at most this many CTAs (so a segment holds at most
+                                       // this many units)
 
 template <int H, int Q>
 struct DecodeCfg {
@@ -92,6 +95,7 @@ struct DecodeCfg {
   static constexpr uint32_t EPI_REGS =
       (LAUNCH_REGS * (STAGES + EPI_WARPS) - STAGE_REGS * STAGES) / EPI_WARPS / 8u * 8u;
   static_assert(STAGES % 4 == 0 && EPI_WARPS % 4 == 0, "roles are whole warpgroups");
+  static_assert(STAGES == EPI_WARPS, "the two roles form two equal selection groups");
   static_assert(STAGE_REGS * STAGES + EPI_REGS * EPI_WARPS <= LAUNCH_REGS * (STAGES + EPI_WARPS),
                 "the re-split fits the registers the block is launched with");
   static constexpr int CAP = decode_cap_tiles(Q) * kTileKeys;  // row-buffer keys per query row
@@ -107,31 +111,39 @@ struct DecodeCfg {
   static constexpr uint32_t OFF_SFB = OFF_QB + 2 * N * 64;          // [2][512]
   static constexpr uint32_t OFF_W = OFF_SFB + 2 * 512;              // [2][N]
   static constexpr uint32_t OFF_LG = OFF_W + 2 * N * 4;             // [Q][CAP] ordered keys
-  static constexpr uint32_t OFF_SCR = OFF_LG + Q * CAP * 4;         // [128] block scratch
+  // Histograms of the range's first and last units (4096 fine bins and 64 coarse bins of 64),
+  // counted while streaming (one query row; with several rows they are counted after the stream).
+  static constexpr bool HIST_IN_STREAM = Q == 1;
+  static constexpr int HST_WORDS = kL1Bins + 64;
+  static constexpr uint32_t OFF_HST = OFF_LG + Q * CAP * 4;         // [2][HST_WORDS]
+  static constexpr uint32_t OFF_SCR = OFF_HST + (HIST_IN_STREAM ? 2 * HST_WORDS * 4 : 0);  // [2][128] scratch
   static constexpr int REL_RING = STAGES / ACC + 2;
   static_assert(STAGES % ACC == 0, "a stage warp keeps to one accumulator");
   // full[STAGES], empty[STAGES], acc_full[ACC], acc_rel[ACC * REL_RING], q_ready[2], q_free[2]
   static constexpr uint32_t NUM_BARS = 2 * STAGES + ACC + ACC * REL_RING + 4;
   static constexpr uint32_t BAR_QREADY = 2 * STAGES + ACC + ACC * REL_RING;
   static constexpr uint32_t BAR_QFREE = BAR_QREADY + 2;
-  static constexpr uint32_t OFF_BAR = OFF_SCR + 128 * 4;
+  static constexpr uint32_t OFF_BAR = OFF_SCR + 2 * 128 * 4;
   static constexpr uint32_t OFF_KS = OFF_BAR + NUM_BARS * 8;  // KernelShared
-  static constexpr uint32_t SMEM_BYTES = OFF_KS + 128;
+  static constexpr uint32_t SMEM_BYTES = OFF_KS + 384;
   static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM");
   static_assert(OFF_LG % 16 == 0 && OFF_QB % 128 == 0, "operand and row-buffer alignment");
-  // The selection phase reuses the stage area (free once the stream has ended), in words:
-  static constexpr int P_WORDS = static_cast<int>(OFF_QB / 4);
-  static constexpr int P_HIST = 0;                    // [kL1Bins] histogram
-  static constexpr int P_LIST = P_HIST + kL1Bins;     // [4096] keys of the threshold bin
-  static constexpr int LIST_CAP = 4096;
-  static constexpr int P_UCNT = P_LIST + LIST_CAP;    // [1024 + 1] per-unit counts / offsets
-  static constexpr int P_UOFF = P_UCNT + 1028;        // [1024 + 1] per-unit record offsets
-  static constexpr int P_REC = P_UOFF + 1028;         // [RCAP] staged (record, unit) pairs
-  static constexpr int RCAP = 2048;
+  // The selection phase reuses the stage area (free once the stream has ended): each of the two
+  // selection groups gets half of it, in words from the group's base:
+  static constexpr int P_WORDS = static_cast<int>(OFF_QB / 4) / 2 / 32 * 32;
+  static constexpr int P_HIST = 0;                    // [kL1Bins + 64] histogram, fine and coarse
+  static constexpr int P_LIST = P_HIST + kL1Bins + 64;  // [LIST_CAP] keys of the threshold bin
+  static constexpr int LIST_CAP = 2048;
+  static constexpr int P_LVL = P_LIST + LIST_CAP;     // [1024 + 32] lower radix levels, fine and coarse
+  static constexpr int P_UOFF = P_LVL + 1056;         // [kDecodeMaxCtas + 1] per-unit record offsets
+  static constexpr int P_REC = P_UOFF + kDecodeMaxCtas + 4;  // [RCAP] staged (record, unit) pairs
+  static constexpr int RCAP = 1024;
+  static constexpr int P_EQPRE = P_REC + 2 * RCAP;    // [Q][kDecodeMaxCtas + 4] prefix of the units' bin keys
   static constexpr int P_SOFF = P_WORDS - 1040;       // [1024 + 1] segment offsets of a sequence merge
-  static constexpr int P_CAND = P_LIST + LIST_CAP;    // the merge's staged candidates (after the records)
+  static constexpr int P_CAND = P_LVL;                // a sequence merge's staged candidates
   static constexpr int CCAP = (P_SOFF - P_CAND) / 2 / 128 * 128;
-  static_assert(P_REC + 2 * RCAP <= P_SOFF && CCAP >= 4096, "selection areas fit the stage area");
+  static_assert(P_EQPRE + Q * (kDecodeMaxCtas + 4) <= P_SOFF && CCAP >= 1024, "selection areas fit");
+  static_assert(P_HIST % 4 == 0 && P_LVL % 4 == 0, "16-byte aligned histograms");
 };
 
 
@@ -147,6 +159,10 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
+}
+
+__device__ __forceinline__ void red_add_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t ldcg_u32(const uint32_t* p) { return __ldcg(p); }
@@ -221,14 +237,26 @@ struct RoundInfo {
   int units;    // units this CTA streamed in earlier rounds (query-buffer phases)
 };
 
+// An exchange between the units of a segment row, from its first round to its second.
+struct TaskState {
+  uint32_t bin;         // threshold bin of the segment row
+  uint32_t need;        // keys of that bin among the top-k
+  uint32_t gt_before;   // keys above the bin in the segment's earlier units
+  uint32_t ok;          // the first round completed
+};
+
 struct KernelShared {
   DecodeSchedHeader h;  // the schedule's header
   uint32_t tmem;        // TMEM base address
   int abort;            // a bounded wait gave up: later waits return at once
   RoundInfo round[2];   // round r in slot r & 1 (written before round r's start barrier, read after it;
                         // slot r & 1 is rewritten only after every warp has passed round r + 1's)
+  TaskState task[2][kMaxNextN];  // per selection group and row
+  uint32_t counter[2][4];        // per selection group
+  int pending[2];                // sequence merges deferred to the end of a group's selection
+  int pending_seq[2][kMaxNextN];
 };
-static_assert(sizeof(KernelShared) <= 128, "fits its slot");
+static_assert(sizeof(KernelShared) <= 384, "fits its slot");
 
 __device__ __forceinline__ DecodeSchedView sched_view(const DecodeParams& p, const DecodeSchedHeader& h) {
   return decode_sched_view(const_cast<void*>(p.sched), h.max_batch, h.ranges_cap, h.units_cap);
@@ -506,6 +534,9 @@ __device__ __forceinline__ void stream_epilogue_warp(const DecodeParams& p, uint
   const int krow = qtr * 32 + lane;
   const uint32_t lane_base = static_cast<uint32_t>(qtr * 32) << 16;
   uint32_t* lg = reinterpret_cast<uint32_t*>(smem + C::OFF_LG);
+  uint32_t* hst = reinterpret_cast<uint32_t*>(smem + C::OFF_HST);
+  if constexpr (C::HIST_IN_STREAM)
+    for (int x = etid; x < 2 * C::HST_WORDS; x += C::EPI_THREADS) hst[x] = 0u;  // ordered by prep's barrier
   if (it.count > 0) prep_query<H, Q>(p, it.at(0), st.units, smem, tmem, etid);
   if (it.count > 1) prep_query<H, Q>(p, it.at(1), st.units + 1, smem, tmem, etid);
   int t0 = st.tiles;  // CTA-wide number of the unit's first tile
@@ -514,6 +545,9 @@ __device__ __forceinline__ void stream_epilogue_warp(const DecodeParams& p, uint
     const float* wsm = reinterpret_cast<const float*>(smem + C::OFF_W) + ((st.units + i) & 1) * N;
     const int ctx = seq_ctx[u.seq];
     const int ntiles = dunit_tiles(u);
+    // the range's first and last units may share their sequence with other CTAs: count their keys
+    uint32_t* uh = nullptr;
+    if constexpr (C::HIST_IN_STREAM) uh = i == 0 ? hst : (i == it.count - 1 ? hst + C::HST_WORDS : nullptr);
     for (int j = ((grp - t0) % C::GROUPS + C::GROUPS) % C::GROUPS; j < ntiles; j += C::GROUPS) {
       const int tt = t0 + j;
       const int a = tt % ACC;
@@ -530,7 +564,12 @@ __device__ __forceinline__ void stream_epilogue_warp(const DecodeParams& p, uint
 #pragma unroll
       for (int r = 0; r < Q; ++r) {
         const bool valid = key < ctx - Q + 1 + r;
-        if (at < C::CAP) lg[r * C::CAP + at] = valid ? ordered_key(logit[r]) : 0u;
+        const uint32_t ok = ordered_key(logit[r]);
+        if (at < C::CAP) lg[r * C::CAP + at] = valid ? ok : 0u;
+        if (C::HIST_IN_STREAM && valid && uh != nullptr) {
+          smem_red_add(&uh[ok >> kL1Shift], 1u);
+          smem_red_add(&uh[kL1Bins + (ok >> (kL1Shift + 6))], 1u);
+        }
         if (valid && p.logits_debug != nullptr && key < p.logits_stride)
           p.logits_debug[(static_cast<int64_t>(u.seq) * Q + r) * p.logits_stride + key] = logit[r];
       }
@@ -621,6 +660,12 @@ __device__ __forceinline__ void pad_row(const Blk& B, const DecodeParams& p, int
   }
 }
 
+// Cross-CTA ordering: a CTA's writes, then a block barrier, then one thread's release (an atomic
+// add at GPU scope) publish the writes; another CTA's thread acquires the count (a spin on an
+// acquire load, or the acquire half of its own atomic), then a block barrier, and that CTA's
+// threads read the published data through L2. The shared flags below are written by one thread
+// before a barrier and read after it; the next write to a flag comes after further barriers.
+
 // Bounded wait by one thread until *ctr >= target; the answer is shared with the block.
 __device__ __forceinline__ bool blk_wait_count(const Blk& B, uint32_t* ctr, uint32_t target, volatile int* abort_flag,
                                                int32_t* status) {
@@ -637,28 +682,25 @@ __device__ __forceinline__ bool blk_wait_count(const Blk& B, uint32_t* ctr, uint
         }
       }
     }
-    __threadfence();
     B.sc[72] = ok ? 1u : 0u;
   }
   B.sync();
-  const bool ok = B.sc[72] != 0u;
-  B.sync();
-  return ok;
+  return B.sc[72] != 0u;
 }
 
-// Ticket after this CTA's writes for a segment row: true for the CTA that arrives last.
+// Publish this CTA's writes for a segment row (count it on *ctr).
+__device__ __forceinline__ void blk_publish(const Blk& B, uint32_t* ctr) {
+  B.sync();
+  if (B.tid == 0) red_add_release_gpu(ctr, 1u);
+}
+
+// Ticket after this CTA's writes for a segment row: true for the CTA that arrives last (which has
+// then acquired every other arrival's writes).
 __device__ __forceinline__ bool blk_ticket(const Blk& B, uint32_t* ctr, uint32_t count) {
   B.sync();
-  if (B.tid == 0) {
-    __threadfence();
-    const uint32_t old = atom_add_acq_rel_gpu(ctr, 1u);
-    __threadfence();
-    B.sc[73] = old + 1u == count ? 1u : 0u;
-  }
+  if (B.tid == 0) B.sc[73] = atom_add_acq_rel_gpu(ctr, 1u) + 1u == count ? 1u : 0u;
   B.sync();
-  const bool last = B.sc[73] != 0u;
-  B.sync();
-  return last;
+  return B.sc[73] != 0u;
 }
 
 struct SegCtx {
@@ -668,26 +710,26 @@ struct SegCtx {
 };
 
 // Exact top-k of a sequence row over its segments' lists (a sequence spanning several rounds).
+// P is the selection group's area.
 template <int H, int Q>
 __device__ void merge_sequence(const DecodeParams& p, const DecodeSchedView& v, const DecodeWs& ws, int seq, int q,
-                               uint8_t* smem, const Blk& B) {
+                               uint32_t* P, const Blk& B) {
   using C = DecodeCfg<H, Q>;
-  uint32_t* P = reinterpret_cast<uint32_t*>(smem);
   uint32_t* off = P + C::P_SOFF;
   const int nseg = v.seq_nseg[seq], s0 = v.seq_seg0[seq];
   const int ctx = v.seq_ctx[seq];
   const int row_end = clampi(ctx - Q + 1 + q, 0, ctx);
+  const int ns = min(nseg, 1024);
   if (B.tid == 0) {
     uint32_t o = 0;
-    for (int s = 0; s < nseg && s < 1024; ++s) {
-      off[s] = o;
-      const DecodeSeg sg = v.segs[s0 + s];
+    for (int k = 0; k < ns; ++k) {
+      off[k] = o;
+      const DecodeSeg sg = v.segs[s0 + k];
       o += static_cast<uint32_t>(min(p.topk, clampi(row_end - sg.kb, 0, sg.ke - sg.kb)));
     }
-    off[min(nseg, 1024)] = o;
+    off[ns] = o;
   }
   B.sync();
-  const int ns = min(nseg, 1024);
   const int M = static_cast<int>(off[ns]);
   auto at = [&](int x) {
     int lo = 0, hi = ns - 1;
@@ -715,223 +757,433 @@ __device__ void merge_sequence(const DecodeParams& p, const DecodeSchedView& v, 
   B.sync();
 }
 
-// Writes a segment row's selection: to the final row, or to the segment list followed by the
-// sequence's ticket (the last segment to finish merges the lists).
-template <int H, int Q, class KeyAt, class TokAt>
-__device__ void finish_segment(const DecodeParams& p, const DecodeSchedView& v, const DecodeWs& ws, const SegCtx& s,
-                               KeyAt key, TokAt tok, int n, bool known, uint32_t bin, uint32_t above, uint8_t* smem,
-                               const Blk& B) {
-  using C = DecodeCfg<H, Q>;
-  uint32_t* P = reinterpret_cast<uint32_t*>(smem);
-  const int seq = s.sg.seq;
-  const int nseg = v.seq_nseg[seq];
-  RowOut out{p.topk_idx + s.out_row * p.topk, p.topk_val != nullptr ? p.topk_val + s.out_row * p.topk : nullptr,
-             nseg > 1 ? ws.seglists + (static_cast<int64_t>(s.seg_id) * Q + s.q) * p.topk : nullptr,
-             static_cast<uint32_t>(max(s.kk, 0))};
-  if (known && s.kk < n && s.kk > 0) {
-    bool consistent = true;
-    const uint2 tn = blk_resolve(B, key, n, bin, static_cast<uint32_t>(s.kk) - above, P + C::P_HIST, P + C::P_LIST,
-                                 C::LIST_CAP, &consistent);
-    if (!consistent && B.tid == 0) set_status(p.status, IDX_FP4_DEV_SYNC);
-    blk_emit(B, key, tok, n, false, tn.x, tn.y, out);
-  } else {
-    blk_select(B, key, tok, n, s.kk, P + C::P_HIST, P + C::P_LIST, C::LIST_CAP, out);
-  }
-  if (nseg <= 1) {
-    pad_row(B, p, s.out_row, s.kk);
-    B.sync();
-    return;
-  }
-  if (blk_ticket(B, &ws.seqsync[(static_cast<int64_t>(seq) * Q + s.q) * 4], static_cast<uint32_t>(nseg)))
-    merge_sequence<H, Q>(p, v, ws, seq, s.q, smem, B);
+// Where a segment row's selection goes: its final output row, or its segment's list when the
+// sequence has several segments (then merged by the last segment to finish).
+__device__ __forceinline__ RowOut seg_out(const DecodeParams& p, const DecodeWs& ws, const SegCtx& s, int nseg,
+                                          int Q) {
+  return RowOut{p.topk_idx + s.out_row * p.topk, p.topk_val != nullptr ? p.topk_val + s.out_row * p.topk : nullptr,
+                nseg > 1 ? ws.seglists + (static_cast<int64_t>(s.seg_id) * Q + s.q) * p.topk : nullptr,
+                static_cast<uint32_t>(max(s.kk, 0))};
 }
 
-// Selection of one round's units of this CTA (the row buffer holds their logits).
+// Selection of one round's units of this CTA by selection group g (the row buffer holds their
+// logits; P is the group's half of the stage area). Group 0 takes the range's first unit, group 1
+// its last unit, and the two share the units between them (each a whole sequence). Segments of one
+// unit are selected here. The units of a longer segment row run a two-round exchange through the
+// workspace, without a merging CTA:
+//   A  each unit publishes the non-empty bins of its 12-bit histogram from its own k-th key's bin
+//      up (the segment's k-th key lies at or above every unit's, so these bins count it exactly);
+//   B1 once every unit has published, each finds the segment's threshold bin and the keys above it
+//      from the records, and publishes its keys inside that bin (low 20 bits);
+//   B2 once every unit has published those, each resolves the exact threshold key T and how many
+//      keys equal to T are kept, works out from the counts how many selected keys the segment's
+//      earlier units hold, and writes its own selected keys at that offset, in token order.
+// A unit's waits only follow other units' publications, and the two groups run their first and
+// last units' exchanges side by side, so no CTA's publication waits behind another exchange.
 template <int H, int Q>
-__device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, const Blk& B) {
+__device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int g, const Blk& B) {
   using C = DecodeCfg<H, Q>;
   KernelShared* ks = reinterpret_cast<KernelShared*>(smem + C::OFF_KS);
   volatile int* abort_flag = &ks->abort;
   const DecodeSchedView v = sched_view(p, ks->h);
   const DecodeWs ws = decode_ws_view(p.workspace, decode_caps_of(ks->h), ks->h.max_batch, Q);
   const int uf = ks->round[slot].uf, ul = ks->round[slot].ul;
-  uint32_t* P = reinterpret_cast<uint32_t*>(smem);
+  uint32_t* P = reinterpret_cast<uint32_t*>(smem) + g * C::P_WORDS;
   uint32_t* hist = P + C::P_HIST;
+  uint32_t* lvl = P + C::P_LVL;
+  uint32_t* cnt = ks->counter[g];
   const uint32_t* lg = reinterpret_cast<const uint32_t*>(smem + C::OFF_LG);
   const int topk = p.topk;
-  auto seg_ctx = [&](const DecodeUnit& u, int q) {
+  const int lane = B.lane(), warp = B.warp();
+  const int ex = g == 0 ? uf : (ul - 1 > uf ? ul - 1 : -1);  // this group's range-end unit
+  auto seg_ctx_of = [&](const DecodeUnit& u, const DecodeSeg& sg, int ctx, int q) {
     SegCtx s;
-    s.sg = v.segs[u.seg];
+    s.sg = sg;
     s.seg_id = u.seg;
     s.q = q;
-    s.row_end = v.seq_ctx[u.seq] - Q + 1 + q;
+    s.row_end = ctx - Q + 1 + q;
     s.kk = min(topk, clampi(s.row_end - s.sg.kb, 0, s.sg.ke - s.sg.kb));
     s.out_row = static_cast<int64_t>(u.seq) * Q + q;
     return s;
   };
+  auto seg_ctx = [&](const DecodeUnit& u, int q) { return seg_ctx_of(u, v.segs[u.seg], v.seq_ctx[u.seq], q); };
+  // the range-end unit's schedule entries, read once (each read is a round trip to L2)
+  DecodeUnit ue{};
+  DecodeSeg se{};
+  int ctx_e = 0, nseg_e = 0;
+  if (ex >= 0) {
+    ue = v.units[ex];
+    se = v.segs[ue.seg];
+    ctx_e = v.seq_ctx[ue.seq];
+    nseg_e = v.seq_nseg[ue.seq];
+  }
+  auto seg_keys = [&](const SegCtx& s) { return clampi(s.row_end - s.sg.kb, 0, s.sg.ke - s.sg.kb); };
   auto sync_word = [&](const SegCtx& s, int k) { return &ws.sync[(static_cast<int64_t>(s.seg_id) * Q + s.q) * 4 + k]; };
-  auto rec_base = [&](int unit, int q) {
-    return ws.records + q * ws.rec_stride + static_cast<int64_t>(v.units[unit].tile0) * kTileKeys + unit;
+  // Unit j of a segment: its first tile and tile count follow from the segment's first tile and the
+  // range length (unit 0 starts the segment, unit j > 0 starts range seg.tile0 / per + j), so the
+  // other units' areas are found without reading the unit table.
+  const int per = ks->h.per;
+  auto unit_tile0 = [&](const DecodeSeg& sg, int j) { return j == 0 ? sg.tile0 : (sg.tile0 / per + j) * per; };
+  auto unit_tiles = [&](const DecodeSeg& sg, int j) {
+    const int seg_end = sg.tile0 + (sg.ke - sg.kb + kTileKeys - 1) / kTileKeys;
+    const int t1 = j + 1 < sg.nunits ? unit_tile0(sg, j + 1) : seg_end;
+    return max(0, min(t1, seg_end) - unit_tile0(sg, j));
   };
-  auto cand_base = [&](const SegCtx& s) { return ws.cands + s.q * ws.cand_stride + static_cast<int64_t>(s.sg.tile0) * kTileKeys; };
-
-  // Merge of a segment row by its last unit: the candidates (every key at or above the threshold
-  // bin, or every key of the row when `all`) in token order at the segment's candidate array.
-  auto merge_segment = [&](const SegCtx& s, int M, bool all, uint32_t bin, uint32_t above) {
-    const uint2* src = cand_base(s);
-    uint2* cand = reinterpret_cast<uint2*>(P + C::P_CAND);
-    const bool staged = M <= C::CCAP;
-    if (staged) {
-      for (int x = B.tid; x < M; x += B.nt) cand[x] = ldcg_u2(src + x);
-      B.sync();
-    }
-    auto key = [&](int x) { return staged ? cand[x].x : ldcg_u2(src + x).x; };
-    auto tok = [&](int x) { return static_cast<int>(staged ? cand[x].y : ldcg_u2(src + x).y); };
-    if (B.tid == 0) {
-      *sync_word(s, 0) = 0u;  // every unit has passed its wait on the published histograms
-      *sync_word(s, 1) = 0u;
-      if (M < s.kk) set_status(p.status, IDX_FP4_DEV_SYNC);
-    }
-    finish_segment<H, Q>(p, v, ws, s, key, tok, M, !all, bin, above, smem, B);
+  // a unit's published bins: a count, then the records
+  auto rec_of = [&](const DecodeSeg& sg, int j, int q) {
+    return ws.records + q * ws.rec_stride + static_cast<int64_t>(unit_tile0(sg, j)) * kTileKeys + sg.first_unit + j;
   };
-
-  // Phase A: selections that need nobody else, and the published histograms of longer segments.
-  for (int i = uf; i < ul; ++i) {
+  // a unit's list of threshold-bin keys, in its own part of the candidate area
+  auto list_of = [&](const DecodeSeg& sg, int j, int q) {
+    return reinterpret_cast<uint32_t*>(ws.cands + q * ws.cand_stride + static_cast<int64_t>(unit_tile0(sg, j)) * kTileKeys);
+  };
+  auto exchanged = [&](const SegCtx& s) { return s.sg.nunits > 1 && s.kk < seg_keys(s); };
+  if (B.tid == 0) ks->pending[g] = 0;
+  // A completed segment row: pad its final row, or count it for its sequence (the last segment of a
+  // longer sequence merges the lists, at once or deferred to the end of this group's selection,
+  // since a merge reuses the areas the group's pending exchanges still hold).
+  auto segment_done = [&](const SegCtx& s, bool defer) {
+    const int seq = s.sg.seq, nseg = v.seq_nseg[seq];
+    if (nseg <= 1) {
+      pad_row(B, p, s.out_row, s.kk);
+      return;
+    }
+    if (blk_ticket(B, &ws.seqsync[(static_cast<int64_t>(seq) * Q + s.q) * 4], static_cast<uint32_t>(nseg))) {
+      if (!defer) {
+        merge_sequence<H, Q>(p, v, ws, seq, s.q, P, B);
+      } else if (B.tid == 0) {
+        ks->pending_seq[g][ks->pending[g]++] = seq * kMaxNextN + s.q;
+      }
+    }
+  };
+  // The last unit to finish a longer segment row resets the row's counters and completes it.
+  auto finish_exchange = [&](const SegCtx& s, bool defer) {
+    if (blk_ticket(B, sync_word(s, 2), static_cast<uint32_t>(s.sg.nunits))) {
+      if (B.tid == 0) {
+        *sync_word(s, 0) = 0u;
+        *sync_word(s, 1) = 0u;
+        *sync_word(s, 2) = 0u;
+      }
+      if (v.seq_nseg[s.sg.seq] > 1) segment_done(s, defer);
+    }
+  };
+  // Selection of a unit that is a whole segment row (nothing to wait for).
+  auto select_local = [&](int i, int q) {
     const DecodeUnit u = v.units[i];
+    const SegCtx s = seg_ctx(u, q);
+    const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
+    const uint32_t* keys = lg + q * C::CAP + u.buf;
+    auto key = [&](int x) { return keys[x]; };
+    auto tok = [&](int x) { return u.kb + x; };
+    blk_select(B, key, tok, un, s.kk, hist, P + C::P_LIST, C::LIST_CAP, seg_out(p, ws, s, v.seq_nseg[u.seq], Q));
+    segment_done(s, false);
+    B.sync();
+  };
+
+  // ---- A: the range-end unit's rows: whole rows, rows whose every key is selected, published bins
+  if (ex >= 0) {
+    const DecodeUnit& u = ue;
+    const int nseg = nseg_e;
     for (int q = 0; q < Q; ++q) {
-      const SegCtx s = seg_ctx(u, q);
+      const SegCtx s = seg_ctx_of(u, se, ctx_e, q);
       const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
       const uint32_t* keys = lg + q * C::CAP + u.buf;
-      auto key = [&](int x) { return keys[x]; };
-      auto tok = [&](int x) { return u.kb + x; };
       if (s.sg.nunits == 1) {
-        finish_segment<H, Q>(p, v, ws, s, key, tok, un, false, 0u, 0u, smem, B);
-      } else if (s.kk >= clampi(s.row_end - s.sg.kb, 0, s.sg.ke - s.sg.kb)) {
+        select_local(ex, q);
+      } else if (!exchanged(s)) {
         // every key of the segment row is selected: each unit writes its keys at their place
-        uint2* dst = cand_base(s) + (u.kb - s.sg.kb);
-        for (int x = B.tid; x < un; x += B.nt) dst[x] = make_uint2(keys[x], static_cast<uint32_t>(u.kb + x));
-        if (blk_ticket(B, sync_word(s, 1), static_cast<uint32_t>(s.sg.nunits))) merge_segment(s, s.kk, true, 0u, 0u);
+        const RowOut out = seg_out(p, ws, s, nseg, Q);
+        const uint32_t base = static_cast<uint32_t>(u.kb - s.sg.kb);
+        for (int x = B.tid; x < un; x += B.nt) out(base + static_cast<uint32_t>(x), keys[x], u.kb + x);
+        if (u.uidx == 0 && nseg <= 1) pad_row(B, p, s.out_row, s.kk);
+        finish_exchange(s, false);
+        B.sync();
       } else {
-        // histogram of the unit row; publish the bins from the unit's own k-th key's bin up
-        blk_zero(B, hist, kL1Bins);
+        const uint32_t* uh;  // fine bins, then 64 coarse bins
+        if constexpr (C::HIST_IN_STREAM) {
+          uh = reinterpret_cast<const uint32_t*>(smem + C::OFF_HST) + (ex == uf ? 0 : C::HST_WORDS);
+        } else {
+          blk_zero(B, hist, kL1Bins + 64);
+          B.sync();
+          for (int x = B.tid; x < un; x += B.nt) {
+            smem_red_add(&hist[keys[x] >> kL1Shift], 1u);
+            smem_red_add(&hist[kL1Bins + (keys[x] >> (kL1Shift + 6))], 1u);
+          }
+          uh = hist;
+        }
         B.sync();
-        for (int x = B.tid; x < un; x += B.nt) smem_red_add(&hist[keys[x] >> kL1Shift], 1u);
+        // the unit's own k-th key's bin (all bins when it holds fewer keys)
+        if (warp == 0) {
+          const uint32_t bu = un >= s.kk ? warp_find_bin2<64, 64>(uh, uh + kL1Bins, static_cast<uint32_t>(s.kk), lane).x : 0u;
+          if (lane == 0) cnt[1] = bu;
+        }
         B.sync();
-        const uint32_t bu = un >= s.kk ? blk_find_bin(B, hist, kL1Bins, static_cast<uint32_t>(s.kk)).x : 0u;
-        const int nb = kL1Bins - static_cast<int>(bu);
-        const int per = (nb + B.nt - 1) / B.nt;
-        const int b0 = static_cast<int>(bu) + min(nb, B.tid * per), b1 = static_cast<int>(bu) + min(nb, B.tid * per + per);
-        uint32_t cnt = 0;
-        for (int b = b0; b < b1; ++b) cnt += hist[b] != 0u ? 1u : 0u;
-        uint32_t total = 0;
-        uint32_t o = blk_scan2(B, cnt, 0u, &total, nullptr).x;
-        uint32_t* rec = rec_base(i, q);
-        for (int b = b0; b < b1; ++b)
-          if (hist[b] != 0u) rec[1 + o++] = (static_cast<uint32_t>(b) << 17) | hist[b];
-        if (B.tid == 0) rec[0] = total;
-        blk_ticket(B, sync_word(s, 0), 0u);  // publish (the count is never the last one's)
+        const uint32_t bu = cnt[1];
+        uint32_t* rec = rec_of(s.sg, u.uidx, q);
+        const int2 br = blk_run4(B, kL1Bins - static_cast<int>(bu));
+        uint32_t nz = 0;
+        for (int b = br.x; b < br.y; ++b) nz += uh[bu + b] != 0u ? 1u : 0u;
+        uint32_t nrec = 0;
+        uint32_t at = 1u + blk_scan2(B, nz, 0u, &nrec, nullptr).x;
+        if (nz != 0u)
+          for (int b = br.x; b < br.y; ++b) {
+            const uint32_t c = uh[bu + b];
+            if (c != 0u) rec[at++] = ((bu + static_cast<uint32_t>(b)) << 17) | c;
+          }
+        if (B.tid == 0) rec[0] = nrec;
+        blk_publish(B, sync_word(s, 0));
       }
     }
   }
+  // the units inside the range (whole sequences): shared between the groups by parity
+  for (int i = uf + 1 + g; i < ul - 1; i += 2)
+    for (int q = 0; q < Q; ++q) select_local(i, q);
+  if (ex < 0) {
+    B.sync();
+    return;
+  }
 
-  // Phase B: the threshold bin of each longer segment from every unit's published bins, this unit's
-  // candidates, and the merge by the last unit.
-  for (int i = uf; i < ul; ++i) {
-    const DecodeUnit u = v.units[i];
-    for (int q = 0; q < Q; ++q) {
-      const SegCtx s = seg_ctx(u, q);
-      if (s.sg.nunits == 1 || s.kk >= clampi(s.row_end - s.sg.kb, 0, s.sg.ke - s.sg.kb)) continue;
-      const int nu = s.sg.nunits, fu = s.sg.first_unit;
-      if (!blk_wait_count(B, sync_word(s, 0), static_cast<uint32_t>(nu), abort_flag, p.status)) continue;
-      // record counts of every unit -> offsets (a contiguous chunk of units per thread)
-      uint32_t* uoff = P + C::P_UOFF;
-      uint32_t* ucnt = P + C::P_UCNT;
-      const int cper = (nu + B.nt - 1) / B.nt;
-      const int c0 = min(nu, B.tid * cper), c1 = min(nu, c0 + cper);
-      uint32_t mine = 0;
-      // (a count is at most the unit's keys and the number of bins: anything else could only be a
-      // workspace that was not zero-filled, and is clamped so that every read stays in the unit's area)
-      for (int j = c0; j < c1; ++j) {
-        const DecodeUnit uj = v.units[fu + j];
-        const uint32_t cap = static_cast<uint32_t>(min(kL1Bins, max(uj.ke - uj.kb, 0)));
-        const uint32_t c = min(ldcg_u32(rec_base(fu + j, q)), cap);
-        uoff[j] = c;
-        mine += c;
+  // ---- B1: the threshold bin from every unit's bins; this unit's keys inside it --------------
+  const DecodeUnit& u = ue;
+  const int nseg = nseg_e;
+  for (int q = 0; q < Q; ++q) {
+    const SegCtx s = seg_ctx_of(u, se, ctx_e, q);
+    TaskState& ts = ks->task[g][q];
+    if (B.tid == 0) ts.ok = 0u;
+    if (s.sg.nunits == 1 || !exchanged(s)) continue;
+    const int nu = min(s.sg.nunits, kDecodeMaxCtas);
+    if (!blk_wait_count(B, sync_word(s, 0), static_cast<uint32_t>(s.sg.nunits), abort_flag, p.status)) continue;
+    // record counts -> offsets. A count is at most the unit's keys and the number of bins: anything
+    // else could only come from a workspace that was not zero-filled, and is clamped so that every
+    // read stays inside the unit's own area.
+    uint32_t* uoff = P + C::P_UOFF;
+    const int cper = (nu + B.nt - 1) / B.nt;
+    const int c0 = min(nu, B.tid * cper), c1 = min(nu, c0 + cper);
+    uint32_t mine = 0;
+    for (int j = c0; j < c1; ++j) {
+      const uint32_t cap = static_cast<uint32_t>(min(kL1Bins, unit_tiles(s.sg, j) * kTileKeys));
+      const uint32_t c = min(ldcg_u32(rec_of(s.sg, j, q)), cap);
+      uoff[j] = c;
+      mine += c;
+    }
+    uint32_t R = 0;
+    uint32_t run = blk_scan2(B, mine, 0u, &R, nullptr).x;
+    for (int j = c0; j < c1; ++j) {
+      const uint32_t c = uoff[j];
+      uoff[j] = run;
+      run += c;
+    }
+    if (B.tid == 0) uoff[nu] = R;
+    blk_zero(B, hist, kL1Bins + 64);
+    B.sync();
+    auto unit_of = [&](int f) {
+      int lo = 0, hi = nu - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int>(uoff[mid]) <= f) lo = mid; else hi = mid - 1;
       }
-      uint32_t R = 0;
-      uint32_t run = blk_scan2(B, mine, 0u, &R, nullptr).x;
-      for (int j = c0; j < c1; ++j) {
-        const uint32_t c = uoff[j];
-        uoff[j] = run;
-        run += c;
+      return lo;
+    };
+    uint2* recs = reinterpret_cast<uint2*>(P + C::P_REC);
+    const bool staged = static_cast<int>(R) <= C::RCAP;
+    auto record = [&](int f) {
+      if (staged) return recs[f];
+      const int j = unit_of(f);
+      return make_uint2(ldcg_u32(rec_of(s.sg, j, q) + 1 + (f - static_cast<int>(uoff[j]))), static_cast<uint32_t>(j));
+    };
+    for (int f = B.tid; f < static_cast<int>(R); f += B.nt) {
+      const int j = unit_of(f);
+      const uint32_t r = ldcg_u32(rec_of(s.sg, j, q) + 1 + (f - static_cast<int>(uoff[j])));
+      if (staged) recs[f] = make_uint2(r, static_cast<uint32_t>(j));
+      const uint32_t b = (r >> 17) & (kL1Bins - 1), c = r & 0x1FFFFu;
+      smem_red_add(&hist[b], c);
+      smem_red_add(&hist[kL1Bins + (b >> 6)], c);
+    }
+    B.sync();
+    if (warp == 0) {
+      const uint2 tb = warp_find_bin2<64, 64>(hist, hist + kL1Bins, static_cast<uint32_t>(s.kk), lane);
+      if (lane == 0) {
+        ts.bin = tb.x;
+        ts.need = static_cast<uint32_t>(s.kk) - tb.y;
       }
-      if (B.tid == 0) uoff[nu] = R;
-      blk_zero(B, hist, kL1Bins);
-      blk_zero(B, ucnt, nu);
-      B.sync();
-      auto unit_of = [&](int f) {
-        int lo = 0, hi = nu - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (static_cast<int>(uoff[mid]) <= f) lo = mid; else hi = mid - 1;
-        }
-        return lo;
-      };
-      uint2* recs = reinterpret_cast<uint2*>(P + C::P_REC);
-      const bool staged = static_cast<int>(R) <= C::RCAP;
-      auto record = [&](int f) {
-        if (staged) return recs[f];
-        const int j = unit_of(f);
-        return make_uint2(ldcg_u32(rec_base(fu + j, q) + 1 + (f - static_cast<int>(uoff[j]))), static_cast<uint32_t>(j));
-      };
-      for (int f = B.tid; f < static_cast<int>(R); f += B.nt) {
-        const int j = unit_of(f);
-        const uint32_t r = ldcg_u32(rec_base(fu + j, q) + 1 + (f - static_cast<int>(uoff[j])));
-        if (staged) recs[f] = make_uint2(r, static_cast<uint32_t>(j));
-        smem_red_add(&hist[(r >> 17) & (kL1Bins - 1)], r & 0x1FFFFu);
-      }
-      B.sync();
-      const uint2 tb = blk_find_bin(B, hist, kL1Bins, static_cast<uint32_t>(s.kk));
-      const uint32_t bstar = tb.x, above = tb.y;
-      for (int f = B.tid; f < static_cast<int>(R); f += B.nt) {
-        const uint2 r = record(f);
-        if (((r.x >> 17) & (kL1Bins - 1)) >= bstar) smem_red_add(&ucnt[r.y], r.x & 0x1FFFFu);
-      }
-      B.sync();
-      // this unit's offset in the segment's candidate array, and the array's length
-      mine = 0;
-      for (int j = c0; j < c1; ++j) mine += ucnt[j];
-      uint32_t M = 0;
-      run = blk_scan2(B, mine, 0u, &M, nullptr).x;
-      for (int j = c0; j < c1; ++j) {
-        const uint32_t c = ucnt[j];
-        ucnt[j] = run;
-        run += c;
-      }
-      B.sync();
-      const uint32_t my_off = ucnt[i - fu];
-      // this unit's keys at or above the threshold bin, in token order
-      const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
-      const uint32_t* keys = lg + q * C::CAP + u.buf;
-      const int2 kr = blk_run(B, un);
-      uint32_t c = 0;
-      for (int x = kr.x; x < kr.y; ++x) c += (keys[x] >> kL1Shift) >= bstar ? 1u : 0u;
-      uint32_t o = my_off + blk_scan2(B, c, 0u, nullptr, nullptr).x;
-      // (offsets past the segment's own keys can only come from inconsistent counts: not written)
-      uint2* dst = cand_base(s);
-      const uint32_t seg_keys = static_cast<uint32_t>(s.sg.ke - s.sg.kb);
-      if (c != 0u)
-        for (int x = kr.x; x < kr.y; ++x) {
-          const uint32_t k = keys[x];
-          if ((k >> kL1Shift) >= bstar) {
-            if (o < seg_keys) dst[o] = make_uint2(k, static_cast<uint32_t>(u.kb + x));
-            ++o;
+    }
+    // per unit: keys above the bin (before this unit) and inside it (their prefix over units)
+    uint32_t* eqpre = P + C::P_EQPRE + q * (kDecodeMaxCtas + 4);
+    blk_zero(B, eqpre, nu + 1);
+    if (B.tid == 0) cnt[2] = 0u;
+    B.sync();
+    const uint32_t bstar = ts.bin;
+    const int me = u.uidx;
+    uint32_t gt_before = 0;
+    for (int f = B.tid; f < static_cast<int>(R); f += B.nt) {
+      const uint2 r = record(f);
+      const uint32_t b = (r.x >> 17) & (kL1Bins - 1), c = r.x & 0x1FFFFu;
+      if (b == bstar) eqpre[r.y + 1] = c;
+      if (b > bstar && static_cast<int>(r.y) < me) gt_before += c;
+    }
+    if (gt_before != 0u) atomicAdd(&cnt[2], gt_before);
+    B.sync();
+    mine = 0;
+    for (int j = c0; j < c1; ++j) mine += eqpre[j + 1];
+    run = blk_scan2(B, mine, 0u, nullptr, nullptr).x;
+    for (int j = c0; j < c1; ++j) {
+      run += eqpre[j + 1];
+      eqpre[j + 1] = run;
+    }
+    if (B.tid == 0) {
+      ts.gt_before = cnt[2];
+      ts.ok = 1u;
+    }
+    B.sync();
+    // this unit's keys inside the threshold bin, low 20 bits, in token order
+    const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
+    const uint32_t* keys = lg + q * C::CAP + u.buf;
+    uint32_t* dst = list_of(s.sg, u.uidx, q);
+    const uint32_t my_eq = eqpre[me + 1] - eqpre[me];
+    const int2 kr = blk_run4(B, un);
+    uint32_t c = 0;
+#pragma unroll 4
+    for (int x = kr.x; x < kr.y; x += 4) {
+      const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c += (x + e < kr.y && (vec_lane(vv, e) >> kL1Shift) == bstar) ? 1u : 0u;
+    }
+    uint32_t listed = 0;
+    uint32_t at = blk_scan2(B, c, 0u, &listed, nullptr).x;
+    if (c != 0u)
+      for (int x = kr.x; x < kr.y; x += 4) {
+        const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t k = vec_lane(vv, e);
+          if (x + e < kr.y && (k >> kL1Shift) == bstar) {
+            if (at < my_eq) dst[at] = k & 0xFFFFFu;
+            ++at;
           }
         }
-      if (blk_ticket(B, sync_word(s, 1), static_cast<uint32_t>(nu)))
-        merge_segment(s, static_cast<int>(min(M, seg_keys)), false, bstar, above);
-    }
+      }
+    if (B.tid == 0 && listed != my_eq) set_status(p.status, IDX_FP4_DEV_SYNC);
+    blk_publish(B, sync_word(s, 1));
   }
+  B.sync();  // every row's task state is settled
+
+  // ---- B2: the exact threshold from every unit's bin keys; this unit's selected keys ---------
+  for (int q = 0; q < Q; ++q) {
+    const SegCtx s = seg_ctx_of(u, se, ctx_e, q);
+    const TaskState& ts = ks->task[g][q];
+    if (ts.ok == 0u) continue;
+    const int nu = min(s.sg.nunits, kDecodeMaxCtas);
+    if (!blk_wait_count(B, sync_word(s, 1), static_cast<uint32_t>(s.sg.nunits), abort_flag, p.status)) continue;
+    const uint32_t* eqpre = P + C::P_EQPRE + q * (kDecodeMaxCtas + 4);
+    const int me = u.uidx;
+    const int L = static_cast<int>(eqpre[nu]);
+    auto src = [&](int x) {
+      int lo = 0, hi = nu - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<int>(eqpre[mid]) <= x) lo = mid; else hi = mid - 1;
+      }
+      return list_of(s.sg, lo, q) + (x - static_cast<int>(eqpre[lo]));
+    };
+    uint32_t* list = P + C::P_LIST;
+    const bool staged = L <= C::LIST_CAP;
+    if (staged) {
+      for (int x = B.tid; x < L; x += B.nt) list[x] = ldcg_u32(src(x));
+      B.sync();
+    }
+    auto low = [&](int x) { return staged ? list[x] : (ldcg_u32(src(x)) & 0xFFFFFu); };
+    // two radix levels (10 + 10 bits) inside the bin, each a 1024-bin histogram with 32 coarse bins
+    uint32_t need = ts.need, tlow = 0u;
+#pragma unroll 1
+    for (int level = 0; level < 2; ++level) {
+      blk_zero(B, lvl, 1024 + 32);
+      B.sync();
+      for (int x = B.tid; x < L; x += B.nt) {
+        const uint32_t l = low(x);
+        const uint32_t d = level == 0 ? (l >> 10) : (l & 1023u);
+        if (level == 0 || (l >> 10) == (tlow >> 10)) {
+          smem_red_add(&lvl[d], 1u);
+          smem_red_add(&lvl[1024 + (d >> 5)], 1u);
+        }
+      }
+      B.sync();
+      if (warp == 0) {
+        const uint2 r = warp_find_bin2<32, 32>(lvl, lvl + 1024, need, lane);
+        if (lane == 0) {
+          cnt[1] = r.x;
+          cnt[2] = r.y;
+        }
+      }
+      B.sync();
+      tlow |= cnt[1] << (level == 0 ? 10 : 0);
+      need -= cnt[2];
+      B.sync();
+    }
+    // keys of the bin above T and equal to T in the segment's earlier units, and equal in this one
+    if (B.tid == 0) {
+      cnt[0] = 0u;
+      cnt[1] = 0u;
+      cnt[3] = 0u;
+    }
+    B.sync();
+    uint32_t a_gt = 0, a_eq = 0, m_eq = 0;
+    const int e0 = static_cast<int>(eqpre[me]), e1 = static_cast<int>(eqpre[me + 1]);
+    for (int x = B.tid; x < e1; x += B.nt) {
+      const uint32_t l = low(x);
+      if (x < e0) {
+        a_gt += l > tlow ? 1u : 0u;
+        a_eq += l == tlow ? 1u : 0u;
+      } else {
+        m_eq += l == tlow ? 1u : 0u;
+      }
+    }
+    if (a_gt != 0u) atomicAdd(&cnt[0], a_gt);
+    if (a_eq != 0u) atomicAdd(&cnt[1], a_eq);
+    if (m_eq != 0u) atomicAdd(&cnt[3], m_eq);
+    B.sync();
+    const uint32_t T = (ts.bin << kL1Shift) | tlow;
+    const uint32_t eq_before = cnt[1];
+    const uint32_t take = need > eq_before ? min(need - eq_before, cnt[3]) : 0u;
+    const uint32_t off = ts.gt_before + cnt[0] + min(eq_before, need);
+    // this unit's selected keys in token order, at `off`
+    const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
+    const uint32_t* keys = lg + q * C::CAP + u.buf;
+    const int2 run = blk_run4(B, un);
+    uint32_t gt = 0, eq = 0;
+#pragma unroll 4
+    for (int x = run.x; x < run.y; x += 4) {
+      const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t k = vec_lane(vv, e);
+        gt += (x + e < run.y && k > T) ? 1u : 0u;
+        eq += (x + e < run.y && k == T) ? 1u : 0u;
+      }
+    }
+    const uint2 pre = blk_scan2(B, gt, eq, nullptr, nullptr);
+    const RowOut out = seg_out(p, ws, s, nseg, Q);
+    uint32_t pos = off + pre.x + min(pre.y, take), eqr = pre.y;
+    if (gt + eq != 0u)
+      for (int x = run.x; x < run.y; x += 4) {
+        const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t k = vec_lane(vv, e);
+          const bool in = x + e < run.y;
+          const bool eqk = in && k == T;
+          if ((in && k > T) || (eqk && eqr < take)) out(pos++, k, u.kb + x + e);
+          eqr += eqk ? 1u : 0u;
+        }
+      }
+    finish_exchange(s, true);
+  }
+  B.sync();
+  const int pending = ks->pending[g];
+  for (int k = 0; k < pending; ++k) {
+    const int code = ks->pending_seq[g][k];
+    merge_sequence<H, Q>(p, v, ws, code / kMaxNextN, code % kMaxNextN, P, B);
+  }
+  B.sync();
 }
 
 template <int H, int Q>
@@ -990,36 +1242,45 @@ __global__ void __launch_bounds__(DecodeCfg<H, Q>::THREADS, 1) decode_kernel(con
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  // Rounds: the epilogue warps publish each round's range and, after the round's stream, run its
-  // selection; the stage warps stream each round's tiles. Register budgets are set once per role.
+  // Rounds: the epilogue warps publish each round's range; the stage warps stream its tiles and the
+  // epilogue warps read them out; then every warp, in two selection groups, selects the round's
+  // units. Register budgets are re-split for the stream and evened out for the selection.
   const int rounds = ks->h.rounds;
-  if (warp < C::STAGES) {
-    warpgroup_regs_dec<C::STAGE_REGS>();
-    for (int r = 0; r < rounds; ++r) {
-      named_barrier_sync(kRoundBarrier, C::THREADS);
-      if (ks->round[r & 1].uf < ks->round[r & 1].ul) stream_stage_warp<H, Q>(p, smem, r & 1, warp, lane);
-    }
-  } else {
-    warpgroup_regs_inc<C::EPI_REGS>();
-    const int etid = static_cast<int>(threadIdx.x) - C::EPI_WARP0 * 32;
-    const Blk B{etid, C::EPI_THREADS, kSelBarrier, reinterpret_cast<uint32_t*>(smem + C::OFF_SCR)};
-    int tiles = 0, units = 0;  // streamed in earlier rounds (kept by every epilogue thread alike)
-    for (int r = 0; r < rounds; ++r) {
-      const int slot = r & 1;
+  const bool stage_role = warp < C::STAGES;
+  int tiles = 0, units = 0;  // streamed in earlier rounds (kept by every epilogue thread alike)
+  for (int r = 0; r < rounds; ++r) {
+    const int slot = r & 1;
+    if (stage_role) {
+      warpgroup_regs_dec<C::STAGE_REGS>();
+      named_barrier_sync(kAllBarrier, C::THREADS);
+      if (ks->round[slot].uf < ks->round[slot].ul) stream_stage_warp<H, Q>(p, smem, slot, warp, lane);
+      warpgroup_regs_inc<C::LAUNCH_REGS>();
+    } else {
+      warpgroup_regs_inc<C::EPI_REGS>();
+      const int etid = static_cast<int>(threadIdx.x) - C::EPI_WARP0 * 32;
       const DecodeSchedView v = sched_view(p, ks->h);
       const int ri = r * ks->h.ctas + static_cast<int>(blockIdx.x);
       const int uf = v.range_first[ri], ul = v.range_first[ri + 1];
       if (etid == 0) ks->round[slot] = RoundInfo{uf, ul, tiles, units};
-      fence_proxy_async_smem();  // the selection's writes to the stage area precede the bulk copies
-      named_barrier_sync(kRoundBarrier, C::THREADS);
-      if (uf >= ul) continue;
-      stream_epilogue_warp<H, Q>(p, smem, slot, warp - C::EPI_WARP0, lane);
-      B.sync();  // every tile is read out: the stage area is free and the row buffer complete
-      select_round<H, Q>(p, smem, slot, B);
-      for (int i = uf; i < ul; ++i) tiles += dunit_tiles(v.units[i]);
-      units += ul - uf;
-      B.sync();
+      named_barrier_sync(kAllBarrier, C::THREADS);
+      if (uf < ul) {
+        stream_epilogue_warp<H, Q>(p, smem, slot, warp - C::EPI_WARP0, lane);
+        for (int i = uf; i < ul; ++i) tiles += dunit_tiles(v.units[i]);
+        units += ul - uf;
+      }
+      warpgroup_regs_dec<C::LAUNCH_REGS>();
     }
+    // every tile is read out: the stage area is free and the row buffer complete
+    named_barrier_sync(kAllBarrier, C::THREADS);
+    if (ks->round[slot].uf < ks->round[slot].ul) {
+      const int g = stage_role ? 0 : 1;
+      const int gtid = static_cast<int>(threadIdx.x) - (stage_role ? 0 : C::EPI_WARP0 * 32);
+      const Blk B{gtid, C::THREADS / 2, stage_role ? kSelBarrier0 : kSelBarrier1,
+                  reinterpret_cast<uint32_t*>(smem + C::OFF_SCR) + g * 128};
+      select_round<H, Q>(p, smem, slot, g, B);
+    }
+    fence_proxy_async_smem();  // the selection's writes to the stage area precede the next bulk copies
+    named_barrier_sync(kAllBarrier, C::THREADS);
   }
   tc_fence_before_sync();
   __syncthreads();
