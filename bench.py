@@ -4,11 +4,16 @@
 One step = one decode step of the hot path on the long-context workload (16 sequences x
 131072 cached keys, 64 index heads, head_dim 128, top-2048, MXFP4 paged cache with block 64):
 the writer quantises the step's new key and query heads, the schedule is rebuilt, and the
-decode scorer scores every cached key and selects each sequence's top-k. The step is captured
-once in CUDA graphs and replayed; an L2-sized buffer is rewritten between timed steps. The
-causal-prefill workload (4 prompts of 2634..4295 tokens in 512-row steps) is timed in the same
-run and reported in the line's "prefill" object, and prefill over a staged flat cache (one
-16384-token prompt, identity page table) in "prefill_flat".
+decode kernel scores every cached key and selects each sequence's top-k. Writer + schedule and
+the decode call are each captured in a CUDA graph and replayed; between timed steps a buffer
+twice the L2 size is written and then read, so each step starts with none of its inputs in L2
+and no dirty lines left to write back.
+
+The same line carries, as sub-objects: the other decode workloads (batch 1 x 4096, batch 8 x
+96K..128K, batch 8 x 262144), graph replay across changing context sets, the writer and the
+schedule on their own, decode with two verify rows per sequence (next_n 2) through the decode
+and the prefill calls, causal prefill (4 prompts of 2634..4295 tokens in 512-row steps) and
+prefill over a staged flat cache, and the oracle on the host cores (all cores, and one core).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -21,7 +26,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import re
 import statistics
@@ -38,7 +42,12 @@ UNIT = "keys/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio of the FP4 and bf16 tensor rates
-SCORER_SOURCES = ["scorer.cu", "topk.cuh", "ptx.cuh", "common.cuh"]
+# the decode kernel's sources; the committed ncu traffic figure holds while their code is unchanged
+DECODE_SOURCES = ["decode_kernel.cuh", "block.cuh", "decode_sched.cuh", "ptx.cuh", "common.cuh", "decode.cu",
+                  "decode_n1.cu"]
+DECODE_PROFILE = "decode_kernel_b16_ctx131072.txt"
+L2_NOTE = ("inputs (142.6 MB of keys) larger than L2, and a 2x-L2 buffer written then read between timed "
+           "calls (no step input left in L2, no dirty line left to write back); graph-replayed calls")
 
 
 def parse_args(argv=None):
@@ -172,19 +181,18 @@ def _code_only(text: str) -> str:
     return " ".join(text.split())
 
 
-def scorer_source_hash() -> str:
-    """Hash of the scorer's code (comments and layout ignored): the committed ncu traffic figure is
-    used only while the code it was measured on is unchanged."""
+def decode_source_hash() -> str:
+    """Hash of the decode kernel's code (comments and layout ignored)."""
     h = hashlib.sha256()
-    for name in SCORER_SOURCES:
+    for name in DECODE_SOURCES:
         with open(os.path.join(ROOT, "fp4_sparse_attention_mxfp4_gb300", "csrc", name)) as f:
             h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic():
-    """DRAM bytes per scorer launch from the committed ncu summary, if it still matches the source."""
-    path = os.path.join(ROOT, "profiles", "decode_scorer_b16_ctx131072.txt")
+    """DRAM bytes per decode launch from the committed ncu summary, if it still matches the source."""
+    path = os.path.join(ROOT, "profiles", DECODE_PROFILE)
     try:
         kv = {}
         with open(path) as f:
@@ -192,7 +200,7 @@ def profiled_traffic():
                 if "=" in ln and not ln.startswith("#"):
                     k, v = ln.strip().split("=", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("source_hash") == scorer_source_hash():
+        if kv.get("source_hash") == decode_source_hash():
             return float(kv["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -201,25 +209,47 @@ def profiled_traffic():
 
 # ---- workloads ---------------------------------------------------------------------------
 
-def decode_alg_bytes(ctx_lens, heads: int, topk: int) -> int:
-    """Algorithmic bytes of one decode call: 68 B per key (64 packed + 4 scale), 4 B per page-table
-    entry read, 72 B per query head (64 + 4 packed/scales, 4 weight) and 8 B per output slot."""
+def decode_alg_bytes(ctx_lens, heads: int, topk: int, next_n: int = 1) -> int:
+    """Algorithmic bytes of one decode call: 68 B per key (64 packed + 4 scale) read once for all
+    next_n rows, 4 B per page-table entry, and per query row 72 B per head (64 + 4 packed/scales,
+    4 weight) and 8 B per output slot."""
     tot = 0
     for c in ctx_lens:
         c = int(c)
-        tot += 68 * c + 4 * (-(-c // 64)) + heads * (68 + 4) + topk * 8
+        tot += 68 * c + 4 * (-(-c // 64)) + next_n * (heads * (68 + 4) + topk * 8)
     return tot
 
 
+class L2Flush:
+    """Between timed calls: write a buffer of twice the L2 size, then read it back, so the next
+    call finds none of its inputs in L2 and no dirty lines to write back."""
+
+    def __init__(self, torch):
+        props = torch.cuda.get_device_properties(torch.cuda.current_device())
+        l2 = getattr(props, "L2_cache_size", 128 << 20)
+        self.buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device="cuda")
+
+    def __call__(self):
+        self.buf.fill_(1)
+        self.buf.sum()
+
+
 class DecodeBench:
+    """One decode workload resident on the device: cache filled once (setup), per-step inputs, and
+    the writer + schedule and decode calls, each capturable in a graph. Works for a DecodeCase
+    (one row per sequence) and an MtpCase (next_n verify rows per sequence, decode-shaped call)."""
+
     def __init__(self, case):
         import numpy as np
         import torch
 
         import fp4_sparse_attention_mxfp4_gb300 as fx
-        self.fx, self.torch, self.case = fx, torch, case
+        self.fx, self.torch, self.np, self.case = fx, torch, np, case
+        self.next_n = n = int(getattr(case, "next_n", 1))
         B, H, k = case.batch, case.heads, case.topk
+        R = B * n
         d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+        self.d = d
         self.kv_p = torch.full((case.layout.num_pages, 4, 64, 16), 0x77, dtype=torch.uint8, device="cuda")
         self.kv_s = torch.full((case.layout.num_pages, 4, 64), 0xFF, dtype=torch.uint8, device="cuda")
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -229,33 +259,66 @@ class DecodeBench:
         for a in range(0, slots.size, chunk):
             fx.idx_fp4_quant_and_cache(d(case.k_bf16[a:a + chunk].view(np.int16)), d(slots[a:a + chunk]),
                                        self.kv_p, self.kv_s, status=self.status)
-        # per-step inputs: the newest key of each sequence and the query heads
-        last = np.cumsum(case.ctx_lens) - 1
-        self.k_new = d(case.k_bf16[last].view(np.int16))
-        self.slots_new = d(slots[last])
+        # per-step inputs: each sequence's newest next_n keys and the query heads
+        ends = np.cumsum(case.ctx_lens)
+        new = np.concatenate([np.arange(e - n, e) for e in ends])
+        self.k_new = d(case.k_bf16[new].view(np.int16))
+        self.slots_new = d(slots[new])
         self.q_bf16 = d(case.q_bf16.view(np.int16))
-        self.q_packed = torch.empty((B, H, 64), dtype=torch.uint8, device="cuda")
-        self.q_scale = torch.empty((B, H, 4), dtype=torch.uint8, device="cuda")
+        self.q_packed = torch.empty((R, H, 64), dtype=torch.uint8, device="cuda")
+        self.q_scale = torch.empty((R, H, 4), dtype=torch.uint8, device="cuda")
         self.w = d(case.w)
         self.bt = d(case.layout.block_tables)
         self.ctx = d(case.ctx_lens)
         self.max_ctx = int(case.ctx_lens.max())
         self.sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(B, self.max_ctx), dtype=torch.uint8, device="cuda")
-        self.ws = torch.zeros(fx.idx_fp4_decode_workspace_bytes(B, self.max_ctx, k), dtype=torch.uint8, device="cuda")
-        self.topk_idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
-        self.topk_val = torch.empty((B, k), dtype=torch.float32, device="cuda")
+        ws = fx.idx_fp4_decode_mtp_workspace_bytes(B, self.max_ctx, k, n)
+        self.ws = torch.zeros(ws, dtype=torch.uint8, device="cuda")
+        self.topk_idx = torch.empty((R, k), dtype=torch.int32, device="cuda")
+        self.topk_val = torch.empty((R, k), dtype=torch.float32, device="cuda")
         torch.cuda.synchronize()
 
+    def set_contexts(self, ctx_lens):
+        """A new context-length set in the same device buffers (between graph replays): the
+        sequences' lengths, and the keys and slots of their newest positions (each sequence's keys
+        are a prefix of its full context, so the cache stays consistent)."""
+        np, case, n = self.np, self.case, self.next_n
+        ctx_lens = np.asarray(ctx_lens, np.int32)
+        assert np.all(ctx_lens >= n) and np.all(ctx_lens <= case.ctx_lens)
+        starts = np.cumsum(case.ctx_lens) - case.ctx_lens
+        new = np.concatenate([np.arange(s + c - n, s + c) for s, c in zip(starts, ctx_lens)])
+        slots = np.concatenate([case.layout.slots(b, int(c) - n, int(c)) for b, c in enumerate(ctx_lens)])
+        self.ctx.copy_(self.d(ctx_lens))
+        self.k_new.copy_(self.d(case.k_bf16[new].view(np.int16)))
+        self.slots_new.copy_(self.d(slots.astype(np.int32)))
+        self.torch.cuda.synchronize()
+
+    def write(self):
+        self.fx.idx_fp4_quant_and_cache(self.k_new, self.slots_new, self.kv_p, self.kv_s, q_bf16=self.q_bf16,
+                                        q_packed=self.q_packed, q_scale=self.q_scale, status=self.status)
+
+    def schedule(self):
+        if self.next_n == 1:
+            self.fx.idx_fp4_build_decode_schedule(self.ctx, self.case.batch, self.max_ctx, self.sched,
+                                                  status=self.status)
+        else:
+            self.fx.idx_fp4_build_decode_schedule_mtp(self.ctx, self.next_n, self.case.batch, self.max_ctx,
+                                                      self.sched, status=self.status)
+
     def prep(self):
-        fx = self.fx
-        fx.idx_fp4_quant_and_cache(self.k_new, self.slots_new, self.kv_p, self.kv_s, q_bf16=self.q_bf16,
-                                   q_packed=self.q_packed, q_scale=self.q_scale, status=self.status)
-        fx.idx_fp4_build_decode_schedule(self.ctx, self.case.batch, self.max_ctx, self.sched, status=self.status)
+        self.write()
+        self.schedule()
 
     def decode(self):
-        self.fx.idx_fp4_decode_logits_topk(self.q_packed, self.q_scale, self.w, self.kv_p, self.kv_s, self.bt,
-                                           self.ctx, self.case.topk, self.sched, self.ws, self.topk_idx,
-                                           self.topk_val, status=self.status)
+        fx = self.fx
+        if self.next_n == 1:
+            fx.idx_fp4_decode_logits_topk(self.q_packed, self.q_scale, self.w, self.kv_p, self.kv_s, self.bt,
+                                          self.ctx, self.case.topk, self.sched, self.ws, self.topk_idx,
+                                          self.topk_val, status=self.status)
+        else:
+            fx.idx_fp4_decode_mtp_logits_topk(self.q_packed, self.q_scale, self.w, self.kv_p, self.kv_s, self.bt,
+                                              self.ctx, self.next_n, self.case.topk, self.sched, self.ws,
+                                              self.topk_idx, self.topk_val, status=self.status)
 
     def capture(self):
         torch = self.torch
@@ -268,28 +331,36 @@ class DecodeBench:
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         self.g_prep, self.g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        self.g_write, self.g_sched = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.g_prep):
             self.prep()
         with torch.cuda.graph(self.g_dec):
             self.decode()
+        with torch.cuda.graph(self.g_write):
+            self.write()
+        with torch.cuda.graph(self.g_sched):
+            self.schedule()
         torch.cuda.synchronize()
 
+    def ok(self):
+        return int(self.status.item()) == 0
 
-def run_decode_timed(bench: DecodeBench, steps: int, warmup: int, dist, clock: ClockSampler):
+
+def time_decode(bench: DecodeBench, steps: int, warmup: int, flush: L2Flush, dist=None, clock=None):
+    """Replays writer + schedule and the decode call `steps` times (after `warmup` untimed steps),
+    with events around each graph on the launching stream and an L2 flush between steps. Returns
+    per-step milliseconds of the whole step and of the decode call, and the clock record."""
     torch = bench.torch
-    props = torch.cuda.get_device_properties(0)
-    l2 = getattr(props, "L2_cache_size", 128 << 20)
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device="cuda")
-    bench.capture()
     for _ in range(warmup):
         bench.g_prep.replay()
         bench.g_dec.replay()
-        flush.fill_(1)
+        flush()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize()
     barrier(dist)
-    clock.start()
+    if clock is not None:
+        clock.start()
     torch.cuda.synchronize()
     for e0, e1, e2 in ev:
         e0.record()
@@ -297,13 +368,92 @@ def run_decode_timed(bench: DecodeBench, steps: int, warmup: int, dist, clock: C
         e1.record()
         bench.g_dec.replay()
         e2.record()
-        flush.fill_(1)
+        flush()
     torch.cuda.synchronize()
     barrier(dist)
-    clocks = clock.stop()
+    clocks = clock.stop() if clock is not None else None
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     dec_ms = [b.elapsed_time(c) for _, b, c in ev]
     return step_ms, dec_ms, clocks
+
+
+def time_graph(torch, graph, steps: int, warmup: int, flush: L2Flush, before=None):
+    """Mean milliseconds of one graph replay, L2 flushed between replays."""
+    for _ in range(warmup):
+        if before is not None:
+            before()
+        graph.replay()
+        flush()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        graph.replay()
+        b.record()
+        flush()
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def shape_line(name, case, dec_ms, hbm, next_n=1, extra=None):
+    alg = decode_alg_bytes(case.ctx_lens, case.heads, case.topk, next_n)
+    dec_s = statistics.mean(dec_ms) / 1e3
+    keys = int(case.ctx_lens.sum())
+    out = {"workload": name, "batch": int(case.batch), "keys": keys, "us_per_call": dec_s * 1e6,
+           "us_min": min(dec_ms) * 1e3, "keys_per_s": keys / dec_s, "alg_bytes": alg,
+           "hbm_frac": alg / dec_s / 1e9 / hbm}
+    if extra:
+        out.update(extra)
+    return out
+
+
+def run_decode_shapes(steps: int, warmup: int, flush: L2Flush, hbm: float, single_row_us: float):
+    """The other decode workloads, each at its own size, plus decode with two verify rows."""
+    import synth
+    import torch
+    shapes = []
+    for n, name in [(2, "batch 1 x 4096 keys (latency-bound)"), (3, "batch 8 x 96K..128K keys"),
+                    (5, "batch 8 x 262144 keys")]:
+        case = synth.decode_config(n)
+        b = DecodeBench(case)
+        b.capture()
+        _, dec_ms, _ = time_decode(b, steps, warmup, flush)
+        shapes.append(shape_line(name, case, dec_ms, hbm, extra={"status_ok": b.ok()}))
+        del b
+        torch.cuda.empty_cache()
+    case = synth.mtp_config()
+    b = DecodeBench(case)
+    b.capture()
+    _, dec_ms, _ = time_decode(b, steps, warmup, flush)
+    mtp = shape_line("decode, next_n 2 verify rows per sequence, decode-shaped call: 16 x 131072 keys, 64 heads, "
+                     "top-2048 per row", case, dec_ms, hbm, next_n=2,
+                     extra={"row_key_pairs_per_s": int(case.row_ends().astype("int64").sum()) /
+                            (statistics.mean(dec_ms) / 1e3),
+                            "vs_single_row_call": statistics.mean(dec_ms) * 1e3 / single_row_us,
+                            "status_ok": b.ok()})
+    del b
+    torch.cuda.empty_cache()
+    return shapes, mtp
+
+
+def run_replay_sets(bench: DecodeBench, steps: int, warmup: int, flush: L2Flush, hbm: float):
+    """One captured writer + schedule + decode graph pair replayed across changing context-length
+    sets (the buffers' contents change, the graphs do not): decode time per set."""
+    import synth
+    case = bench.case
+    sets = synth.replay_ctx_sets(3, case.batch, bench.max_ctx)
+    names = ["all 131072", "U[65536, 131072]", "U[1, 131072], first below k", "all 131072 again"]
+    out = []
+    ok = True
+    for name, ctx in zip(names, sets):
+        bench.set_contexts(ctx)
+        _, dec_ms, _ = time_decode(bench, steps, warmup, flush)
+        ok = ok and bench.ok()
+        sub = type("C", (), {})()
+        sub.ctx_lens, sub.heads, sub.topk, sub.batch = ctx, case.heads, case.topk, case.batch
+        out.append(shape_line(name, sub, dec_ms, hbm))
+    bench.set_contexts(case.ctx_lens)
+    return {"sets": out, "status_ok": ok}
 
 
 def run_decode_e2e(bench: DecodeBench, steps: int, warmup: int):
@@ -363,7 +513,7 @@ def run_decode_e2e(bench: DecodeBench, steps: int, warmup: int):
     return statistics.mean(times), h2d, d2h
 
 
-def run_prefill(steps: int, warmup: int, case=None):
+def run_prefill(steps: int, warmup: int, flush: L2Flush, case=None):
     """Causal prefill of a PrefillCase (default: 4 prompts of 2634..4295 tokens) in 512-row steps,
     all steps captured in one graph; returns seconds per full prefill pass and the algorithmic
     FLOPs of a pass."""
@@ -416,24 +566,23 @@ def run_prefill(steps: int, warmup: int, case=None):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         one_pass()
-    flush = torch.empty((256 << 20) // 4, dtype=torch.int32, device="cuda")
     for _ in range(warmup):
         g.replay()
-        flush.fill_(1)
+        flush()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize()
     for a, b in ev:
         a.record()
         g.replay()
         b.record()
-        flush.fill_(1)
+        flush()
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
     ok = int(status.item()) == 0
     return statistics.mean(ms) / 1e3, flops, len(case.steps), ok
 
 
-def run_mtp(steps: int, warmup: int):
+def run_mtp_prefill_form(steps: int, warmup: int, flush: L2Flush):
     """Decode with two verify rows per sequence (16 x 131072 keys, next_n 2) through the prefill
     call, captured in a graph and replayed with an L2 flush between calls. Returns seconds per
     call, (query row, key) pairs scored per call, algorithmic bytes per call and the status."""
@@ -478,26 +627,26 @@ def run_mtp(steps: int, warmup: int):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         call()
-    flush = torch.empty((256 << 20) // 4, dtype=torch.int32, device="cuda")
     for _ in range(warmup):
         g.replay()
-        flush.fill_(1)
+        flush()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize()
     for a, b in ev:
         a.record()
         g.replay()
         b.record()
-        flush.fill_(1)
+        flush()
     torch.cuda.synchronize()
     sec = statistics.mean(a.elapsed_time(b) for a, b in ev) / 1e3
     pairs = int(case.row_ends().astype(np.int64).sum())
-    alg = decode_alg_bytes(case.ctx_lens, H * n, k * n)  # keys once; n query rows' operands and outputs
+    alg = decode_alg_bytes(case.ctx_lens, H, k, n)  # keys once; n query rows' operands and outputs
     return sec, pairs, alg, int(status.item()) == 0
 
 
-def oracle_decode_rate(case, threads: int, min_seconds: float = 8.0, max_reps: int = 5):
-    """The oracle (fp64 scoring + exact sort top-k) on the given decode workload, host cores."""
+def oracle_decode_rate(case, threads: int, min_seconds: float, max_reps: int = 5):
+    """The oracle (fp64 scoring + exact sort top-k) on the given decode workload, host cores:
+    keys per second over whole repetitions."""
     import numpy as np
 
     import oracle
@@ -522,9 +671,7 @@ def workload_config(case):
     return {"workload": "decode: 16 sequences x 131072 cached keys, 64 index heads, head_dim 128, top-2048, "
                         "MXFP4 paged index cache (page 64, swizzled scale plane), random page tables",
             "batch": int(case.batch), "ctx_len": int(case.ctx_lens[0]), "heads": int(case.heads),
-            "topk": int(case.topk), "cache_bytes_per_key": 68,
-            "l2": "256 MiB buffer rewritten between timed steps; graph-replayed steps",
-            "seed": 3}
+            "topk": int(case.topk), "cache_bytes_per_key": 68, "l2": L2_NOTE, "seed": 3}
 
 
 def run_reference(args):
@@ -572,7 +719,8 @@ def run_reference(args):
 
 
 def run_profile(args):
-    """Direct launches of the decode step (no graphs, no flush) for an ncu capture."""
+    """Direct launches of the decode step (no graphs, no flush) for an ncu capture: writer,
+    schedule and decode kernel per step, on the 16 x 131072 workload."""
     import synth
     import torch
     bench = DecodeBench(synth.decode_config(4))
@@ -580,9 +728,23 @@ def run_profile(args):
         bench.prep()
         bench.decode()
     torch.cuda.synchronize()
-    print(json.dumps({"profile_run": "decode b16 x 131072", "launches_per_step": 4,
+    print(json.dumps({"profile_run": "decode b16 x 131072", "launches_per_step": 3,
                       "status": int(bench.status.item())}), flush=True)
-    return 0 if int(bench.status.item()) == 0 else 1
+    return 0 if bench.ok() else 1
+
+
+def cpu_baselines(case):
+    """The oracle as it stands on the host cores: all cores on the full workload, and one core on
+    a bounded sample of it (the 16 sequences' first 16384 keys)."""
+    import synth
+    threads = os.cpu_count() or 1
+    rate, reps, keys = oracle_decode_rate(case, threads, min_seconds=6.0)
+    sample = synth.decode_case("decode sample 16 x 16384", 3, [16384] * 16, case.heads, case.topk)
+    rate1, reps1, keys1 = oracle_decode_rate(sample, 1, min_seconds=6.0)
+    return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"the full workload ({keys} keys) scored and selected {reps}x, fp64 oracle, {threads} threads",
+            "single_core": {"value": rate1, "unit": UNIT, "cores": 1,
+                            "sample": f"16 sequences x 16384 keys ({keys1} keys) scored and selected {reps1}x"}}
 
 
 def run_ours(args):
@@ -594,67 +756,78 @@ def run_ours(args):
     dist = dist_init("nccl") if world > 1 else None
     import fp4_sparse_attention_mxfp4_gb300 as fx
     fx.lib()
+    hbm, bf16, bf16_sus, peak_kind = measured_peaks()
     case = synth.decode_config(4)
     bench = DecodeBench(case)
+    bench.capture()
+    flush = L2Flush(torch)
     clock = ClockSampler(gpu_index_for_smi(local))
-    step_ms, dec_ms, clocks = run_decode_timed(bench, args.steps, args.warmup, dist, clock)
+    step_ms, dec_ms, clocks = time_decode(bench, args.steps, args.warmup, flush, dist, clock)
     keys_per_step = int(case.ctx_lens.sum())
     local_seconds = sum(step_ms) / 1e3
     value, seconds_max = aggregate(dist, keys_per_step * args.steps, local_seconds, device="cuda")
     ms_per_step = seconds_max / args.steps * 1e3
     dec_mean_s = statistics.mean(dec_ms) / 1e3
-    hbm, bf16, bf16_sus, peak_kind = measured_peaks()
     alg = decode_alg_bytes(case.ctx_lens, case.heads, case.topk)
     achieved = alg / dec_mean_s / 1e9
-    traffic = profiled_traffic()
-    ok = int(bench.status.item()) == 0
+    ok = bench.ok()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp4->f32", "data": "synthetic",
         "config": workload_config(case) | {"parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "decode_us_per_layer": dec_mean_s * 1e6,
-        "roofline": {"bound": "hbm", "kernel": "idx_fp4_decode_logits_topk (scorer + merge)",
+        "decode_us_min": min(dec_ms) * 1e3,
+        "step_us": {"writer+schedule": statistics.mean(s - d for s, d in zip(step_ms, dec_ms)) * 1e3,
+                    "decode": dec_mean_s * 1e6},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (idx_fp4_decode_logits_topk: one cooperative launch, "
+                                               "scoring and exact top-k)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": f"{peak_kind} hbm_gbs", "alg_bytes_per_launch": alg,
-                     "traffic": traffic},
-        "gpu_launches": 4 * args.steps,
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)", "alg_bytes_per_launch": alg,
+                     "traffic": profiled_traffic()},
+        "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "status_ok": ok,
     }
     if not args.no_extras:
+        n_small = max(10, min(args.steps, 50))
         e2e_s, h2d, d2h = run_decode_e2e(bench, max(10, min(args.steps, 100)), 3)
         e2e_val, _ = aggregate(dist, keys_per_step, e2e_s, device="cuda")
         line["e2e"] = {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-        pf_s, pf_flops, pf_steps, pf_ok = run_prefill(max(5, min(args.steps, 50)), 3)
+        line["writer_schedule_alone_us"] = {
+            "writer (16 keys + 16 x 64 query heads)": time_graph(torch, bench.g_write, n_small, 3, flush) * 1e3,
+            "schedule": time_graph(torch, bench.g_sched, n_small, 3, flush) * 1e3}
+        line["graph_replay_ctx_sets"] = run_replay_sets(bench, n_small, 3, flush, hbm)
+        single_row_us = dec_mean_s * 1e6
+        del bench
+        torch.cuda.empty_cache()
+        shapes, mtp = run_decode_shapes(n_small, 3, flush, hbm, single_row_us)
+        line["decode_shapes"] = shapes
+        line["decode_mtp"] = mtp
+        mt_s, mt_pairs, mt_alg, mt_ok = run_mtp_prefill_form(n_small, 3, flush)
+        line["decode_mtp_prefill_form"] = {
+            "workload": "the same next_n 2 rows through the prefill call", "us_per_layer": mt_s * 1e6,
+            "row_key_pairs_per_s": mt_pairs / mt_s, "alg_bytes_per_call": mt_alg,
+            "hbm_frac": mt_alg / mt_s / 1e9 / hbm, "status_ok": mt_ok}
         fp4_peak = bf16 * FP4_OVER_BF16
+        pf_s, pf_flops, pf_steps, pf_ok = run_prefill(max(5, min(args.steps, 50)), 3, flush)
         line["prefill"] = {
             "workload": "causal prefill: 4 prompts (2634..4295 tokens), 512-row steps with padding rows, "
                         "64 heads, top-2048", "steps_per_pass": pf_steps, "ms_per_pass": pf_s * 1e3,
             "alg_flop_per_pass": pf_flops, "tflops": pf_flops / pf_s / 1e12,
             "peak_tflops": fp4_peak, "peak_source": f"{peak_kind} bf16_tflops x {FP4_OVER_BF16:g} (nominal FP4/bf16)",
             "frac_fp4_peak": pf_flops / pf_s / 1e12 / fp4_peak, "status_ok": pf_ok}
-        import synth
-        mt_s, mt_pairs, mt_alg, mt_ok = run_mtp(max(10, min(args.steps, 50)), 3)
-        line["decode_mtp"] = {
-            "workload": "decode with 2 verify rows per sequence (next_n 2) through the prefill call: 16 x 131072 "
-                        "keys, 64 heads, top-2048", "us_per_layer": mt_s * 1e6, "row_key_pairs_per_s": mt_pairs / mt_s,
-            "alg_bytes_per_call": mt_alg, "hbm_frac": mt_alg / mt_s / 1e9 / hbm, "status_ok": mt_ok}
-        pf_s, pf_flops, pf_steps, pf_ok = run_prefill(max(5, min(args.steps, 20)), 3, synth.prefill_flat_config())
+        pf_s, pf_flops, pf_steps, pf_ok = run_prefill(max(5, min(args.steps, 20)), 3, flush,
+                                                      synth.prefill_flat_config())
         line["prefill_flat"] = {
             "workload": "causal prefill over a staged flat cache (identity page table): one 16384-token prompt, "
                         "512-row steps with padding rows, 64 heads, top-2048; rows past 8192 keys merged from "
                         "key chunks", "steps_per_pass": pf_steps, "ms_per_pass": pf_s * 1e3,
             "alg_flop_per_pass": pf_flops, "tflops": pf_flops / pf_s / 1e12, "peak_tflops": fp4_peak,
             "frac_fp4_peak": pf_flops / pf_s / 1e12 / fp4_peak, "status_ok": pf_ok}
+        ok = ok and all(s["status_ok"] for s in shapes) and mtp["status_ok"] and pf_ok
         if rank == 0 and world == 1:
-            del bench
-            torch.cuda.empty_cache()
-            threads = os.cpu_count() or 1
-            rate, reps, keys = oracle_decode_rate(case, threads)
-            line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                    "sample": f"the full workload ({keys} keys) scored and selected {reps}x, "
-                                              "fp64 oracle on the host cores"}
+            line["cpu_baseline"] = cpu_baselines(case)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -294,3 +294,20 @@ def test_decode_schedule_invariants():
             assert skb == mine[0][0] and ske == mine[-1][1]
         nsegs += int(seq_nseg[b])
     assert nsegs == h["num_segs"]
+
+
+def test_decode_several_rounds():
+    """More keys than one pass of the grid holds (a range is at most 16384 keys at next_n 1): the
+    step runs in rounds, sequences cut by a round boundary are merged from their segments' lists.
+    Rows of sequences on both sides of the boundary against the oracle, and the schedule's rounds."""
+    sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 256)
+    per_round = sms * 128 * 128
+    nseq = -(-(per_round * 9 // 8) // 131072)
+    ctx = [131072] * (nseq - 1) + [100003]
+    case = synth.decode_case("rounds", 41, ctx, 64, 2048)
+    run = DecodeRun(case).run()
+    h = parse_decode_schedule(run.sched, run.max_batch)[0]
+    assert h["rounds"] >= 2 and h["ok"] == 1
+    boundary = min(h["ctas"] * h["per"] // 1024, nseq - 1)  # the sequence holding the first round's end
+    ref = _oracle_side(case)
+    _check_decode(run, ref, rows=[0, boundary, nseq - 1], full_logits=True)
