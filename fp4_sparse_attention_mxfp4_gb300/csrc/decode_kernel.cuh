@@ -125,7 +125,7 @@ struct DecodeCfg {
   static constexpr uint32_t BAR_QFREE = BAR_QREADY + 2;
   static constexpr uint32_t OFF_BAR = OFF_SCR + 2 * 128 * 4;
   static constexpr uint32_t OFF_KS = OFF_BAR + NUM_BARS * 8;  // KernelShared
-  static constexpr uint32_t SMEM_BYTES = OFF_KS + 384;
+  static constexpr uint32_t SMEM_BYTES = OFF_KS + 512;
   static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM");
   static_assert(OFF_LG % 16 == 0 && OFF_QB % 128 == 0, "operand and row-buffer alignment");
   // The selection phase reuses the stage area (free once the stream has ended): each of the two
@@ -144,6 +144,10 @@ struct DecodeCfg {
   static constexpr int CCAP = (P_SOFF - P_CAND) / 2 / 128 * 128;
   static_assert(P_EQPRE + Q * (kDecodeMaxCtas + 4) <= P_SOFF && CCAP >= 1024, "selection areas fit");
   static_assert(P_HIST % 4 == 0 && P_LVL % 4 == 0, "16-byte aligned histograms");
+  // When the whole CTA selects one unit, the second group's half holds, per row, the row-buffer
+  // positions (16 bits) of the keys that can still be selected.
+  static constexpr int P_CIDX = P_WORDS;
+  static_assert(CAP <= 65536 && Q * CAP / 2 <= P_WORDS, "candidate positions fit the second half");
 };
 
 
@@ -237,6 +241,15 @@ struct RoundInfo {
   int units;    // units this CTA streamed in earlier rounds (query-buffer phases)
 };
 
+// The schedule entries of a range's first or last unit, read into shared memory during the stream.
+struct RangeMeta {
+  DecodeUnit u;
+  DecodeSeg sg;
+  int ctx;   // its sequence's context
+  int nseg;  // its sequence's segments
+  int pad[2];
+};
+
 // An exchange between the units of a segment row, from its first round to its second.
 struct TaskState {
   uint32_t bin;         // threshold bin of the segment row
@@ -255,8 +268,10 @@ struct KernelShared {
   uint32_t counter[2][4];        // per selection group
   int pending[2];                // sequence merges deferred to the end of a group's selection
   int pending_seq[2][kMaxNextN];
+  RangeMeta meta[2];             // the round's first and last units (written during the stream)
+  uint32_t ncand[kMaxNextN];     // per row: candidate positions listed (whole-CTA selection)
 };
-static_assert(sizeof(KernelShared) <= 384, "fits its slot");
+static_assert(sizeof(KernelShared) <= 512, "fits its slot");
 
 __device__ __forceinline__ DecodeSchedView sched_view(const DecodeParams& p, const DecodeSchedHeader& h) {
   return decode_sched_view(const_cast<void*>(p.sched), h.max_batch, h.ranges_cap, h.units_cap);
@@ -539,6 +554,13 @@ __device__ __forceinline__ void stream_epilogue_warp(const DecodeParams& p, uint
     for (int x = etid; x < 2 * C::HST_WORDS; x += C::EPI_THREADS) hst[x] = 0u;  // ordered by prep's barrier
   if (it.count > 0) prep_query<H, Q>(p, it.at(0), st.units, smem, tmem, etid);
   if (it.count > 1) prep_query<H, Q>(p, it.at(1), st.units + 1, smem, tmem, etid);
+  // the last group's first thread, idle until that group's first tile, reads the entries the
+  // selection starts from
+  if (e == C::EPI_WARPS - 4 && lane == 0 && it.count > 0)
+    for (int m = 0; m < 2; ++m) {
+      const DecodeUnit u = it.at(m == 0 ? 0 : it.count - 1);
+      ks->meta[m] = RangeMeta{u, v.segs[u.seg], seq_ctx[u.seq], v.seq_nseg[u.seq], {0, 0}};
+    }
   int t0 = st.tiles;  // CTA-wide number of the unit's first tile
   for (int i = 0; i < it.count; ++i) {
     const DecodeUnit u = it.at(i);
@@ -794,6 +816,9 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   uint32_t* cnt = ks->counter[g];
   const uint32_t* lg = reinterpret_cast<const uint32_t*>(smem + C::OFF_LG);
   const int topk = p.topk;
+  // the whole CTA selects the range's one unit: candidate positions are listed in the second half
+  const bool compact = B.nt == C::THREADS;
+  uint16_t* cidx = reinterpret_cast<uint16_t*>(reinterpret_cast<uint32_t*>(smem) + C::P_CIDX);
   const int lane = B.lane(), warp = B.warp();
   const int ex = g == 0 ? uf : (ul - 1 > uf ? ul - 1 : -1);  // this group's range-end unit
   auto seg_ctx_of = [&](const DecodeUnit& u, const DecodeSeg& sg, int ctx, int q) {
@@ -807,15 +832,16 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     return s;
   };
   auto seg_ctx = [&](const DecodeUnit& u, int q) { return seg_ctx_of(u, v.segs[u.seg], v.seq_ctx[u.seq], q); };
-  // the range-end unit's schedule entries, read once (each read is a round trip to L2)
+  // the range-end unit's schedule entries, read into shared memory during the stream
   DecodeUnit ue{};
   DecodeSeg se{};
   int ctx_e = 0, nseg_e = 0;
   if (ex >= 0) {
-    ue = v.units[ex];
-    se = v.segs[ue.seg];
-    ctx_e = v.seq_ctx[ue.seq];
-    nseg_e = v.seq_nseg[ue.seq];
+    const RangeMeta& m = ks->meta[ex == uf ? 0 : 1];
+    ue = m.u;
+    se = m.sg;
+    ctx_e = m.ctx;
+    nseg_e = m.nseg;
   }
   auto seg_keys = [&](const SegCtx& s) { return clampi(s.row_end - s.sg.kb, 0, s.sg.ke - s.sg.kb); };
   auto sync_word = [&](const SegCtx& s, int k) { return &ws.sync[(static_cast<int64_t>(s.seg_id) * Q + s.q) * 4 + k]; };
@@ -932,6 +958,30 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
           }
         if (B.tid == 0) rec[0] = nrec;
         blk_publish(B, sync_word(s, 0));
+        if (compact) {
+          // While the other units publish: list the positions of this unit's keys at or above its
+          // own k-th key's bin, in token order. The segment's threshold is at or above that bin,
+          // so the later passes need only these.
+          uint16_t* ci = cidx + q * C::CAP;
+          const int2 kr = blk_run4(B, un);
+          uint32_t c = 0;
+#pragma unroll 4
+          for (int x = kr.x; x < kr.y; x += 4) {
+            const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c += (x + e < kr.y && (vec_lane(vv, e) >> kL1Shift) >= bu) ? 1u : 0u;
+          }
+          uint32_t listed = 0;
+          uint32_t at = blk_scan2(B, c, 0u, &listed, nullptr).x;
+          if (c != 0u)
+            for (int x = kr.x; x < kr.y; x += 4) {
+              const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (x + e < kr.y && (vec_lane(vv, e) >> kL1Shift) >= bu) ci[at++] = static_cast<uint16_t>(x + e);
+            }
+          if (B.tid == 0) ks->ncand[q] = listed;
+        }
       }
     }
   }
@@ -1040,28 +1090,44 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     const uint32_t* keys = lg + q * C::CAP + u.buf;
     uint32_t* dst = list_of(s.sg, u.uidx, q);
     const uint32_t my_eq = eqpre[me + 1] - eqpre[me];
-    const int2 kr = blk_run4(B, un);
-    uint32_t c = 0;
-#pragma unroll 4
-    for (int x = kr.x; x < kr.y; x += 4) {
-      const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) c += (x + e < kr.y && (vec_lane(vv, e) >> kL1Shift) == bstar) ? 1u : 0u;
-    }
     uint32_t listed = 0;
-    uint32_t at = blk_scan2(B, c, 0u, &listed, nullptr).x;
-    if (c != 0u)
-      for (int x = kr.x; x < kr.y; x += 4) {
-        const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t k = vec_lane(vv, e);
-          if (x + e < kr.y && (k >> kL1Shift) == bstar) {
+    if (compact) {
+      const uint16_t* ci = cidx + q * C::CAP;
+      const int2 kr = blk_run(B, static_cast<int>(ks->ncand[q]));
+      uint32_t c = 0;
+      for (int f = kr.x; f < kr.y; ++f) c += (keys[ci[f]] >> kL1Shift) == bstar ? 1u : 0u;
+      uint32_t at = blk_scan2(B, c, 0u, &listed, nullptr).x;
+      if (c != 0u)
+        for (int f = kr.x; f < kr.y; ++f) {
+          const uint32_t k = keys[ci[f]];
+          if ((k >> kL1Shift) == bstar) {
             if (at < my_eq) dst[at] = k & 0xFFFFFu;
             ++at;
           }
         }
+    } else {
+      const int2 kr = blk_run4(B, un);
+      uint32_t c = 0;
+#pragma unroll 4
+      for (int x = kr.x; x < kr.y; x += 4) {
+        const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c += (x + e < kr.y && (vec_lane(vv, e) >> kL1Shift) == bstar) ? 1u : 0u;
       }
+      uint32_t at = blk_scan2(B, c, 0u, &listed, nullptr).x;
+      if (c != 0u)
+        for (int x = kr.x; x < kr.y; x += 4) {
+          const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t k = vec_lane(vv, e);
+            if (x + e < kr.y && (k >> kL1Shift) == bstar) {
+              if (at < my_eq) dst[at] = k & 0xFFFFFu;
+              ++at;
+            }
+          }
+        }
+    }
     if (B.tid == 0 && listed != my_eq) set_status(p.status, IDX_FP4_DEV_SYNC);
     blk_publish(B, sync_word(s, 1));
   }
@@ -1074,6 +1140,13 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     if (ts.ok == 0u) continue;
     const int nu = min(s.sg.nunits, kDecodeMaxCtas);
     if (!blk_wait_count(B, sync_word(s, 1), static_cast<uint32_t>(s.sg.nunits), abort_flag, p.status)) continue;
+    // Every unit is past its wait on the second count once all have counted themselves here; the
+    // last one then clears the row's counters. With one segment nothing else depends on this ticket,
+    // so one thread takes it now and its answer is read at the end (with several segments the
+    // ticket also orders the segment lists before the sequence merge, and is taken after them).
+    bool last_done = false;
+    if (nseg <= 1 && B.tid == 0)
+      last_done = atom_add_acq_rel_gpu(sync_word(s, 2), 1u) + 1u == static_cast<uint32_t>(s.sg.nunits);
     const uint32_t* eqpre = P + C::P_EQPRE + q * (kDecodeMaxCtas + 4);
     const int me = u.uidx;
     const int L = static_cast<int>(eqpre[nu]);
@@ -1088,7 +1161,24 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     uint32_t* list = P + C::P_LIST;
     const bool staged = L <= C::LIST_CAP;
     if (staged) {
-      for (int x = B.tid; x < L; x += B.nt) list[x] = ldcg_u32(src(x));
+      // warp w copies the lists of units w, w + warps, ... (coalesced, loads issued ahead)
+      for (int j = warp; j < nu; j += B.nw()) {
+        const int a = static_cast<int>(eqpre[j]), n = static_cast<int>(eqpre[j + 1]) - a;
+        const uint32_t* from = list_of(s.sg, j, q);
+        for (int x0 = 0; x0 < n; x0 += 128) {
+          uint32_t r[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int x = x0 + e * 32 + lane;
+            r[e] = x < n ? ldcg_u32(from + x) : 0u;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int x = x0 + e * 32 + lane;
+            if (x < n) list[a + x] = r[e];
+          }
+        }
+      }
       B.sync();
     }
     auto low = [&](int x) { return staged ? list[x] : (ldcg_u32(src(x)) & 0xFFFFFu); };
@@ -1148,34 +1238,61 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     // this unit's selected keys in token order, at `off`
     const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
     const uint32_t* keys = lg + q * C::CAP + u.buf;
-    const int2 run = blk_run4(B, un);
-    uint32_t gt = 0, eq = 0;
-#pragma unroll 4
-    for (int x = run.x; x < run.y; x += 4) {
-      const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t k = vec_lane(vv, e);
-        gt += (x + e < run.y && k > T) ? 1u : 0u;
-        eq += (x + e < run.y && k == T) ? 1u : 0u;
-      }
-    }
-    const uint2 pre = blk_scan2(B, gt, eq, nullptr, nullptr);
     const RowOut out = seg_out(p, ws, s, nseg, Q);
-    uint32_t pos = off + pre.x + min(pre.y, take), eqr = pre.y;
-    if (gt + eq != 0u)
+    if (compact) {
+      const uint16_t* ci = cidx + q * C::CAP;
+      const int2 run = blk_run(B, static_cast<int>(ks->ncand[q]));
+      uint32_t gt = 0, eq = 0;
+      for (int f = run.x; f < run.y; ++f) {
+        const uint32_t k = keys[ci[f]];
+        gt += k > T ? 1u : 0u;
+        eq += k == T ? 1u : 0u;
+      }
+      const uint2 pre = blk_scan2(B, gt, eq, nullptr, nullptr);
+      uint32_t pos = off + pre.x + min(pre.y, take), eqr = pre.y;
+      if (gt + eq != 0u)
+        for (int f = run.x; f < run.y; ++f) {
+          const int x = ci[f];
+          const uint32_t k = keys[x];
+          const bool eqk = k == T;
+          if (k > T || (eqk && eqr < take)) out(pos++, k, u.kb + x);
+          eqr += eqk ? 1u : 0u;
+        }
+    } else {
+      const int2 run = blk_run4(B, un);
+      uint32_t gt = 0, eq = 0;
+#pragma unroll 4
       for (int x = run.x; x < run.y; x += 4) {
         const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const uint32_t k = vec_lane(vv, e);
-          const bool in = x + e < run.y;
-          const bool eqk = in && k == T;
-          if ((in && k > T) || (eqk && eqr < take)) out(pos++, k, u.kb + x + e);
-          eqr += eqk ? 1u : 0u;
+          gt += (x + e < run.y && k > T) ? 1u : 0u;
+          eq += (x + e < run.y && k == T) ? 1u : 0u;
         }
       }
-    finish_exchange(s, true);
+      const uint2 pre = blk_scan2(B, gt, eq, nullptr, nullptr);
+      uint32_t pos = off + pre.x + min(pre.y, take), eqr = pre.y;
+      if (gt + eq != 0u)
+        for (int x = run.x; x < run.y; x += 4) {
+          const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t k = vec_lane(vv, e);
+            const bool in = x + e < run.y;
+            const bool eqk = in && k == T;
+            if ((in && k > T) || (eqk && eqr < take)) out(pos++, k, u.kb + x + e);
+            eqr += eqk ? 1u : 0u;
+          }
+        }
+    }
+    if (nseg > 1) {
+      finish_exchange(s, true);
+    } else if (last_done) {
+      *sync_word(s, 0) = 0u;
+      *sync_word(s, 1) = 0u;
+      *sync_word(s, 2) = 0u;
+    }
   }
   B.sync();
   const int pending = ks->pending[g];
@@ -1272,7 +1389,12 @@ __global__ void __launch_bounds__(DecodeCfg<H, Q>::THREADS, 1) decode_kernel(con
     }
     // every tile is read out: the stage area is free and the row buffer complete
     named_barrier_sync(kAllBarrier, C::THREADS);
-    if (ks->round[slot].uf < ks->round[slot].ul) {
+    if (ks->round[slot].ul - ks->round[slot].uf == 1) {
+      // a range inside one sequence (one unit): every warp of the CTA selects it, as group 0
+      const Blk B{static_cast<int>(threadIdx.x), C::THREADS, kSelBarrier0,
+                  reinterpret_cast<uint32_t*>(smem + C::OFF_SCR)};
+      select_round<H, Q>(p, smem, slot, 0, B);
+    } else if (ks->round[slot].uf < ks->round[slot].ul) {
       const int g = stage_role ? 0 : 1;
       const int gtid = static_cast<int>(threadIdx.x) - (stage_role ? 0 : C::EPI_WARP0 * 32);
       const Blk B{gtid, C::THREADS / 2, stage_role ? kSelBarrier0 : kSelBarrier1,
