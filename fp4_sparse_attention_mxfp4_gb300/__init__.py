@@ -9,6 +9,10 @@ asynchronously on the current (or given) stream:
     idx_fp4_decode_logits_topk     decode: score every cached key of each sequence, top-k
     idx_fp4_decode_mtp_logits_topk decode with next_n verify rows per sequence (one key pass)
     idx_fp4_prefill_logits_topk    causal prefill: score keys [0, row_end) per row, top-k
+    idx_fp4_build_decode_schedule_range  decode over key ranges (a key shard per call)
+    idx_fp4_merge_candidates       exact top-k of the union of several shards' candidate lists
+
+``shard.py`` holds the host side of key-sharded decode (ranges per shard, gather, merge).
 """
 from ._lib import (  # noqa: F401
     DEV_BAD_CTX,
@@ -24,6 +28,7 @@ from ._lib import (  # noqa: F401
     STATIC_SCRATCH_BYTES,
     idx_fp4_build_decode_schedule,
     idx_fp4_build_decode_schedule_mtp,
+    idx_fp4_build_decode_schedule_range,
     idx_fp4_decode_logits_topk,
     idx_fp4_decode_mtp_logits_topk,
     idx_fp4_decode_mtp_workspace_bytes,
@@ -31,6 +36,7 @@ from ._lib import (  # noqa: F401
     idx_fp4_decode_static_bytes,
     idx_fp4_decode_schedule_bytes,
     idx_fp4_decode_workspace_bytes,
+    idx_fp4_merge_candidates,
     idx_fp4_prefill_logits_topk,
     idx_fp4_prefill_workspace_bytes,
     idx_fp4_quant_and_cache,

@@ -50,6 +50,8 @@ SIGNATURES = {
     "idx_fp4_decode_mtp_workspace_bytes": (_SZ, [_I32, _I64, _I32, _I32]),
     "idx_fp4_decode_mtp_logits_topk": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I32, _P,
                                               _SZ, _P, _SZ, _P, _P, _P, _I64, _P, _P]),
+    "idx_fp4_build_decode_schedule_range": (_I32, [_P, _P, _I32, _I32, _I64, _P, _SZ, _P, _P]),
+    "idx_fp4_merge_candidates": (_I32, [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]),
     "idx_fp4_prefill_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I64, _I32]),
     "idx_fp4_decode_static_bytes": (_SZ, [_I32, _I64, _I32]),
     "idx_fp4_decode_logits_topk_static": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I64, _P,
@@ -168,6 +170,46 @@ def idx_fp4_build_decode_schedule(ctx_lens, max_batch: int, max_ctx: int, sched,
     code = lib().idx_fp4_build_decode_schedule(_ptr(ctx_lens), ctx_lens.shape[0], int(max_batch), int(max_ctx),
                                                _ptr(sched), sched.numel(), _ptr(status), _stream(stream))
     _check("idx_fp4_build_decode_schedule", code)
+
+
+def idx_fp4_build_decode_schedule_range(key_begin, key_end, max_batch: int, max_ctx: int, sched, status=None,
+                                        stream=None):
+    """Decode schedule over the key ranges [key_begin[b], key_end[b]) (device int32 [B] each;
+    key_begin a multiple of 128). Run the decode call with key_end as its ctx_lens."""
+    _need(key_begin, "key_begin", torch.int32, 1)
+    _need(key_end, "key_end", torch.int32, 1)
+    if key_begin.shape != key_end.shape:
+        raise ValueError("key_begin and key_end must have the same shape")
+    _need(sched, "sched", torch.uint8, 1)
+    if status is not None:
+        _need(status, "status", torch.int32)
+    code = lib().idx_fp4_build_decode_schedule_range(_ptr(key_begin), _ptr(key_end), key_end.shape[0], int(max_batch),
+                                                     int(max_ctx), _ptr(sched), sched.numel(), _ptr(status),
+                                                     _stream(stream))
+    _check("idx_fp4_build_decode_schedule_range", code)
+
+
+def idx_fp4_merge_candidates(cand_val, cand_idx, topk: int, topk_idx, topk_val=None, status=None, stream=None):
+    """Exact top-k of the union of candidate lists per row: cand_val f32 / cand_idx int32
+    [lists, rows, k_in] (index < 0 = empty) -> topk_idx [rows, topk] (ascending, -1 padded) and
+    topk_val (nullable)."""
+    _need(cand_val, "cand_val", torch.float32, 3)
+    _need(cand_idx, "cand_idx", torch.int32, 3)
+    if cand_val.shape != cand_idx.shape:
+        raise ValueError("cand_val and cand_idx must have the same shape")
+    W, R, K = cand_idx.shape
+    _need(topk_idx, "topk_idx", torch.int32, 2)
+    if tuple(topk_idx.shape) != (R, int(topk)):
+        raise ValueError(f"topk_idx must be [{R}, {topk}]")
+    if topk_val is not None:
+        _need(topk_val, "topk_val", torch.float32, 2)
+        if tuple(topk_val.shape) != (R, int(topk)):
+            raise ValueError(f"topk_val must be [{R}, {topk}]")
+    if status is not None:
+        _need(status, "status", torch.int32)
+    code = lib().idx_fp4_merge_candidates(_ptr(cand_val), _ptr(cand_idx), W, R, K, int(topk), _ptr(topk_idx),
+                                          _ptr(topk_val), _ptr(status), _stream(stream))
+    _check("idx_fp4_merge_candidates", code)
 
 
 def idx_fp4_decode_workspace_bytes(max_batch: int, max_ctx: int, topk: int) -> int:

@@ -15,14 +15,16 @@ cudaError_t launch_quant_and_cache(const uint16_t* k, int64_t num_tokens, const 
                                    uint8_t* kv_scale, int64_t num_pages, const uint16_t* q, int64_t num_q_vec,
                                    uint8_t* q_packed, uint8_t* q_scale, int32_t* status, int num_sms,
                                    cudaStream_t stream);
-cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, int batch, int next_n, int max_batch,
-                                         int64_t max_ctx, int ctas, const DecodeCaps& caps, void* sched,
-                                         int32_t* status, cudaStream_t stream);
+cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, const int32_t* key_begin, int batch, int next_n,
+                                         int max_batch, int64_t max_ctx, int ctas, const DecodeCaps& caps,
+                                         void* sched, int32_t* status, cudaStream_t stream);
 cudaError_t launch_build_prefill_schedule(const int32_t* cu_seqlens, const int32_t* row_ends, const int32_t* ctx_lens,
                                           int num_requests, int num_rows, int rows_per_unit, int table_width,
                                           int64_t units_cap, int64_t slots_cap, void* workspace, int32_t* status,
                                           cudaStream_t stream);
 bool decode_shape_supported(int heads, int next_n);
+cudaError_t launch_merge_candidates(const float* cand_val, const int32_t* cand_idx, int lists, int rows, int k_in,
+                                    int topk, int32_t* topk_idx, float* topk_val, cudaStream_t stream);
 cudaError_t launch_decode(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
                           const uint8_t* kv_packed, const uint8_t* kv_scale, int64_t num_pages,
                           const int32_t* block_tables, int bt_stride, const int32_t* ctx_lens, int batch, int heads,
@@ -77,8 +79,8 @@ size_t decode_ws_bytes(int max_batch, int64_t max_ctx, int topk, int next_n) {
   return decode_ws_bytes_for(caps, max_batch, next_n, topk);
 }
 
-int build_schedule(const int32_t* ctx_lens_dev, int batch, int next_n, int max_batch, int64_t max_ctx, void* sched_dev,
-                   size_t sched_bytes, int32_t* status_dev, cudaStream_t stream) {
+int build_schedule(const int32_t* ctx_lens_dev, const int32_t* key_begin_dev, int batch, int next_n, int max_batch,
+                   int64_t max_ctx, void* sched_dev, size_t sched_bytes, int32_t* status_dev, cudaStream_t stream) {
   if (max_batch < 1 || max_batch > kMaxBatch || batch < 0 || batch > max_batch || max_ctx < 0 || max_ctx > kMaxCtx ||
       next_n < 1 || next_n > kMaxNextN)
     return IDX_FP4_ERR_ARG;
@@ -88,8 +90,8 @@ int build_schedule(const int32_t* ctx_lens_dev, int batch, int next_n, int max_b
   if (sched_bytes < decode_sched_bytes_for(max_batch, caps)) return IDX_FP4_ERR_CAPACITY;
   const int ctas = decode_ctas();
   if (ctas <= 0) return IDX_FP4_ERR_CUDA;
-  return to_code(launch_build_decode_schedule(ctx_lens_dev, batch, next_n, max_batch, max_ctx, ctas, caps, sched_dev,
-                                              status_dev, stream));
+  return to_code(launch_build_decode_schedule(ctx_lens_dev, key_begin_dev, batch, next_n, max_batch, max_ctx, ctas,
+                                              caps, sched_dev, status_dev, stream));
 }
 
 int decode_call(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights, const uint8_t* kv_packed,
@@ -166,13 +168,34 @@ size_t idx_fp4_decode_schedule_bytes(int max_batch, int64_t max_ctx) {
 
 int idx_fp4_build_decode_schedule(const int32_t* ctx_lens_dev, int batch, int max_batch, int64_t max_ctx,
                                   void* sched_dev, size_t sched_bytes, int32_t* status_dev, cudaStream_t stream) {
-  return build_schedule(ctx_lens_dev, batch, 1, max_batch, max_ctx, sched_dev, sched_bytes, status_dev, stream);
+  return build_schedule(ctx_lens_dev, nullptr, batch, 1, max_batch, max_ctx, sched_dev, sched_bytes, status_dev,
+                        stream);
+}
+
+int idx_fp4_build_decode_schedule_range(const int32_t* key_begin_dev, const int32_t* key_end_dev, int batch,
+                                        int max_batch, int64_t max_ctx, void* sched_dev, size_t sched_bytes,
+                                        int32_t* status_dev, cudaStream_t stream) {
+  if (batch > 0 && key_begin_dev == nullptr) return IDX_FP4_ERR_ARG;
+  return build_schedule(key_end_dev, key_begin_dev, batch, 1, max_batch, max_ctx, sched_dev, sched_bytes, status_dev,
+                        stream);
 }
 
 int idx_fp4_build_decode_schedule_mtp(const int32_t* ctx_lens_dev, int batch, int next_n, int max_batch,
                                       int64_t max_ctx, void* sched_dev, size_t sched_bytes, int32_t* status_dev,
                                       cudaStream_t stream) {
-  return build_schedule(ctx_lens_dev, batch, next_n, max_batch, max_ctx, sched_dev, sched_bytes, status_dev, stream);
+  return build_schedule(ctx_lens_dev, nullptr, batch, next_n, max_batch, max_ctx, sched_dev, sched_bytes, status_dev,
+                        stream);
+}
+
+int idx_fp4_merge_candidates(const float* cand_val, const int32_t* cand_idx, int num_lists, int rows, int k_in,
+                             int topk, int32_t* topk_idx, float* topk_val, int32_t* status_dev, cudaStream_t stream) {
+  (void)status_dev;
+  if (num_lists < 1 || rows < 0 || k_in < 1) return IDX_FP4_ERR_ARG;
+  if (topk < 1 || topk > IDX_FP4_MAX_TOPK) return IDX_FP4_ERR_SHAPE;
+  if (static_cast<int64_t>(num_lists) * k_in > IDX_FP4_MERGE_MAX_CANDIDATES) return IDX_FP4_ERR_CAPACITY;
+  if (rows == 0) return IDX_FP4_OK;
+  if (cand_val == nullptr || cand_idx == nullptr || topk_idx == nullptr) return IDX_FP4_ERR_ARG;
+  return to_code(launch_merge_candidates(cand_val, cand_idx, num_lists, rows, k_in, topk, topk_idx, topk_val, stream));
 }
 
 size_t idx_fp4_decode_workspace_bytes(int max_batch, int64_t max_ctx, int topk) {

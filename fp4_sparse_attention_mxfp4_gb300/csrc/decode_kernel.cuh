@@ -140,9 +140,9 @@ struct DecodeCfg {
   static constexpr int RCAP = 1024;
   static constexpr int P_EQPRE = P_REC + 2 * RCAP;    // [Q][kDecodeMaxCtas + 4] prefix of the units' bin keys
   static constexpr int P_SOFF = P_WORDS - 1040;       // [1024 + 1] segment offsets of a sequence merge
-  static constexpr int P_CAND = P_LVL;                // a sequence merge's staged candidates
-  static constexpr int CCAP = (P_SOFF - P_CAND) / 2 / 128 * 128;
-  static_assert(P_EQPRE + Q * (kDecodeMaxCtas + 4) <= P_SOFF && CCAP >= 1024, "selection areas fit");
+  static constexpr int P_CAND = P_LVL;                // a sequence merge's staged candidate keys
+  static constexpr int CCAP = (P_SOFF - P_CAND) / 128 * 128;
+  static_assert(P_EQPRE + Q * (kDecodeMaxCtas + 4) <= P_SOFF && CCAP >= 4096, "selection areas fit");
   static_assert(P_HIST % 4 == 0 && P_LVL % 4 == 0, "16-byte aligned histograms");
   // When the whole CTA selects one unit, the second group's half holds, per row, the row-buffer
   // positions (16 bits) of the keys that can still be selected.
@@ -761,14 +761,16 @@ __device__ void merge_sequence(const DecodeParams& p, const DecodeSchedView& v, 
     }
     return ws.seglists + (static_cast<int64_t>(s0 + lo) * Q + q) * p.topk + (x - static_cast<int>(off[lo]));
   };
-  uint2* cand = reinterpret_cast<uint2*>(P + C::P_CAND);
+  // the keys are staged when they fit (two segments' full lists at least); tokens are read from
+  // the lists for the kept keys only
+  uint32_t* ckey = P + C::P_CAND;
   const bool staged = M <= C::CCAP;
   if (staged) {
-    for (int x = B.tid; x < M; x += B.nt) cand[x] = ldcg_u2(at(x));
+    for (int x = B.tid; x < M; x += B.nt) ckey[x] = ldcg_u2(at(x)).x;
     B.sync();
   }
-  auto key = [&](int x) { return staged ? cand[x].x : ldcg_u2(at(x)).x; };
-  auto tok = [&](int x) { return static_cast<int>(staged ? cand[x].y : ldcg_u2(at(x)).y); };
+  auto key = [&](int x) { return staged ? ckey[x] : ldcg_u2(at(x)).x; };
+  auto tok = [&](int x) { return static_cast<int>(ldcg_u2(at(x)).y); };
   const int64_t row = static_cast<int64_t>(seq) * Q + q;
   const int kk = min(p.topk, row_end);
   RowOut out{p.topk_idx + row * p.topk, p.topk_val != nullptr ? p.topk_val + row * p.topk : nullptr, nullptr,
@@ -865,32 +867,31 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   };
   auto exchanged = [&](const SegCtx& s) { return s.sg.nunits > 1 && s.kk < seg_keys(s); };
   if (B.tid == 0) ks->pending[g] = 0;
-  // A completed segment row: pad its final row, or count it for its sequence (the last segment of a
-  // longer sequence merges the lists, at once or deferred to the end of this group's selection,
-  // since a merge reuses the areas the group's pending exchanges still hold).
-  auto segment_done = [&](const SegCtx& s, bool defer) {
+  // A completed segment row: pad its final row, or count it for its sequence; the last segment of a
+  // longer sequence merges the lists at the end of this group's selection (a merge reuses the areas
+  // the group's exchanges hold). Only a range-end unit can belong to a sequence spanning rounds, so a
+  // group defers at most one merge per row.
+  auto segment_done = [&](const SegCtx& s) {
     const int seq = s.sg.seq, nseg = v.seq_nseg[seq];
     if (nseg <= 1) {
       pad_row(B, p, s.out_row, s.kk);
       return;
     }
-    if (blk_ticket(B, &ws.seqsync[(static_cast<int64_t>(seq) * Q + s.q) * 4], static_cast<uint32_t>(nseg))) {
-      if (!defer) {
-        merge_sequence<H, Q>(p, v, ws, seq, s.q, P, B);
-      } else if (B.tid == 0) {
-        ks->pending_seq[g][ks->pending[g]++] = seq * kMaxNextN + s.q;
-      }
+    if (blk_ticket(B, &ws.seqsync[(static_cast<int64_t>(seq) * Q + s.q) * 4], static_cast<uint32_t>(nseg)) &&
+        B.tid == 0) {
+      if (ks->pending[g] < kMaxNextN) ks->pending_seq[g][ks->pending[g]++] = seq * kMaxNextN + s.q;
+      else set_status(p.status, IDX_FP4_DEV_CAPACITY);
     }
   };
   // The last unit to finish a longer segment row resets the row's counters and completes it.
-  auto finish_exchange = [&](const SegCtx& s, bool defer) {
+  auto finish_exchange = [&](const SegCtx& s) {
     if (blk_ticket(B, sync_word(s, 2), static_cast<uint32_t>(s.sg.nunits))) {
       if (B.tid == 0) {
         *sync_word(s, 0) = 0u;
         *sync_word(s, 1) = 0u;
         *sync_word(s, 2) = 0u;
       }
-      if (v.seq_nseg[s.sg.seq] > 1) segment_done(s, defer);
+      if (v.seq_nseg[s.sg.seq] > 1) segment_done(s);
     }
   };
   // Selection of a unit that is a whole segment row (nothing to wait for).
@@ -902,7 +903,7 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     auto key = [&](int x) { return keys[x]; };
     auto tok = [&](int x) { return u.kb + x; };
     blk_select(B, key, tok, un, s.kk, hist, P + C::P_LIST, C::LIST_CAP, seg_out(p, ws, s, v.seq_nseg[u.seq], Q));
-    segment_done(s, false);
+    segment_done(s);
     B.sync();
   };
 
@@ -915,14 +916,14 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
       const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
       const uint32_t* keys = lg + q * C::CAP + u.buf;
       if (s.sg.nunits == 1) {
-        select_local(ex, q);
+        // a whole segment row: selected with the group's other whole rows below
       } else if (!exchanged(s)) {
         // every key of the segment row is selected: each unit writes its keys at their place
         const RowOut out = seg_out(p, ws, s, nseg, Q);
         const uint32_t base = static_cast<uint32_t>(u.kb - s.sg.kb);
         for (int x = B.tid; x < un; x += B.nt) out(base + static_cast<uint32_t>(x), keys[x], u.kb + x);
         if (u.uidx == 0 && nseg <= 1) pad_row(B, p, s.out_row, s.kk);
-        finish_exchange(s, false);
+        finish_exchange(s);
         B.sync();
       } else {
         const uint32_t* uh;  // fine bins, then 64 coarse bins
@@ -985,9 +986,15 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
       }
     }
   }
-  // the units inside the range (whole sequences): shared between the groups by parity
-  for (int i = uf + 1 + g; i < ul - 1; i += 2)
+  // whole segment rows: the range-end unit's when its segment is whole, and the units inside the
+  // range (whole sequences), shared between the groups by parity (one loop, one copy of the code)
+  const bool ex_whole = ex >= 0 && se.nunits == 1;
+  const int mfirst = uf + 1 + g;
+  const int nmid = mfirst < ul - 1 ? (ul - 1 - mfirst + 1) / 2 : 0;
+  for (int k = 0; k < nmid + (ex_whole ? 1 : 0); ++k) {
+    const int i = ex_whole ? (k == 0 ? ex : mfirst + 2 * (k - 1)) : mfirst + 2 * k;
     for (int q = 0; q < Q; ++q) select_local(i, q);
+  }
   if (ex < 0) {
     B.sync();
     return;
@@ -1287,7 +1294,7 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
         }
     }
     if (nseg > 1) {
-      finish_exchange(s, true);
+      finish_exchange(s);
     } else if (last_done) {
       *sync_word(s, 0) = 0u;
       *sync_word(s, 1) = 0u;
@@ -1389,16 +1396,15 @@ __global__ void __launch_bounds__(DecodeCfg<H, Q>::THREADS, 1) decode_kernel(con
     }
     // every tile is read out: the stage area is free and the row buffer complete
     named_barrier_sync(kAllBarrier, C::THREADS);
-    if (ks->round[slot].ul - ks->round[slot].uf == 1) {
-      // a range inside one sequence (one unit): every warp of the CTA selects it, as group 0
-      const Blk B{static_cast<int>(threadIdx.x), C::THREADS, kSelBarrier0,
-                  reinterpret_cast<uint32_t*>(smem + C::OFF_SCR)};
-      select_round<H, Q>(p, smem, slot, 0, B);
-    } else if (ks->round[slot].uf < ks->round[slot].ul) {
-      const int g = stage_role ? 0 : 1;
-      const int gtid = static_cast<int>(threadIdx.x) - (stage_role ? 0 : C::EPI_WARP0 * 32);
-      const Blk B{gtid, C::THREADS / 2, stage_role ? kSelBarrier0 : kSelBarrier1,
-                  reinterpret_cast<uint32_t*>(smem + C::OFF_SCR) + g * 128};
+    if (ks->round[slot].uf < ks->round[slot].ul) {
+      // A range inside one sequence (one unit) is selected by every warp of the CTA, as group 0;
+      // otherwise the stage warps (group 0) and the epilogue warps (group 1) select side by side.
+      // One call site, so the selection's code is laid out once.
+      const bool whole = ks->round[slot].ul - ks->round[slot].uf == 1;
+      const int g = whole || stage_role ? 0 : 1;
+      const int gtid = static_cast<int>(threadIdx.x) - (g == 0 ? 0 : C::EPI_WARP0 * 32);
+      const Blk B{whole ? static_cast<int>(threadIdx.x) : gtid, whole ? C::THREADS : C::THREADS / 2,
+                  g == 0 ? kSelBarrier0 : kSelBarrier1, reinterpret_cast<uint32_t*>(smem + C::OFF_SCR) + g * 128};
       select_round<H, Q>(p, smem, slot, g, B);
     }
     fence_proxy_async_smem();  // the selection's writes to the stage area precede the next bulk copies

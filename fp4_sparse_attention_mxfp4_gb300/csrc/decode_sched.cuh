@@ -18,7 +18,9 @@ namespace idxfp4 {
 
 constexpr uint32_t kDecodeMagic = 0x44534333u;  // "DSC3"
 constexpr int kMaxNextN = 4;                     // query rows per sequence (speculative verify rows)
-constexpr int kMinTilesPerRange = 8;             // a CTA's share is at least 1024 keys
+constexpr int kMinTilesPerRange = 32;  // a CTA's share is at least 4096 keys: a short sequence stays in
+                                       // one CTA, since streaming 32 tiles there costs less than an exchange
+                                       // between CTAs
 
 // Tiles of one CTA range: its logits (4 bytes per key and row) fill the row buffer.
 __host__ __device__ constexpr int decode_cap_tiles(int next_n) {

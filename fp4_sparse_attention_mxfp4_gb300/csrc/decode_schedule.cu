@@ -8,6 +8,11 @@
 // step's graph reads: all sequences' 128-key tiles are laid end to end and cut into rounds x ctas
 // ranges of `per` tiles. No count on the host depends on device data, so a captured graph replays
 // across changing context lengths. One CTA builds the tables with block scans.
+//
+// A key-range schedule ("Score a DSA sparse indexer in FP4", section "Decode context parallelism":
+// each rank scores its own shard of a sequence's keys and its local top-k is merged with the
+// others') gives each sequence the keys [key_begin, ctx): the first key is a multiple of the
+// 128-key tile, units and segments carry absolute key positions, and the row end stays ctx.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -50,6 +55,7 @@ __device__ int scan_excl(int v, int* warp_sums, int* total) {
 }
 
 __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const int32_t* __restrict__ ctx_lens,
+                                                                        const int32_t* __restrict__ key_begin,
                                                                         int batch, int next_n, int max_batch,
                                                                         int64_t max_ctx, int ctas, DecodeCaps caps,
                                                                         void* sched, int32_t* status) {
@@ -57,6 +63,7 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
   int* s_start = s_dyn;                   // [kMaxBatch + 1] first tile of each sequence
   int* s_ne = s_start + kMaxBatch + 1;    // [kMaxBatch + 1] non-empty sequences before each
   int* s_seg0 = s_ne + kMaxBatch + 1;     // [kMaxBatch + 1] segments before each
+  int* s_kb0 = s_seg0 + kMaxBatch + 1;    // [kMaxBatch] first key of each sequence's range
   __shared__ int warp_sums[32];
   __shared__ int s_total, s_nonempty, s_segs, s_chunk;
   pdl_wait();
@@ -70,14 +77,24 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int b = tid * kPer + j;
-    int c = 0;
+    int c = 0, k0 = 0;
     if (b < batch) {
       const int64_t raw = ctx_lens[b];
       if (raw < 0 || raw > max_ctx) set_status(status, IDX_FP4_DEV_BAD_CTX);
       else c = static_cast<int>(raw);
       v.seq_ctx[b] = c;
+      if (key_begin != nullptr) {
+        const int64_t kb = key_begin[b];
+        if (kb < 0 || kb > c || kb % kTileKeys != 0) {
+          set_status(status, IDX_FP4_DEV_BAD_CTX);
+          k0 = c;  // no keys
+        } else {
+          k0 = static_cast<int>(kb);
+        }
+      }
+      s_kb0[b] = k0;
     }
-    tiles[j] = (c + kTileKeys - 1) / kTileKeys;
+    tiles[j] = (c - k0 + kTileKeys - 1) / kTileKeys;
     ne[j] = tiles[j] > 0 ? 1 : 0;
     my_tiles += tiles[j];
     my_ne += ne[j];
@@ -183,8 +200,8 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
         const int64_t seg_lo = static_cast<int64_t>(r) * round_tiles > sb ? static_cast<int64_t>(r) * round_tiles : sb;
         DecodeUnit u;
         u.seq = b;
-        u.kb = (ulo - sb) * kTileKeys;
-        u.ke = min((uhi - sb) * kTileKeys, v.seq_ctx[b]);
+        u.kb = s_kb0[b] + (ulo - sb) * kTileKeys;
+        u.ke = min(s_kb0[b] + (uhi - sb) * kTileKeys, v.seq_ctx[b]);
         u.buf = (ulo - lo) * kTileKeys;
         u.seg = s_seg0[b] + (r - r0);
         u.uidx = i - static_cast<int>(seg_lo / per);
@@ -213,8 +230,8 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
       s.seq = b;
       s.first_unit = v.range_first[i0] + (s_ne[b] - s_ne[seq_of(i0 * per)]);
       s.nunits = i1 - i0 + 1;
-      s.kb = (slo - sb) * kTileKeys;
-      s.ke = min((shi - sb) * kTileKeys, v.seq_ctx[b]);
+      s.kb = s_kb0[b] + (slo - sb) * kTileKeys;
+      s.ke = min(s_kb0[b] + (shi - sb) * kTileKeys, v.seq_ctx[b]);
       s.rank = k;
       s.tile0 = slo;
       s.pad = 0;
@@ -245,14 +262,14 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
 
 }  // namespace
 
-cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, int batch, int next_n, int max_batch,
-                                         int64_t max_ctx, int ctas, const DecodeCaps& caps, void* sched,
-                                         int32_t* status, cudaStream_t stream) {
-  constexpr size_t smem = sizeof(int) * 3 * (kMaxBatch + 1);
+cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, const int32_t* key_begin, int batch, int next_n,
+                                         int max_batch, int64_t max_ctx, int ctas, const DecodeCaps& caps,
+                                         void* sched, int32_t* status, cudaStream_t stream) {
+  constexpr size_t smem = sizeof(int) * (4 * (kMaxBatch + 1));
   cudaError_t e = set_smem_once<build_decode_schedule_kernel>(smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(build_decode_schedule_kernel, dim3(1), dim3(kThreads), smem, stream, 1, false, ctx_lens, batch,
-                    next_n, max_batch, max_ctx, ctas, caps, sched, status);
+  return launch_pdl(build_decode_schedule_kernel, dim3(1), dim3(kThreads), smem, stream, 1, false, ctx_lens,
+                    key_begin, batch, next_n, max_batch, max_ctx, ctas, caps, sched, status);
 }
 
 }  // namespace idxfp4

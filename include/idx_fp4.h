@@ -203,6 +203,40 @@ int idx_fp4_decode_mtp_logits_topk(const uint8_t *q_packed, const uint8_t *q_sca
                                    float *topk_val, float *logits_debug, int64_t logits_stride, int32_t *status_dev,
                                    cudaStream_t stream);
 
+/* ---- Key-sharded decode (context parallelism) -----------------------------------------------
+ * ("Score a DSA sparse indexer in FP4", section "Decode context parallelism": each rank scores its
+ * own shard of every sequence's keys and keeps its local top-k; the ranks' candidates are gathered
+ * and merged into each row's top-k.) On one GPU the shards are key ranges scored by separate
+ * decode calls; across GPUs each rank runs its own range and the caller gathers the candidate
+ * lists (an all-gather of [rows][topk] indices and values per rank) before the merge.
+ *
+ * idx_fp4_build_decode_schedule_range: a decode schedule (next_n = 1) in which sequence b scores
+ * only the keys [key_begin[b], key_end[b]) (device int32 [batch] each). key_begin[b] must be a
+ * multiple of 128 (the scorer's key tile) with 0 <= key_begin[b] <= key_end[b] <= max_ctx, else
+ * IDX_FP4_DEV_BAD_CTX is set and the row scores no key. Run it with idx_fp4_decode_logits_topk,
+ * passing key_end_dev as ctx_lens_dev: row b then holds the top-min(topk, key_end - key_begin)
+ * keys of its range with absolute token indices (ascending), padded with -1 / -inf. Sizing
+ * functions, workspace and the other arguments are those of the plain decode call. */
+int idx_fp4_build_decode_schedule_range(const int32_t *key_begin_dev, const int32_t *key_end_dev, int batch,
+                                        int max_batch, int64_t max_ctx, void *sched_dev, size_t sched_bytes,
+                                        int32_t *status_dev, cudaStream_t stream);
+
+/* idx_fp4_merge_candidates: the exact top-k of the union of num_lists candidate lists per row.
+ *   cand_val f32 / cand_idx int32 [num_lists][rows][k_in] (device): list l of row r at
+ *     (l * rows + r) * k_in; entries with a negative index are empty. The indices of one row
+ *     are distinct (shards hold disjoint keys).
+ *   topk_idx [rows][topk] (required), topk_val [rows][topk] (nullable), device, caller-owned.
+ * Row r keeps the min(topk, valid entries) best by (value descending, index ascending) and
+ * writes them in ascending index order, padded with -1 / -inf: merging the lists of every key
+ * range of a sequence gives exactly the sequence's decode top-k. One CTA per row.
+ * num_lists * k_in <= IDX_FP4_MERGE_MAX_CANDIDATES (else IDX_FP4_ERR_CAPACITY); 1 <= topk <=
+ * IDX_FP4_MAX_TOPK (else IDX_FP4_ERR_SHAPE); rows == 0 launches nothing. status_dev may be NULL:
+ * this call detects nothing on the device. */
+#define IDX_FP4_MERGE_MAX_CANDIDATES 16384
+int idx_fp4_merge_candidates(const float *cand_val, const int32_t *cand_idx, int num_lists, int rows, int k_in,
+                             int topk, int32_t *topk_idx, float *topk_val, int32_t *status_dev,
+                             cudaStream_t stream);
+
 /* Bytes of the prefill workspace (the call's unit table, and candidate lists for rows longer
  * than one unit's 8192-key (64-head) / 16384-key (128-head) share) for rows of up to max_ctx
  * keys (host; 0 for invalid arguments). */

@@ -64,6 +64,8 @@ def _load():
                 "orc_select_topk": (None, [P, i64, i32, P, P]),
                 "orc_decode_topk": (None, [P, P, P, P, P, P, i64, P, i32, i32, i32, P, i64, P, P, i32]),
                 "orc_prefill_topk": (None, [P, P, P, P, P, P, i64, P, P, i32, i32, i32, i32, P, i64, P, P, i32]),
+                "orc_range_topk": (None, [P, P, P, P, P, P, i64, P, P, i32, i32, i32, P, i64, P, P, i32]),
+                "orc_merge_candidates": (None, [P, P, i32, i32, i32, i32, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -183,6 +185,34 @@ def select_topk(logits, n: int, k: int):
     val = np.zeros(k, np.float64)
     _load().orc_select_topk(_p(lg), int(n), int(k), _p(idx), _p(val))
     return idx, val
+
+
+def range_topk(q_packed, q_scale, w, kv_packed, kv_scale, block_tables, key_begin, key_end, k: int,
+               threads: int = 1):
+    """Top-k of each sequence over its keys [key_begin[b], key_end[b]) with absolute indices:
+    (topk_idx int32 [B][k], topk_val fp64 [B][k]) in (value desc, index asc) order."""
+    q_packed, q_scale = _c(q_packed, np.uint8), _c(q_scale, np.uint8)
+    w = _c(w, np.float32)
+    bt, kb, ke = _c(block_tables, np.int32), _c(key_begin, np.int32), _c(key_end, np.int32)
+    B, H = w.shape
+    width = max(int((ke - kb).max()) if kb.size else 0, 1)
+    scratch = np.zeros((B, width))
+    idx = np.zeros((B, k), np.int32)
+    val = np.zeros((B, k), np.float64)
+    _load().orc_range_topk(_p(q_packed), _p(q_scale), _p(w), _p(kv_packed), _p(kv_scale), _p(bt), bt.shape[1],
+                           _p(kb), _p(ke), B, H, int(k), _p(scratch), width, _p(idx), _p(val), threads)
+    return idx, val
+
+
+def merge_candidates(vals, idx, k: int):
+    """Each row's k best of the union of candidate lists vals/idx [lists][rows][k_in] (index < 0
+    = empty): (topk_idx int32 [rows][k], topk_val fp64 [rows][k]) in (value desc, index asc) order."""
+    vals, idx = _c(vals, np.float64), _c(idx, np.int32)
+    L, R, K = idx.shape
+    out_idx = np.zeros((R, k), np.int32)
+    out_val = np.zeros((R, k), np.float64)
+    _load().orc_merge_candidates(_p(vals), _p(idx), L, R, K, int(k), _p(out_idx), _p(out_val))
+    return out_idx, out_val
 
 
 def decode_topk(q_packed, q_scale, w, kv_packed, kv_scale, block_tables, ctx_lens, k: int, threads: int = 1):

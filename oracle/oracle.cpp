@@ -38,6 +38,13 @@
 //       has row_end = 0 and scores nothing.
 //   R6  Top-k is the set of the min(k, n) best keys by (logit descending, index
 //       ascending); the output is padded with index -1 and value -inf.
+//   (R7-R11 are the quantiser rule stated above, queries quantised alike, the 68-byte key,
+//   the prefill padding variants and the next_n visible-key rule; they need no function here.)
+//   R12 Key-sharded decode ([P2], section "Decode context parallelism": each rank scores its
+//       shard of the keys, keeps its local top-k, and the gathered candidates are merged): a
+//       shard is a contiguous key range [key_begin, key_end) of the sequence; its top-k uses
+//       the absolute token index; the merge keeps the min(k, n) best of the union of the
+//       shards' lists by the R6 order.
 
 #include <algorithm>
 #include <cmath>
@@ -306,6 +313,47 @@ void orc_prefill_logits(const uint8_t* q_packed, const uint8_t* q_scale, const f
 
 void orc_select_topk(const double* logits, int64_t n, int k, int32_t* idx, double* val) {
   select_topk(logits, n, k, idx, val);
+}
+
+// R12: the top-k of each sequence over its key range only (absolute indices). Scratch is the
+// caller's [batch][scratch_stride], scratch_stride >= the longest range.
+void orc_range_topk(const uint8_t* q_packed, const uint8_t* q_scale, const float* w, const uint8_t* kv_packed,
+                    const uint8_t* kv_scale, const int32_t* block_tables, int64_t bt_stride, const int32_t* key_begin,
+                    const int32_t* key_end, int batch, int H, int k, double* scratch, int64_t scratch_stride,
+                    int32_t* topk_idx, double* topk_val, int threads) {
+  parallel_for(batch, threads, [&](int64_t b) {
+    const int64_t t0 = key_begin[b], t1 = key_end[b];
+    const int64_t n = t1 > t0 ? t1 - t0 : 0;
+    row_logits(q_packed, q_scale, w, b, H, kv_packed, kv_scale, block_tables + b * bt_stride, t0, t0 + n,
+               scratch + b * scratch_stride);
+    select_topk(scratch + b * scratch_stride, n, k, topk_idx + b * k, topk_val + b * k);
+    for (int i = 0; i < k; ++i)
+      if (topk_idx[b * k + i] >= 0) topk_idx[b * k + i] += static_cast<int32_t>(t0);
+  });
+}
+
+// R12: the merge of candidate lists [lists][rows][k_in] (index < 0 = empty) into each row's
+// min(k, n) best of the union by (value descending, index ascending), in that order.
+void orc_merge_candidates(const double* vals, const int32_t* idx, int lists, int rows, int k_in, int k,
+                          int32_t* out_idx, double* out_val) {
+  for (int r = 0; r < rows; ++r) {
+    std::vector<std::pair<double, int32_t>> all;
+    for (int l = 0; l < lists; ++l)
+      for (int i = 0; i < k_in; ++i) {
+        const int64_t at = (static_cast<int64_t>(l) * rows + r) * k_in + i;
+        if (idx[at] >= 0) all.emplace_back(vals[at], idx[at]);
+      }
+    std::sort(all.begin(), all.end(), [](const std::pair<double, int32_t>& a, const std::pair<double, int32_t>& b) {
+      if (a.first != b.first) return a.first > b.first;
+      return a.second < b.second;
+    });
+    const int64_t m = std::min<int64_t>(k, static_cast<int64_t>(all.size()));
+    for (int i = 0; i < k; ++i) {
+      out_idx[static_cast<int64_t>(r) * k + i] = i < m ? all[static_cast<size_t>(i)].second : -1;
+      out_val[static_cast<int64_t>(r) * k + i] =
+          i < m ? all[static_cast<size_t>(i)].first : -std::numeric_limits<double>::infinity();
+    }
+  }
 }
 
 // Full decode path: logits then top-k per row. Scratch is the caller's [batch][scratch_stride].

@@ -123,3 +123,19 @@ def test_prefill_rejects_bad_arguments(L):
     assert _prefill(L, R=9000) == ARG  # more rows than one call takes
     assert L.idx_fp4_prefill_workspace_bytes(0, 100, 64, 4096, 2048) == 0
     assert L.idx_fp4_prefill_workspace_bytes(2, 100, 48, 4096, 2048) == 0
+
+
+def test_range_schedule_and_merge_reject_bad_arguments(L):
+    n16 = L.idx_fp4_decode_schedule_bytes(16, 1 << 20)
+    f = L.idx_fp4_build_decode_schedule_range
+    assert f(None, FAKE, 4, 16, 1 << 20, FAKE, n16, None, None) == ARG      # no key_begin
+    assert f(FAKE, FAKE, 17, 16, 1 << 20, FAKE, n16, None, None) == ARG     # batch > max_batch
+    assert f(FAKE, FAKE, 4, 16, 1 << 20, FAKE, n16 - 1, None, None) == CAP  # buffer too small
+    m = L.idx_fp4_merge_candidates
+    assert m(FAKE, FAKE, 0, 4, 64, 64, FAKE, None, None, None) == ARG       # no list
+    assert m(FAKE, FAKE, 2, -1, 64, 64, FAKE, None, None, None) == ARG      # negative rows
+    assert m(FAKE, FAKE, 2, 4, 64, 0, FAKE, None, None, None) == SHAPE      # topk 0
+    assert m(FAKE, FAKE, 2, 4, 64, 4096, FAKE, None, None, None) == SHAPE   # topk past the maximum
+    assert m(FAKE, FAKE, 9, 4, 2048, 2048, FAKE, None, None, None) == CAP   # 18432 candidates per row
+    assert m(FAKE, FAKE, 2, 4, 64, 64, None, None, None, None) == ARG       # no output
+    assert m(None, None, 2, 0, 64, 64, None, None, None, None) == OK        # no rows: nothing launched
