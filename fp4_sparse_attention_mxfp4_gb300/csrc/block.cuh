@@ -44,16 +44,21 @@ __device__ __forceinline__ uint2 blk_scan2(const Blk& B, uint32_t a, uint32_t b,
     B.sc[2 * w + 1] = ib;
   }
   B.sync();
-  uint32_t pa = 0, pb = 0, sa = 0, sb = 0;
-  for (int w2 = 0; w2 < B.nw(); ++w2) {
-    const uint32_t xa = B.sc[2 * w2], xb = B.sc[2 * w2 + 1];
-    if (w2 < w) {
-      pa += xa;
-      pb += xb;
+  // every warp scans the warp totals across its lanes (lane l holds warp l's)
+  uint32_t xa = lane < B.nw() ? B.sc[2 * lane] : 0u, xb = lane < B.nw() ? B.sc[2 * lane + 1] : 0u;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t va = __shfl_up_sync(0xFFFFFFFFu, xa, off);
+    const uint32_t vb = __shfl_up_sync(0xFFFFFFFFu, xb, off);
+    if (lane >= off) {
+      xa += va;
+      xb += vb;
     }
-    sa += xa;
-    sb += xb;
   }
+  const uint32_t sa = __shfl_sync(0xFFFFFFFFu, xa, 31), sb = __shfl_sync(0xFFFFFFFFu, xb, 31);
+  const uint32_t qa = __shfl_sync(0xFFFFFFFFu, xa, w > 0 ? w - 1 : 0);
+  const uint32_t qb = __shfl_sync(0xFFFFFFFFu, xb, w > 0 ? w - 1 : 0);
+  const uint32_t pa = w > 0 ? qa : 0u, pb = w > 0 ? qb : 0u;
   B.sync();
   if (ta != nullptr) *ta = sa;
   if (tb != nullptr) *tb = sb;
@@ -66,10 +71,12 @@ __device__ __forceinline__ uint2 blk_find_bin(const Blk& B, const uint32_t* hist
   const int per = (nb + B.nt - 1) / B.nt;
   const int b0 = min(nb, B.tid * per), b1 = min(nb, b0 + per);
   uint32_t s = 0;
+#pragma unroll 1
   for (int b = b0; b < b1; ++b) s += hist[b];
   uint32_t total = 0;
   const uint32_t pre = blk_scan2(B, s, 0u, &total, nullptr).x;
   uint32_t above = total - pre - s;  // elements in the bins of later threads
+#pragma unroll 1
   for (int b = b1 - 1; b >= b0; --b) {
     const uint32_t c = hist[b];
     if (above < need && need <= above + c) {
@@ -106,6 +113,7 @@ __device__ __forceinline__ uint2 blk_resolve(const Blk& B, KeyAt key, int n, uin
                                              uint32_t* hist, uint32_t* list, int list_cap, bool* consistent) {
   const int2 run = blk_run(B, n);
   uint32_t cnt = 0;
+#pragma unroll 1
   for (int p = run.x; p < run.y; ++p) cnt += (key(p) >> kL1Shift) == bin ? 1u : 0u;
   uint32_t in_bin = 0;
   uint32_t o = blk_scan2(B, cnt, 0u, &in_bin, nullptr).x;
@@ -113,6 +121,7 @@ __device__ __forceinline__ uint2 blk_resolve(const Blk& B, KeyAt key, int n, uin
   if (!*consistent) return make_uint2((bin << kL1Shift) | 0xFFFFFu, 0u);
   const bool listed = in_bin <= static_cast<uint32_t>(list_cap);
   if (listed && cnt != 0u)
+#pragma unroll 1
     for (int p = run.x; p < run.y; ++p) {
       const uint32_t k = key(p);
       if ((k >> kL1Shift) == bin) list[o++] = k;
@@ -131,8 +140,10 @@ __device__ __forceinline__ uint2 blk_resolve(const Blk& B, KeyAt key, int n, uin
       else if ((l >> 10) == (low >> 10)) smem_red_add(&hist[l & 1023u], 1u);
     };
     if (listed) {
+#pragma unroll 1
       for (int i = B.tid; i < static_cast<int>(in_bin); i += B.nt) count(list[i]);
     } else {
+#pragma unroll 1
       for (int p = B.tid; p < n; p += B.nt) count(key(p));
     }
     B.sync();

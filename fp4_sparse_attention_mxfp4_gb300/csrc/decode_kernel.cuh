@@ -618,6 +618,7 @@ __device__ __forceinline__ void blk_emit(const Blk& B, KeyAt key, TokAt tok, int
   if (all) {
     gt = static_cast<uint32_t>(run.y - run.x);
   } else {
+#pragma unroll 1
     for (int x = run.x; x < run.y; ++x) {
       const uint32_t k = key(x);
       gt += k > T ? 1u : 0u;
@@ -627,6 +628,7 @@ __device__ __forceinline__ void blk_emit(const Blk& B, KeyAt key, TokAt tok, int
   const uint2 pre = blk_scan2(B, gt, eq, nullptr, nullptr);
   uint32_t pos = pre.x + min(pre.y, need), eqr = pre.y;
   if (gt + eq != 0u)
+#pragma unroll 1
     for (int x = run.x; x < run.y; ++x) {
       const uint32_t k = key(x);
       const bool eqk = !all && k == T;
@@ -647,6 +649,7 @@ __device__ __forceinline__ void blk_select(const Blk& B, KeyAt key, TokAt tok, i
   }
   blk_zero(B, hist, kL1Bins);
   B.sync();
+#pragma unroll 1
   for (int x = B.tid; x < n; x += B.nt) smem_red_add(&hist[key(x) >> kL1Shift], 1u);
   B.sync();
   const uint2 r = blk_find_bin(B, hist, kL1Bins, static_cast<uint32_t>(kk));
