@@ -144,9 +144,12 @@ struct DecodeCfg {
   static constexpr int CCAP = (P_SOFF - P_CAND) / 128 * 128;
   static_assert(P_EQPRE + Q * (kDecodeMaxCtas + 4) <= P_SOFF && CCAP >= 4096, "selection areas fit");
   static_assert(P_HIST % 4 == 0 && P_LVL % 4 == 0, "16-byte aligned histograms");
-  // When the whole CTA selects one unit, the second group's half holds, per row, the row-buffer
-  // positions (16 bits) of the keys that can still be selected.
-  static constexpr int P_CIDX = P_WORDS;
+  // Row-buffer positions (16 bits) of the keys that can still be selected, per row: in the words
+  // between the exchange's areas and the merge offsets, or, when the whole CTA selects one unit, in
+  // the second group's half.
+  static constexpr int P_CIDX = P_EQPRE + Q * (kDecodeMaxCtas + 4);
+  static constexpr int CIDX_GROUP = (P_SOFF - P_CIDX) * 2 / Q / 8 * 8;  // positions per row, own area
+  static constexpr int CIDX_WHOLE = CAP;                                 // positions per row, second half
   static_assert(CAP <= 65536 && Q * CAP / 2 <= P_WORDS, "candidate positions fit the second half");
 };
 
@@ -269,7 +272,7 @@ struct KernelShared {
   int pending[2];                // sequence merges deferred to the end of a group's selection
   int pending_seq[2][kMaxNextN];
   RangeMeta meta[2];             // the round's first and last units (written during the stream)
-  uint32_t ncand[kMaxNextN];     // per row: candidate positions listed (whole-CTA selection)
+  int ncand[2][kMaxNextN];       // per group and row: candidate positions listed (-1: every key)
 };
 static_assert(sizeof(KernelShared) <= 512, "fits its slot");
 
@@ -821,9 +824,11 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   uint32_t* cnt = ks->counter[g];
   const uint32_t* lg = reinterpret_cast<const uint32_t*>(smem + C::OFF_LG);
   const int topk = p.topk;
-  // the whole CTA selects the range's one unit: candidate positions are listed in the second half
-  const bool compact = B.nt == C::THREADS;
-  uint16_t* cidx = reinterpret_cast<uint16_t*>(reinterpret_cast<uint32_t*>(smem) + C::P_CIDX);
+  // candidate positions: the second half when the whole CTA selects the range's one unit, else the
+  // group's own spare words
+  const bool whole = B.nt == C::THREADS;
+  const int ccap = whole ? C::CIDX_WHOLE : C::CIDX_GROUP;
+  uint16_t* cidx = reinterpret_cast<uint16_t*>(whole ? reinterpret_cast<uint32_t*>(smem) + C::P_WORDS : P + C::P_CIDX);
   const int lane = B.lane(), warp = B.warp();
   const int ex = g == 0 ? uf : (ul - 1 > uf ? ul - 1 : -1);  // this group's range-end unit
   auto seg_ctx_of = [&](const DecodeUnit& u, const DecodeSeg& sg, int ctx, int q) {
@@ -962,11 +967,11 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
           }
         if (B.tid == 0) rec[0] = nrec;
         blk_publish(B, sync_word(s, 0));
-        if (compact) {
+        {
           // While the other units publish: list the positions of this unit's keys at or above its
           // own k-th key's bin, in token order. The segment's threshold is at or above that bin,
-          // so the later passes need only these.
-          uint16_t* ci = cidx + q * C::CAP;
+          // so the later passes need only these (all keys when the list would not fit).
+          uint16_t* ci = cidx + q * ccap;
           const int2 kr = blk_run4(B, un);
           uint32_t c = 0;
 #pragma unroll 4
@@ -977,14 +982,15 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
           }
           uint32_t listed = 0;
           uint32_t at = blk_scan2(B, c, 0u, &listed, nullptr).x;
-          if (c != 0u)
+          const bool fits = listed <= static_cast<uint32_t>(ccap);
+          if (fits && c != 0u)
             for (int x = kr.x; x < kr.y; x += 4) {
               const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
 #pragma unroll
               for (int e = 0; e < 4; ++e)
                 if (x + e < kr.y && (vec_lane(vv, e) >> kL1Shift) >= bu) ci[at++] = static_cast<uint16_t>(x + e);
             }
-          if (B.tid == 0) ks->ncand[q] = listed;
+          if (B.tid == 0) ks->ncand[g][q] = fits ? static_cast<int>(listed) : -1;
         }
       }
     }
@@ -1100,41 +1106,24 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     const uint32_t* keys = lg + q * C::CAP + u.buf;
     uint32_t* dst = list_of(s.sg, u.uidx, q);
     const uint32_t my_eq = eqpre[me + 1] - eqpre[me];
+    // over the listed candidate positions, or every key when the list did not fit
+    const int nc = ks->ncand[g][q];
+    const uint16_t* ci = cidx + q * ccap;
+    auto pos = [&](int f) { return nc >= 0 ? static_cast<int>(ci[f]) : f; };
     uint32_t listed = 0;
-    if (compact) {
-      const uint16_t* ci = cidx + q * C::CAP;
-      const int2 kr = blk_run(B, static_cast<int>(ks->ncand[q]));
+    {
+      const int2 kr = blk_run(B, nc >= 0 ? nc : un);
       uint32_t c = 0;
-      for (int f = kr.x; f < kr.y; ++f) c += (keys[ci[f]] >> kL1Shift) == bstar ? 1u : 0u;
+#pragma unroll 4
+      for (int f = kr.x; f < kr.y; ++f) c += (keys[pos(f)] >> kL1Shift) == bstar ? 1u : 0u;
       uint32_t at = blk_scan2(B, c, 0u, &listed, nullptr).x;
       if (c != 0u)
+#pragma unroll 1
         for (int f = kr.x; f < kr.y; ++f) {
-          const uint32_t k = keys[ci[f]];
+          const uint32_t k = keys[pos(f)];
           if ((k >> kL1Shift) == bstar) {
             if (at < my_eq) dst[at] = k & 0xFFFFFu;
             ++at;
-          }
-        }
-    } else {
-      const int2 kr = blk_run4(B, un);
-      uint32_t c = 0;
-#pragma unroll 4
-      for (int x = kr.x; x < kr.y; x += 4) {
-        const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) c += (x + e < kr.y && (vec_lane(vv, e) >> kL1Shift) == bstar) ? 1u : 0u;
-      }
-      uint32_t at = blk_scan2(B, c, 0u, &listed, nullptr).x;
-      if (c != 0u)
-        for (int x = kr.x; x < kr.y; x += 4) {
-          const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t k = vec_lane(vv, e);
-            if (x + e < kr.y && (k >> kL1Shift) == bstar) {
-              if (at < my_eq) dst[at] = k & 0xFFFFFu;
-              ++at;
-            }
           }
         }
     }
@@ -1249,51 +1238,29 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
     const uint32_t* keys = lg + q * C::CAP + u.buf;
     const RowOut out = seg_out(p, ws, s, nseg, Q);
-    if (compact) {
-      const uint16_t* ci = cidx + q * C::CAP;
-      const int2 run = blk_run(B, static_cast<int>(ks->ncand[q]));
+    {
+      // over the listed candidate positions, or every key when the list did not fit
+      const int nc = ks->ncand[g][q];
+      const uint16_t* ci = cidx + q * ccap;
+      auto pos_of = [&](int f) { return nc >= 0 ? static_cast<int>(ci[f]) : f; };
+      const int2 run = blk_run(B, nc >= 0 ? nc : un);
       uint32_t gt = 0, eq = 0;
+#pragma unroll 4
       for (int f = run.x; f < run.y; ++f) {
-        const uint32_t k = keys[ci[f]];
+        const uint32_t k = keys[pos_of(f)];
         gt += k > T ? 1u : 0u;
         eq += k == T ? 1u : 0u;
       }
       const uint2 pre = blk_scan2(B, gt, eq, nullptr, nullptr);
       uint32_t pos = off + pre.x + min(pre.y, take), eqr = pre.y;
       if (gt + eq != 0u)
+#pragma unroll 1
         for (int f = run.x; f < run.y; ++f) {
-          const int x = ci[f];
+          const int x = pos_of(f);
           const uint32_t k = keys[x];
           const bool eqk = k == T;
           if (k > T || (eqk && eqr < take)) out(pos++, k, u.kb + x);
           eqr += eqk ? 1u : 0u;
-        }
-    } else {
-      const int2 run = blk_run4(B, un);
-      uint32_t gt = 0, eq = 0;
-#pragma unroll 4
-      for (int x = run.x; x < run.y; x += 4) {
-        const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t k = vec_lane(vv, e);
-          gt += (x + e < run.y && k > T) ? 1u : 0u;
-          eq += (x + e < run.y && k == T) ? 1u : 0u;
-        }
-      }
-      const uint2 pre = blk_scan2(B, gt, eq, nullptr, nullptr);
-      uint32_t pos = off + pre.x + min(pre.y, take), eqr = pre.y;
-      if (gt + eq != 0u)
-        for (int x = run.x; x < run.y; x += 4) {
-          const uint4 vv = *reinterpret_cast<const uint4*>(keys + x);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t k = vec_lane(vv, e);
-            const bool in = x + e < run.y;
-            const bool eqk = in && k == T;
-            if ((in && k > T) || (eqk && eqr < take)) out(pos++, k, u.kb + x + e);
-            eqr += eqk ? 1u : 0u;
-          }
         }
     }
     if (nseg > 1) {
