@@ -135,10 +135,7 @@ struct DecodeCfg {
   static constexpr int P_LIST = P_HIST + kL1Bins + 64;  // [LIST_CAP] keys of the threshold bin
   static constexpr int LIST_CAP = 2048;
   static constexpr int P_LVL = P_LIST + LIST_CAP;     // [1024 + 32] lower radix levels, fine and coarse
-  static constexpr int P_UOFF = P_LVL + 1056;         // [kDecodeMaxCtas + 1] per-unit record offsets
-  static constexpr int P_REC = P_UOFF + kDecodeMaxCtas + 4;  // [RCAP] staged (record, unit) pairs
-  static constexpr int RCAP = 1024;
-  static constexpr int P_EQPRE = P_REC + 2 * RCAP;    // [Q][kDecodeMaxCtas + 4] prefix of the units' bin keys
+  static constexpr int P_EQPRE = P_LVL + 1056;       // [Q][kDecodeMaxCtas + 4] prefix of the units' bin keys
   static constexpr int P_SOFF = P_WORDS - 1040;       // [1024 + 1] segment offsets of a sequence merge
   static constexpr int P_CAND = P_LVL;                // a sequence merge's staged candidate keys
   static constexpr int CCAP = (P_SOFF - P_CAND) / 128 * 128;
@@ -1019,51 +1016,37 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     if (s.sg.nunits == 1 || !exchanged(s)) continue;
     const int nu = min(s.sg.nunits, kDecodeMaxCtas);
     if (!blk_wait_count(B, sync_word(s, 0), static_cast<uint32_t>(s.sg.nunits), abort_flag, p.status)) continue;
-    // record counts -> offsets. A count is at most the unit's keys and the number of bins: anything
-    // else could only come from a workspace that was not zero-filled, and is clamped so that every
-    // read stays inside the unit's own area.
-    uint32_t* uoff = P + C::P_UOFF;
-    const int cper = (nu + B.nt - 1) / B.nt;
-    const int c0 = min(nu, B.tid * cper), c1 = min(nu, c0 + cper);
-    uint32_t mine = 0;
-    for (int j = c0; j < c1; ++j) {
-      const uint32_t cap = static_cast<uint32_t>(min(kL1Bins, unit_tiles(s.sg, j) * kTileKeys));
-      const uint32_t c = min(ldcg_u32(rec_of(s.sg, j, q)), cap);
-      uoff[j] = c;
-      mine += c;
-    }
-    uint32_t R = 0;
-    uint32_t run = blk_scan2(B, mine, 0u, &R, nullptr).x;
-    for (int j = c0; j < c1; ++j) {
-      const uint32_t c = uoff[j];
-      uoff[j] = run;
-      run += c;
-    }
-    if (B.tid == 0) uoff[nu] = R;
+    // Every unit's records: warp w reads units w, w + warps, ... (the count, then the records, 32
+    // words per coalesced load) into the histogram, and keeps its first unit's first words for the
+    // second pass. A count is at most the unit's keys and the number of bins: anything else could
+    // only come from a workspace that was not zero-filled, and is clamped so that every read stays
+    // inside the unit's own area.
+    const int nw = B.nw();
     blk_zero(B, hist, kL1Bins + 64);
     B.sync();
-    auto unit_of = [&](int f) {
-      int lo = 0, hi = nu - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<int>(uoff[mid]) <= f) lo = mid; else hi = mid - 1;
+    auto rec_count = [&](int j, uint32_t w0) {
+      const uint32_t cap = static_cast<uint32_t>(min(kL1Bins, unit_tiles(s.sg, j) * kTileKeys));
+      return min(__shfl_sync(0xFFFFFFFFu, w0, 0), cap);
+    };
+    uint32_t first_w = 0, first_n = 0;
+#pragma unroll 1
+    for (int j = warp; j < nu; j += nw) {
+      const uint32_t* rb = rec_of(s.sg, j, q);
+      const uint32_t w0 = ldcg_u32(rb + lane);
+      const uint32_t n = rec_count(j, w0);
+      if (j == warp) {
+        first_w = w0;
+        first_n = n;
       }
-      return lo;
-    };
-    uint2* recs = reinterpret_cast<uint2*>(P + C::P_REC);
-    const bool staged = static_cast<int>(R) <= C::RCAP;
-    auto record = [&](int f) {
-      if (staged) return recs[f];
-      const int j = unit_of(f);
-      return make_uint2(ldcg_u32(rec_of(s.sg, j, q) + 1 + (f - static_cast<int>(uoff[j]))), static_cast<uint32_t>(j));
-    };
-    for (int f = B.tid; f < static_cast<int>(R); f += B.nt) {
-      const int j = unit_of(f);
-      const uint32_t r = ldcg_u32(rec_of(s.sg, j, q) + 1 + (f - static_cast<int>(uoff[j])));
-      if (staged) recs[f] = make_uint2(r, static_cast<uint32_t>(j));
-      const uint32_t b = (r >> 17) & (kL1Bins - 1), c = r & 0x1FFFFu;
-      smem_red_add(&hist[b], c);
-      smem_red_add(&hist[kL1Bins + (b >> 6)], c);
+#pragma unroll 1
+      for (uint32_t i = lane; i <= n; i += 32) {
+        const uint32_t r = i < 32 ? w0 : ldcg_u32(rb + i);
+        if (i >= 1) {
+          const uint32_t b = (r >> 17) & (kL1Bins - 1), c = r & 0x1FFFFu;
+          smem_red_add(&hist[b], c);
+          smem_red_add(&hist[kL1Bins + (b >> 6)], c);
+        }
+      }
     }
     B.sync();
     if (warp == 0) {
@@ -1073,32 +1056,55 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
         ts.need = static_cast<uint32_t>(s.kk) - tb.y;
       }
     }
-    // per unit: keys above the bin (before this unit) and inside it (their prefix over units)
     uint32_t* eqpre = P + C::P_EQPRE + q * (kDecodeMaxCtas + 4);
-    blk_zero(B, eqpre, nu + 1);
     if (B.tid == 0) cnt[2] = 0u;
     B.sync();
+    // per unit: its keys inside the bin, and the keys above the bin in the units before this one
     const uint32_t bstar = ts.bin;
     const int me = u.uidx;
-    uint32_t gt_before = 0;
-    for (int f = B.tid; f < static_cast<int>(R); f += B.nt) {
-      const uint2 r = record(f);
-      const uint32_t b = (r.x >> 17) & (kL1Bins - 1), c = r.x & 0x1FFFFu;
-      if (b == bstar) eqpre[r.y + 1] = c;
-      if (b > bstar && static_cast<int>(r.y) < me) gt_before += c;
+#pragma unroll 1
+    for (int j = warp; j < nu; j += nw) {
+      const uint32_t* rb = rec_of(s.sg, j, q);
+      const uint32_t w0 = j == warp ? first_w : ldcg_u32(rb + lane);
+      const uint32_t n = j == warp ? first_n : rec_count(j, w0);
+      uint32_t eq = 0, gt = 0;
+#pragma unroll 1
+      for (uint32_t i = lane; i <= n; i += 32) {
+        const uint32_t r = i < 32 ? w0 : ldcg_u32(rb + i);
+        if (i >= 1) {
+          const uint32_t b = (r >> 17) & (kL1Bins - 1), c = r & 0x1FFFFu;
+          eq += b == bstar ? c : 0u;
+          gt += b > bstar ? c : 0u;
+        }
+      }
+      eq = __reduce_add_sync(0xFFFFFFFFu, eq);
+      gt = __reduce_add_sync(0xFFFFFFFFu, gt);
+      if (lane == 0) {
+        eqpre[j + 1] = eq;
+        if (j < me && gt != 0u) atomicAdd(&cnt[2], gt);
+      }
     }
-    if (gt_before != 0u) atomicAdd(&cnt[2], gt_before);
     B.sync();
-    mine = 0;
-    for (int j = c0; j < c1; ++j) mine += eqpre[j + 1];
-    run = blk_scan2(B, mine, 0u, nullptr, nullptr).x;
-    for (int j = c0; j < c1; ++j) {
-      run += eqpre[j + 1];
-      eqpre[j + 1] = run;
-    }
-    if (B.tid == 0) {
-      ts.gt_before = cnt[2];
-      ts.ok = 1u;
+    // prefix of the units' bin keys over the units, by one warp
+    if (warp == 0) {
+      uint32_t run = 0;
+#pragma unroll 1
+      for (int base = 0; base < nu; base += 32) {
+        const int j = base + lane;
+        uint32_t incl = j < nu ? eqpre[j + 1] : 0u;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          if (lane >= off) incl += t;
+        }
+        if (j < nu) eqpre[j + 1] = run + incl;
+        run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      if (lane == 0) {
+        eqpre[0] = 0u;
+        ts.gt_before = cnt[2];
+        ts.ok = 1u;
+      }
     }
     B.sync();
     // this unit's keys inside the threshold bin, low 20 bits, in token order
