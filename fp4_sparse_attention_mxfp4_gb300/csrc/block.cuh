@@ -10,6 +10,7 @@
 // known beforehand.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -235,40 +236,38 @@ __device__ __forceinline__ uint32_t vec_lane(const uint4& v, int e) {
 template <int CB, int FPER>
 __device__ __forceinline__ uint2 warp_find_bin2(const uint32_t* fine, const uint32_t* coarse, uint32_t need, int lane) {
   static_assert((CB == 32 || CB == 64) && (FPER == 32 || FPER == 64), "one or two bins per lane");
-  constexpr int CPL = CB / 32, FPL = FPER / 32;
-  auto search = [&](const uint32_t* h, int per, uint32_t above0, uint32_t& at_above) {
-    uint32_t c[2] = {0u, 0u}, s = 0;
-    for (int k = 0; k < per; ++k) {
-      c[k] = h[lane * per + k];
-      s += c[k];
+  // One level: lane l holds bins PER*l .. PER*l + PER - 1 of h; returns the bin holding the need-th
+  // largest element and the elements above it (above0: elements above h's first bin... last bin).
+  auto search = [&](const uint32_t* h, auto per_c, uint32_t above0, uint32_t& at_above) {
+    constexpr int PER = decltype(per_c)::value;
+    uint32_t c0, c1 = 0u;
+    if constexpr (PER == 2) {
+      const uint2 v = reinterpret_cast<const uint2*>(h)[lane];
+      c0 = v.x;
+      c1 = v.y;
+    } else {
+      c0 = h[lane];
     }
-    uint32_t suf = s;
+    const uint32_t s = c0 + c1;
+    uint32_t suf = s;  // elements in this lane's bins and above
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suf, off);
       if (lane + off < 32) suf += t;
     }
-    const uint32_t a = above0 + suf - s;
+    const uint32_t a = above0 + suf - s;  // elements above this lane's bins
     const unsigned m = __ballot_sync(0xFFFFFFFFu, a < need && need <= a + s);
     const int L = m != 0u ? 31 - __clz(m) : 0;
-    int bin = 0;
-    uint32_t ab = 0;
-    if (lane == L) {
-      uint32_t x = a;
-      for (int k = per - 1; k >= 0; --k) {
-        if (x < need && need <= x + c[k]) {
-          bin = lane * per + k;
-          ab = x;
-        }
-        x += c[k];
-      }
-    }
+    // inside lane L: the upper bin first
+    const bool hi = PER == 2 && a < need && need <= a + c1;
+    const int bin = lane * PER + (PER == 2 && !hi ? 0 : PER - 1);
+    const uint32_t ab = PER == 2 && !hi ? a + c1 : a;
     at_above = __shfl_sync(0xFFFFFFFFu, ab, L);
     return __shfl_sync(0xFFFFFFFFu, bin, L);
   };
   uint32_t a1 = 0, a2 = 0;
-  const int cb = search(coarse, CPL, 0u, a1);
-  const int fb = search(fine + cb * FPER, FPL, a1, a2);
+  const int cb = search(coarse, std::integral_constant<int, CB / 32>{}, 0u, a1);
+  const int fb = search(fine + cb * FPER, std::integral_constant<int, FPER / 32>{}, a1, a2);
   return make_uint2(static_cast<uint32_t>(cb * FPER + fb), a2);
 }
 

@@ -1165,6 +1165,8 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     };
     uint32_t* list = P + C::P_LIST;
     const bool staged = L <= C::LIST_CAP;
+    blk_zero(B, hist, kL1Bins + 64);  // the levels' histograms (ordered by the barrier below)
+    if (!staged) B.sync();
     if (staged) {
       // warp w copies the lists of units w, w + warps, ... (coalesced, loads issued ahead)
       for (int j = warp; j < nu; j += B.nw()) {
@@ -1187,54 +1189,75 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
       B.sync();
     }
     auto low = [&](int x) { return staged ? list[x] : (ldcg_u32(src(x)) & 0xFFFFFu); };
-    // two radix levels (10 + 10 bits) inside the bin, each a 1024-bin histogram with 32 coarse bins
-    uint32_t need = ts.need, tlow = 0u;
-#pragma unroll 1
-    for (int level = 0; level < 2; ++level) {
-      blk_zero(B, lvl, 1024 + 32);
-      B.sync();
-      for (int x = B.tid; x < L; x += B.nt) {
-        const uint32_t l = low(x);
-        const uint32_t d = level == 0 ? (l >> 10) : (l & 1023u);
-        if (level == 0 || (l >> 10) == (tlow >> 10)) {
-          smem_red_add(&lvl[d], 1u);
-          smem_red_add(&lvl[1024 + (d >> 5)], 1u);
-        }
-      }
-      B.sync();
-      if (warp == 0) {
-        const uint2 r = warp_find_bin2<32, 32>(lvl, lvl + 1024, need, lane);
-        if (lane == 0) {
-          cnt[1] = r.x;
-          cnt[2] = r.y;
-        }
-      }
-      B.sync();
-      tlow |= cnt[1] << (level == 0 ? 10 : 0);
-      need -= cnt[2];
-      B.sync();
+    // Two radix levels (10 + 10 bits) inside the bin. The second level's pass also counts, for the
+    // offset of this unit's output, the earlier units' keys above the first level's digit, and
+    // histograms the low digits of the earlier units' and this unit's keys at that digit; the four
+    // histograms sit in the record histogram's words (zeroed before the lists were staged).
+    uint32_t* lv0 = hist;             // [1024 + 32] first digit, fine and coarse
+    uint32_t* lv1 = hist + 1056;      // [1024 + 32] second digit of the keys at the first
+    uint32_t* h1e = hist + 2112;      // [1024] second digit, earlier units, at the first
+    uint32_t* h1m = hist + 3136;      // [1024] second digit, this unit, at the first
+    uint32_t* r2 = B.sc + 80;         // the levels' results, shared with the block
+    const int e0 = static_cast<int>(eqpre[me]), e1 = static_cast<int>(eqpre[me + 1]);
+#pragma unroll 4
+    for (int x = B.tid; x < L; x += B.nt) {
+      const uint32_t d = low(x) >> 10;
+      smem_red_add(&lv0[d], 1u);
+      smem_red_add(&lv0[1024 + (d >> 5)], 1u);
     }
-    // keys of the bin above T and equal to T in the segment's earlier units, and equal in this one
-    if (B.tid == 0) {
-      cnt[0] = 0u;
-      cnt[1] = 0u;
-      cnt[3] = 0u;
+    if (B.tid == 0) r2[4] = 0u;
+    B.sync();
+    if (warp == 0) {
+      const uint2 r = warp_find_bin2<32, 32>(lv0, lv0 + 1024, ts.need, lane);
+      if (lane == 0) {
+        r2[0] = r.x;
+        r2[1] = r.y;
+      }
     }
     B.sync();
-    uint32_t a_gt = 0, a_eq = 0, m_eq = 0;
-    const int e0 = static_cast<int>(eqpre[me]), e1 = static_cast<int>(eqpre[me + 1]);
-    for (int x = B.tid; x < e1; x += B.nt) {
+    const uint32_t t0 = r2[0];
+    uint32_t need = ts.need - r2[1];
+    uint32_t a_gt0 = 0;  // earlier units' keys above the first digit
+#pragma unroll 4
+    for (int x = B.tid; x < L; x += B.nt) {
       const uint32_t l = low(x);
-      if (x < e0) {
-        a_gt += l > tlow ? 1u : 0u;
-        a_eq += l == tlow ? 1u : 0u;
-      } else {
-        m_eq += l == tlow ? 1u : 0u;
+      const uint32_t d0 = l >> 10, d1 = l & 1023u;
+      if (d0 == t0) {
+        smem_red_add(&lv1[d1], 1u);
+        smem_red_add(&lv1[1024 + (d1 >> 5)], 1u);
+        if (x < e0) smem_red_add(&h1e[d1], 1u);
+        else if (x < e1) smem_red_add(&h1m[d1], 1u);
+      }
+      a_gt0 += x < e0 && d0 > t0 ? 1u : 0u;
+    }
+    a_gt0 = __reduce_add_sync(0xFFFFFFFFu, a_gt0);
+    if (lane == 0 && a_gt0 != 0u) atomicAdd(&r2[4], a_gt0);
+    B.sync();
+    if (warp == 0) {
+      const uint2 r = warp_find_bin2<32, 32>(lv1, lv1 + 1024, need, lane);
+      uint32_t above = 0;  // earlier units' keys at the first digit, above the second
+#pragma unroll 8
+      for (int k = 0; k < 32; ++k) {
+        const uint32_t b = static_cast<uint32_t>(lane * 32 + k);
+        above += b > r.x ? h1e[b] : 0u;
+      }
+      above = __reduce_add_sync(0xFFFFFFFFu, above);
+      if (lane == 0) {
+        r2[0] = (t0 << 10) | r.x;  // low 20 bits of T
+        r2[1] = r.y;               // keys of the first digit above T
+        r2[2] = r2[4] + above;     // earlier units' keys above T (inside the bin)
+        r2[3] = h1e[r.x];          // earlier units' keys equal to T
+        r2[5] = h1m[r.x];          // this unit's keys equal to T
       }
     }
-    if (a_gt != 0u) atomicAdd(&cnt[0], a_gt);
-    if (a_eq != 0u) atomicAdd(&cnt[1], a_eq);
-    if (m_eq != 0u) atomicAdd(&cnt[3], m_eq);
+    B.sync();
+    const uint32_t tlow = r2[0];
+    need -= r2[1];
+    if (B.tid == 0) {
+      cnt[0] = r2[2];
+      cnt[1] = r2[3];
+      cnt[3] = r2[5];
+    }
     B.sync();
     const uint32_t T = (ts.bin << kL1Shift) | tlow;
     const uint32_t eq_before = cnt[1];
