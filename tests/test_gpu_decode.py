@@ -248,24 +248,28 @@ def parse_decode_schedule(buf, max_batch):
     return h, range_first, seq_ctx, seq_seg0, seq_nseg, units, segs
 
 
-def test_decode_schedule_invariants():
+@pytest.mark.parametrize("nseq", [8, 40])
+def test_decode_schedule_invariants(nseq):
     """Units of every sequence partition [0, ctx) exactly in token order; each CTA range holds at
     most one row buffer of tiles; segments group a sequence's units per round with consecutive unit
     indices; sequences without keys have no segment."""
-    ctx = np.array([131072, 5, 0, 70000, 128, 129, 1, 262144], np.int32)
-    sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(16, 262144), dtype=torch.uint8, device="cuda")
-    fx.idx_fp4_build_decode_schedule(dev(ctx), 16, 262144, sched)
+    base = np.array([131072, 5, 0, 70000, 128, 129, 1, 262144], np.int32)
+    extra = synth.Rng(77).integers(0, 9000, max(nseq - len(base), 0)).astype(np.int32)
+    ctx = np.concatenate([base, extra])[:nseq]
+    max_batch = 16 if nseq <= 16 else 64
+    sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(max_batch, 262144), dtype=torch.uint8, device="cuda")
+    fx.idx_fp4_build_decode_schedule(dev(ctx), max_batch, 262144, sched)
     torch.cuda.synchronize()
-    h, range_first, seq_ctx, seq_seg0, seq_nseg, units, segs = parse_decode_schedule(sched, 16)
-    assert h["magic"] == 0x44534333 and h["ok"] == 1 and h["batch"] == 8 and h["max_batch"] == 16
+    h, range_first, seq_ctx, seq_seg0, seq_nseg, units, segs = parse_decode_schedule(sched, max_batch)
+    assert h["magic"] == 0x44534333 and h["ok"] == 1 and h["batch"] == nseq and h["max_batch"] == max_batch
     assert h["ctas"] == torch.cuda.get_device_properties(0).multi_processor_count
     tiles = [-(-int(c) // 128) for c in ctx]
     assert h["total_tiles"] == sum(tiles)
-    assert np.array_equal(seq_ctx[:8], ctx)
+    assert np.array_equal(seq_ctx[:nseq], ctx)
     per, ctas, rounds = h["per"], h["ctas"], h["rounds"]
     assert 1 <= per <= 128 and rounds * ctas * per >= h["total_tiles"]
     starts = np.concatenate([[0], np.cumsum(tiles)])
-    covered = {b: [] for b in range(8)}
+    covered = {b: [] for b in range(nseq)}
     for i in range(rounds * ctas):
         lo = i * per
         for ui in range(range_first[i], range_first[i + 1]):
@@ -276,7 +280,7 @@ def test_decode_schedule_invariants():
             assert buf == (tile0 - lo) * 128 and buf + (ke - kb) <= per * 128
     assert range_first[rounds * ctas] == h["num_units"]
     nsegs = 0
-    for b in range(8):
+    for b in range(nseq):
         r = sorted(covered[b])
         if ctx[b] == 0:
             assert r == [] and seq_nseg[b] == 0
@@ -311,3 +315,13 @@ def test_decode_several_rounds():
     boundary = min(h["ctas"] * h["per"] // 1024, nseq - 1)  # the sequence holding the first round's end
     ref = _oracle_side(case)
     _check_decode(run, ref, rows=[0, boundary, nseq - 1], full_logits=True)
+
+
+def test_decode_forty_ragged_sequences():
+    """40 short sequences of ragged lengths (one empty): every row against the oracle."""
+    ctx = synth.Rng(78).integers(1, 6000, 40).astype(np.int32)
+    ctx[3] = 0
+    case = synth.decode_case("batch40", 79, ctx, 32, 256)
+    run = DecodeRun(case).run()
+    ref = _oracle_side(case)
+    _check_decode(run, ref)
