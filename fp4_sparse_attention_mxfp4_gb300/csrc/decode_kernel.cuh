@@ -808,7 +808,7 @@ __device__ __forceinline__ RowOut seg_out(const DecodeParams& p, const DecodeWs&
 // A unit's waits only follow other units' publications, and the two groups run their first and
 // last units' exchanges side by side, so no CTA's publication waits behind another exchange.
 template <int H, int Q>
-__device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int g, const Blk& B) {
+__device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int g, const Blk& B, bool row_split) {
   using C = DecodeCfg<H, Q>;
   KernelShared* ks = reinterpret_cast<KernelShared*>(smem + C::OFF_KS);
   volatile int* abort_flag = &ks->abort;
@@ -827,7 +827,10 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   const int ccap = whole ? C::CIDX_WHOLE : C::CIDX_GROUP;
   uint16_t* cidx = reinterpret_cast<uint16_t*>(whole ? reinterpret_cast<uint32_t*>(smem) + C::P_WORDS : P + C::P_CIDX);
   const int lane = B.lane(), warp = B.warp();
-  const int ex = g == 0 ? uf : (ul - 1 > uf ? ul - 1 : -1);  // this group's range-end unit
+  // this group's range-end unit, and its rows: all rows, or (row_split: both groups on the range's
+  // one unit) every other row from the group's index
+  const int ex = g == 0 || row_split ? uf : (ul - 1 > uf ? ul - 1 : -1);
+  const int q0 = row_split ? g : 0, qstep = row_split ? 2 : 1;
   auto seg_ctx_of = [&](const DecodeUnit& u, const DecodeSeg& sg, int ctx, int q) {
     SegCtx s;
     s.sg = sg;
@@ -916,7 +919,7 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   if (ex >= 0) {
     const DecodeUnit& u = ue;
     const int nseg = nseg_e;
-    for (int q = 0; q < Q; ++q) {
+    for (int q = q0; q < Q; q += qstep) {
       const SegCtx s = seg_ctx_of(u, se, ctx_e, q);
       const int un = clampi(s.row_end - u.kb, 0, u.ke - u.kb);
       const uint32_t* keys = lg + q * C::CAP + u.buf;
@@ -999,7 +1002,7 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   const int nmid = mfirst < ul - 1 ? (ul - 1 - mfirst + 1) / 2 : 0;
   for (int k = 0; k < nmid + (ex_whole ? 1 : 0); ++k) {
     const int i = ex_whole ? (k == 0 ? ex : mfirst + 2 * (k - 1)) : mfirst + 2 * k;
-    for (int q = 0; q < Q; ++q) select_local(i, q);
+    for (int q = q0; q < Q; q += qstep) select_local(i, q);
   }
   if (ex < 0) {
     B.sync();
@@ -1009,7 +1012,7 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   // ---- B1: the threshold bin from every unit's bins; this unit's keys inside it --------------
   const DecodeUnit& u = ue;
   const int nseg = nseg_e;
-  for (int q = 0; q < Q; ++q) {
+  for (int q = q0; q < Q; q += qstep) {
     const SegCtx s = seg_ctx_of(u, se, ctx_e, q);
     TaskState& ts = ks->task[g][q];
     if (B.tid == 0) ts.ok = 0u;
@@ -1139,7 +1142,7 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   B.sync();  // every row's task state is settled
 
   // ---- B2: the exact threshold from every unit's bin keys; this unit's selected keys ---------
-  for (int q = 0; q < Q; ++q) {
+  for (int q = q0; q < Q; q += qstep) {
     const SegCtx s = seg_ctx_of(u, se, ctx_e, q);
     const TaskState& ts = ks->task[g][q];
     if (ts.ok == 0u) continue;
@@ -1399,12 +1402,15 @@ __global__ void __launch_bounds__(DecodeCfg<H, Q>::THREADS, 1) decode_kernel(con
       // A range inside one sequence (one unit) is selected by every warp of the CTA, as group 0;
       // otherwise the stage warps (group 0) and the epilogue warps (group 1) select side by side.
       // One call site, so the selection's code is laid out once.
-      const bool whole = ks->round[slot].ul - ks->round[slot].uf == 1;
+      // With several rows, a one-unit range is split by rows between the two groups instead.
+      const bool one_unit = ks->round[slot].ul - ks->round[slot].uf == 1;
+      const bool whole = one_unit && Q == 1;
+      const bool row_split = one_unit && Q > 1;
       const int g = whole || stage_role ? 0 : 1;
       const int gtid = static_cast<int>(threadIdx.x) - (g == 0 ? 0 : C::EPI_WARP0 * 32);
       const Blk B{whole ? static_cast<int>(threadIdx.x) : gtid, whole ? C::THREADS : C::THREADS / 2,
                   g == 0 ? kSelBarrier0 : kSelBarrier1, reinterpret_cast<uint32_t*>(smem + C::OFF_SCR) + g * 128};
-      select_round<H, Q>(p, smem, slot, g, B);
+      select_round<H, Q>(p, smem, slot, g, B, row_split);
     }
     fence_proxy_async_smem();  // the selection's writes to the stage area precede the next bulk copies
     named_barrier_sync(kAllBarrier, C::THREADS);
