@@ -644,6 +644,26 @@ def run_mtp_prefill_form(steps: int, warmup: int, flush: L2Flush):
     return sec, pairs, alg, int(status.item()) == 0
 
 
+def run_mxf4_probe(iters: int = 2048, reps: int = 5):
+    """The MXFP4 tensor-core rate at the scorers' MMA shape (the library's probe kernel, one CTA per
+    SM issuing back-to-back block-scaled MMAs from shared memory): TFLOP/s over `reps` launches."""
+    import torch
+
+    import fp4_sparse_attention_mxfp4_gb300 as fx
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        fx.idx_fp4_mxf4_probe(iters, status)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record()
+        fx.idx_fp4_mxf4_probe(iters, status)
+        b.record()
+    torch.cuda.synchronize()
+    sec = statistics.median(a.elapsed_time(b) for a, b in ev) / 1e3
+    return fx.idx_fp4_mxf4_probe_flops(iters) / sec / 1e12, int(status.item()) == 0
+
+
 def oracle_decode_rate(case, threads: int, min_seconds: float, max_reps: int = 5):
     """The oracle (fp64 scoring + exact sort top-k) on the given decode workload, host cores:
     keys per second over whole repetitions."""
@@ -810,13 +830,18 @@ def run_ours(args):
             "row_key_pairs_per_s": mt_pairs / mt_s, "alg_bytes_per_call": mt_alg,
             "hbm_frac": mt_alg / mt_s / 1e9 / hbm, "status_ok": mt_ok}
         fp4_peak = bf16 * FP4_OVER_BF16
+        probe_tflops, probe_ok = run_mxf4_probe()
+        line["fp4_mma_probe"] = {
+            "what": "tcgen05.mma kind::mxf4 block_scale, M128 N128 K64 (the scorers' instruction), one CTA per "
+                    "SM, 8 issuing warps, shared-memory operands", "tflops": probe_tflops, "status_ok": probe_ok}
         pf_s, pf_flops, pf_steps, pf_ok = run_prefill(max(5, min(args.steps, 50)), 3, flush)
         line["prefill"] = {
             "workload": "causal prefill: 4 prompts (2634..4295 tokens), 512-row steps with padding rows, "
                         "64 heads, top-2048", "steps_per_pass": pf_steps, "ms_per_pass": pf_s * 1e3,
             "alg_flop_per_pass": pf_flops, "tflops": pf_flops / pf_s / 1e12,
             "peak_tflops": fp4_peak, "peak_source": f"{peak_kind} bf16_tflops x {FP4_OVER_BF16:g} (nominal FP4/bf16)",
-            "frac_fp4_peak": pf_flops / pf_s / 1e12 / fp4_peak, "status_ok": pf_ok}
+            "frac_fp4_peak": pf_flops / pf_s / 1e12 / fp4_peak,
+            "frac_of_mxf4_probe": pf_flops / pf_s / 1e12 / probe_tflops, "status_ok": pf_ok}
         pf_s, pf_flops, pf_steps, pf_ok = run_prefill(max(5, min(args.steps, 20)), 3, flush,
                                                       synth.prefill_flat_config())
         line["prefill_flat"] = {

@@ -37,6 +37,8 @@ from ._lib import (  # noqa: F401
     idx_fp4_decode_schedule_bytes,
     idx_fp4_decode_workspace_bytes,
     idx_fp4_merge_candidates,
+    idx_fp4_mxf4_probe,
+    idx_fp4_mxf4_probe_flops,
     idx_fp4_prefill_logits_topk,
     idx_fp4_prefill_workspace_bytes,
     idx_fp4_quant_and_cache,

@@ -52,6 +52,8 @@ SIGNATURES = {
                                               _SZ, _P, _SZ, _P, _P, _P, _I64, _P, _P]),
     "idx_fp4_build_decode_schedule_range": (_I32, [_P, _P, _I32, _I32, _I64, _P, _SZ, _P, _P]),
     "idx_fp4_merge_candidates": (_I32, [_P, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]),
+    "idx_fp4_mxf4_probe_flops": (_I64, [_I32]),
+    "idx_fp4_mxf4_probe": (_I32, [_I32, _P, _P]),
     "idx_fp4_prefill_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I64, _I32]),
     "idx_fp4_decode_static_bytes": (_SZ, [_I32, _I64, _I32]),
     "idx_fp4_decode_logits_topk_static": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32, _I64, _P,
@@ -210,6 +212,18 @@ def idx_fp4_merge_candidates(cand_val, cand_idx, topk: int, topk_idx, topk_val=N
     code = lib().idx_fp4_merge_candidates(_ptr(cand_val), _ptr(cand_idx), W, R, K, int(topk), _ptr(topk_idx),
                                           _ptr(topk_val), _ptr(status), _stream(stream))
     _check("idx_fp4_merge_candidates", code)
+
+
+def idx_fp4_mxf4_probe_flops(iters: int) -> int:
+    """FLOPs of one idx_fp4_mxf4_probe launch on the current device."""
+    return int(lib().idx_fp4_mxf4_probe_flops(int(iters)))
+
+
+def idx_fp4_mxf4_probe(iters: int, status=None, stream=None):
+    """Launch the MXFP4 MMA rate probe (one CTA per SM, `iters` MMA pairs per issuing warp)."""
+    if status is not None:
+        _need(status, "status", torch.int32)
+    _check("idx_fp4_mxf4_probe", lib().idx_fp4_mxf4_probe(int(iters), _ptr(status), _stream(stream)))
 
 
 def idx_fp4_decode_workspace_bytes(max_batch: int, max_ctx: int, topk: int) -> int:

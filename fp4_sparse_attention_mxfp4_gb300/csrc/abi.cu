@@ -23,6 +23,8 @@ cudaError_t launch_build_prefill_schedule(const int32_t* cu_seqlens, const int32
                                           int64_t units_cap, int64_t slots_cap, void* workspace, int32_t* status,
                                           cudaStream_t stream);
 bool decode_shape_supported(int heads, int next_n);
+int64_t mxf4_probe_flops(int ctas, int iters);
+cudaError_t launch_mxf4_probe(int ctas, int iters, int32_t* status, cudaStream_t stream);
 cudaError_t launch_merge_candidates(const float* cand_val, const int32_t* cand_idx, int lists, int rows, int k_in,
                                     int topk, int32_t* topk_idx, float* topk_val, cudaStream_t stream);
 cudaError_t launch_decode(const uint8_t* q_packed, const uint8_t* q_scale, const float* weights,
@@ -185,6 +187,19 @@ int idx_fp4_build_decode_schedule_mtp(const int32_t* ctx_lens_dev, int batch, in
                                       cudaStream_t stream) {
   return build_schedule(ctx_lens_dev, nullptr, batch, next_n, max_batch, max_ctx, sched_dev, sched_bytes, status_dev,
                         stream);
+}
+
+int64_t idx_fp4_mxf4_probe_flops(int iters) {
+  const int ctas = device_ctas();
+  if (iters < 1 || ctas <= 0) return 0;
+  return mxf4_probe_flops(ctas, iters);
+}
+
+int idx_fp4_mxf4_probe(int iters, int32_t* status_dev, cudaStream_t stream) {
+  if (iters < 1 || iters > (1 << 20)) return IDX_FP4_ERR_ARG;
+  const int ctas = device_ctas();
+  if (ctas <= 0) return IDX_FP4_ERR_CUDA;
+  return to_code(launch_mxf4_probe(ctas, iters, status_dev, stream));
 }
 
 int idx_fp4_merge_candidates(const float* cand_val, const int32_t* cand_idx, int num_lists, int rows, int k_in,

@@ -301,6 +301,17 @@ int idx_fp4_decode_logits_topk_static(const uint8_t *q_packed, const uint8_t *q_
                                       int32_t *topk_idx, float *topk_val, float *logits_debug,
                                       int64_t logits_stride, int32_t *status_dev, cudaStream_t stream);
 
+/* ---- Measurement ------------------------------------------------------------------------
+ * The MXFP4 tensor-core rate the prefill scorer is measured against (the pages give no FP4
+ * peak): idx_fp4_mxf4_probe launches, on `stream`, one CTA per SM whose warps issue `iters`
+ * pairs of block-scaled MXFP4 MMAs each (tcgen05.mma kind::mxf4, M = 128, N = 128, K = 64, the
+ * scorers' instruction) from shared-memory operands; time it with events and divide
+ * idx_fp4_mxf4_probe_flops(iters) (host: the launch's FLOPs on the current device, 0 for
+ * iters < 1) by the time. 1 <= iters <= 2^20 (else IDX_FP4_ERR_ARG). Reads and writes no
+ * caller memory except status_dev (nullable; IDX_FP4_DEV_TIMEOUT if a bounded wait gave up). */
+int64_t idx_fp4_mxf4_probe_flops(int iters);
+int idx_fp4_mxf4_probe(int iters, int32_t *status_dev, cudaStream_t stream);
+
 /* Human-readable name of a return code. */
 const char *idx_fp4_error_string(int code);
 

@@ -94,3 +94,4 @@ def test_sharded_decode_equals_unsharded(world):
     torch.cuda.synchronize()
     assert torch.equal(out_i, run.topk_idx)
     assert torch.equal(out_v.view(torch.int32), run.topk_val.view(torch.int32))
+
