@@ -58,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--profile", action="store_true",
                     help="only set up the decode workload and run warmup+steps direct launches (for ncu)")
+    ap.add_argument("--profile-prefill", action="store_true",
+                    help="only set up the prefill workload and run warmup+steps direct passes (for ncu)")
     ap.add_argument("--no-extras", action="store_true", help="skip the CPU baseline, e2e and prefill legs")
     return ap.parse_args(argv)
 
@@ -513,7 +515,7 @@ def run_decode_e2e(bench: DecodeBench, steps: int, warmup: int):
     return statistics.mean(times), h2d, d2h
 
 
-def run_prefill(steps: int, warmup: int, flush: L2Flush, case=None):
+def run_prefill(steps: int, warmup: int, flush: L2Flush, case=None, direct_passes: int = 0):
     """Causal prefill of a PrefillCase (default: 4 prompts of 2634..4295 tokens) in 512-row steps,
     all steps captured in one graph; returns seconds per full prefill pass and the algorithmic
     FLOPs of a pass."""
@@ -557,6 +559,11 @@ def run_prefill(steps: int, warmup: int, flush: L2Flush, case=None):
             fx.idx_fp4_prefill_logits_topk(p["qp"], p["qs"], p["w"], kv_p, kv_s, p["bt"], p["ctx"], p["cu"], p["re"],
                                            k, p["mc"], p["ws"], p["idx"], p["val"], status=status)
 
+    if direct_passes > 0:
+        for _ in range(direct_passes):
+            one_pass()
+        torch.cuda.synchronize()
+        return 0.0, flops, len(case.steps), int(status.item()) == 0
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -866,6 +873,11 @@ def main(argv=None):
         return run_reference(args)
     if args.profile:
         return run_profile(args)
+    if args.profile_prefill:
+        _, _, steps, ok = run_prefill(0, 0, None, direct_passes=args.warmup + args.steps)
+        print(json.dumps({"profile_run": "causal prefill, 4 prompts", "steps_per_pass": steps, "status_ok": ok}),
+              flush=True)
+        return 0 if ok else 1
     return run_ours(args)
 
 

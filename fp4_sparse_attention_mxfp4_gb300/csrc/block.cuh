@@ -66,32 +66,6 @@ __device__ __forceinline__ uint2 blk_scan2(const Blk& B, uint32_t a, uint32_t b,
   return make_uint2(pa + ia - a, pb + ib - b);
 }
 
-// Bin of the need-th largest element (1 <= need <= total) of hist[0, nb), searching from the top:
-// returns (bin, elements in the bins above it) to every thread.
-__device__ __forceinline__ uint2 blk_find_bin(const Blk& B, const uint32_t* hist, int nb, uint32_t need) {
-  const int per = (nb + B.nt - 1) / B.nt;
-  const int b0 = min(nb, B.tid * per), b1 = min(nb, b0 + per);
-  uint32_t s = 0;
-#pragma unroll 1
-  for (int b = b0; b < b1; ++b) s += hist[b];
-  uint32_t total = 0;
-  const uint32_t pre = blk_scan2(B, s, 0u, &total, nullptr).x;
-  uint32_t above = total - pre - s;  // elements in the bins of later threads
-#pragma unroll 1
-  for (int b = b1 - 1; b >= b0; --b) {
-    const uint32_t c = hist[b];
-    if (above < need && need <= above + c) {
-      B.sc[64] = static_cast<uint32_t>(b);
-      B.sc[65] = above;
-    }
-    above += c;
-  }
-  B.sync();
-  const uint2 r = make_uint2(B.sc[64], B.sc[65]);
-  B.sync();
-  return r;
-}
-
 __device__ __forceinline__ void blk_zero(const Blk& B, uint32_t* p, int n) {
   for (int i = B.tid; i < n; i += B.nt) p[i] = 0u;
 }
@@ -102,6 +76,9 @@ __device__ __forceinline__ int2 blk_run(const Blk& B, int n) {
   const int r0 = min(n, B.tid * per);
   return make_int2(r0, min(n, r0 + per));
 }
+
+template <int CB, int FPER>
+__device__ __forceinline__ uint2 warp_find_bin2(const uint32_t* fine, const uint32_t* coarse, uint32_t need, int lane);
 
 // Threshold of an exact top-kk over n candidates whose first-level bin is known: `bin` holds the
 // kk-th largest key, and `need` (>= 1) of its keys are among the kk. Finds the low 20 bits of T from
@@ -127,18 +104,20 @@ __device__ __forceinline__ uint2 blk_resolve(const Blk& B, KeyAt key, int n, uin
       const uint32_t k = key(p);
       if ((k >> kL1Shift) == bin) list[o++] = k;
     }
+  // two 10-bit levels, each a 1024-bin histogram with 32 coarse bins, searched by one warp
+  blk_zero(B, hist, 2 * (1024 + 32));
   B.sync();
   uint32_t low = 0u;
 #pragma unroll 1
   for (int level = 0; level < 2; ++level) {
-    const int shift = level == 0 ? 10 : 0;
-    blk_zero(B, hist, 1024);
-    B.sync();
+    uint32_t* h = hist + level * (1024 + 32);
     auto count = [&](uint32_t k) {
       if ((k >> kL1Shift) != bin) return;
       const uint32_t l = k & 0xFFFFFu;
-      if (level == 0) smem_red_add(&hist[l >> 10], 1u);
-      else if ((l >> 10) == (low >> 10)) smem_red_add(&hist[l & 1023u], 1u);
+      if (level == 1 && (l >> 10) != (low >> 10)) return;
+      const uint32_t d = level == 0 ? (l >> 10) : (l & 1023u);
+      smem_red_add(&h[d], 1u);
+      smem_red_add(&h[1024 + (d >> 5)], 1u);
     };
     if (listed) {
 #pragma unroll 1
@@ -148,9 +127,16 @@ __device__ __forceinline__ uint2 blk_resolve(const Blk& B, KeyAt key, int n, uin
       for (int p = B.tid; p < n; p += B.nt) count(key(p));
     }
     B.sync();
-    const uint2 r = blk_find_bin(B, hist, 1024, need);
-    need -= r.y;
-    low |= r.x << shift;
+    if (B.warp() == 0) {
+      const uint2 r = warp_find_bin2<32, 32>(h, h + 1024, need, B.lane());
+      if (B.lane() == 0) {
+        B.sc[64] = r.x;
+        B.sc[65] = r.y;
+      }
+    }
+    B.sync();
+    need -= B.sc[65];
+    low |= B.sc[64] << (level == 0 ? 10 : 0);
   }
   return make_uint2((bin << kL1Shift) | low, need);
 }

@@ -641,18 +641,35 @@ __device__ __forceinline__ void blk_emit(const Blk& B, KeyAt key, TokAt tok, int
 // Exact top-kk of n candidates in token order (first-level bin unknown: counted here).
 template <class KeyAt, class TokAt, class Out>
 __device__ __forceinline__ void blk_select(const Blk& B, KeyAt key, TokAt tok, int n, int kk, uint32_t* hist,
-                                           uint32_t* list, int list_cap, Out out) {
+                                           uint32_t* list, int list_cap, Out out, const uint32_t* pre = nullptr) {
   if (kk <= 0 || n <= 0) return;
   if (kk >= n) {
     blk_emit(B, key, tok, n, true, 0u, 0u, out);
     return;
   }
-  blk_zero(B, hist, kL1Bins);
-  B.sync();
+  // the first-level histogram (4096 fine bins, then 64 coarse): counted in the stream, or here
+  const uint32_t* h = pre;
+  if (h == nullptr) {
+    blk_zero(B, hist, kL1Bins + 64);
+    B.sync();
 #pragma unroll 1
-  for (int x = B.tid; x < n; x += B.nt) smem_red_add(&hist[key(x) >> kL1Shift], 1u);
+    for (int x = B.tid; x < n; x += B.nt) {
+      const uint32_t b = key(x) >> kL1Shift;
+      smem_red_add(&hist[b], 1u);
+      smem_red_add(&hist[kL1Bins + (b >> 6)], 1u);
+    }
+    h = hist;
+  }
   B.sync();
-  const uint2 r = blk_find_bin(B, hist, kL1Bins, static_cast<uint32_t>(kk));
+  if (B.warp() == 0) {
+    const uint2 r = warp_find_bin2<64, 64>(h, h + kL1Bins, static_cast<uint32_t>(kk), B.lane());
+    if (B.lane() == 0) {
+      B.sc[64] = r.x;
+      B.sc[65] = r.y;
+    }
+  }
+  B.sync();
+  const uint2 r = make_uint2(B.sc[64], B.sc[65]);
   bool consistent = true;
   const uint2 tn = blk_resolve(B, key, n, r.x, static_cast<uint32_t>(kk) - r.y, hist, list, list_cap, &consistent);
   blk_emit(B, key, tok, n, false, tn.x, tn.y, out);
@@ -910,7 +927,13 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
     const uint32_t* keys = lg + q * C::CAP + u.buf;
     auto key = [&](int x) { return keys[x]; };
     auto tok = [&](int x) { return u.kb + x; };
-    blk_select(B, key, tok, un, s.kk, hist, P + C::P_LIST, C::LIST_CAP, seg_out(p, ws, s, v.seq_nseg[u.seq], Q));
+    // a range-end unit's histogram was counted in the stream (one row)
+    const uint32_t* pre = nullptr;
+    if constexpr (C::HIST_IN_STREAM)
+      if (i == uf || i == ul - 1)
+        pre = reinterpret_cast<const uint32_t*>(smem + C::OFF_HST) + (i == uf ? 0 : C::HST_WORDS);
+    blk_select(B, key, tok, un, s.kk, hist, P + C::P_LIST, C::LIST_CAP, seg_out(p, ws, s, v.seq_nseg[u.seq], Q),
+               pre);
     segment_done(s);
     B.sync();
   };
