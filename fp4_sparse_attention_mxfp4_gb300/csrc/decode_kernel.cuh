@@ -82,21 +82,26 @@ struct DecodeCfg {
   static constexpr int N = H * Q;
   static_assert(N % 16 == 0 && N <= 128, "MMA N dimension: next_n * heads, a multiple of 16 up to 128");
   static constexpr int GROUPS = 3;                 // epilogue groups (tiles t with t % GROUPS == g)
-  static constexpr int ACC = N <= 64 ? 6 : 3;      // TMEM accumulators
-  static constexpr int STAGES = 12;                // tiles in flight; one stage warp per stage
-  static constexpr int EPI_WARP0 = STAGES;
+  // One query row: 12 tiles in flight and 6 accumulators when N <= 64. Several rows: 9 tiles in
+  // flight and 3 accumulators, so that a range of 128 tiles (next_n 2) or 64 (next_n 4) has room for
+  // its logits; the stream is then bound by the epilogue's N columns per key, not by the copies.
+  static constexpr int ACC = N <= 64 && Q == 1 ? 6 : 3;  // TMEM accumulators
+  static constexpr int STAGES = Q == 1 ? 12 : 9;         // tiles in flight; stage warp s streams stage s
+  static constexpr int STAGE_WARPS = 12;                 // the stage role (warps past STAGES only select)
+  static constexpr int EPI_WARP0 = STAGE_WARPS;
   static constexpr int EPI_WARPS = 4 * GROUPS;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
-  static constexpr int THREADS = (STAGES + EPI_WARPS) * 32;
+  static constexpr int THREADS = (STAGE_WARPS + EPI_WARPS) * 32;
   // Registers: the launch gives 65536 / THREADS each; during the stream the stage warpgroups give
   // some back and the epilogue warpgroups take them (a tile's 64 accumulator columns in flight).
   static constexpr uint32_t LAUNCH_REGS = (65536u / static_cast<uint32_t>(THREADS)) / 8u * 8u;
   static constexpr uint32_t STAGE_REGS = 56u;
   static constexpr uint32_t EPI_REGS =
-      (LAUNCH_REGS * (STAGES + EPI_WARPS) - STAGE_REGS * STAGES) / EPI_WARPS / 8u * 8u;
-  static_assert(STAGES % 4 == 0 && EPI_WARPS % 4 == 0, "roles are whole warpgroups");
-  static_assert(STAGES == EPI_WARPS, "the two roles form two equal selection groups");
-  static_assert(STAGE_REGS * STAGES + EPI_REGS * EPI_WARPS <= LAUNCH_REGS * (STAGES + EPI_WARPS),
+      (LAUNCH_REGS * (STAGE_WARPS + EPI_WARPS) - STAGE_REGS * STAGE_WARPS) / EPI_WARPS / 8u * 8u;
+  static_assert(STAGE_WARPS % 4 == 0 && EPI_WARPS % 4 == 0, "roles are whole warpgroups");
+  static_assert(STAGE_WARPS == EPI_WARPS, "the two roles form two equal selection groups");
+  static_assert(STAGES <= STAGE_WARPS, "one stage warp per stage");
+  static_assert(STAGE_REGS * STAGE_WARPS + EPI_REGS * EPI_WARPS <= LAUNCH_REGS * (STAGE_WARPS + EPI_WARPS),
                 "the re-split fits the registers the block is launched with");
   static constexpr int CAP = decode_cap_tiles(Q) * kTileKeys;  // row-buffer keys per query row
   static constexpr uint32_t TMEM_COLS = 512;
@@ -139,7 +144,8 @@ struct DecodeCfg {
   static constexpr int P_SOFF = P_WORDS - 1040;       // [1024 + 1] segment offsets of a sequence merge
   static constexpr int P_CAND = P_LVL;                // a sequence merge's staged candidate keys
   static constexpr int CCAP = (P_SOFF - P_CAND) / 128 * 128;
-  static_assert(P_EQPRE + Q * (kDecodeMaxCtas + 4) <= P_SOFF && CCAP >= 4096, "selection areas fit");
+  // (a merge whose lists exceed CCAP keys reads them from the workspace instead of staging them)
+  static_assert(P_EQPRE + Q * (kDecodeMaxCtas + 4) <= P_SOFF && CCAP >= 2048, "selection areas fit");
   static_assert(P_HIST % 4 == 0 && P_LVL % 4 == 0, "16-byte aligned histograms");
   // Row-buffer positions (16 bits) of the keys that can still be selected, per row: in the words
   // between the exchange's areas and the merge offsets, or, when the whole CTA selects one unit, in
@@ -147,7 +153,7 @@ struct DecodeCfg {
   static constexpr int P_CIDX = P_EQPRE + Q * (kDecodeMaxCtas + 4);
   static constexpr int CIDX_GROUP = (P_SOFF - P_CIDX) * 2 / Q / 8 * 8;  // positions per row, own area
   static constexpr int CIDX_WHOLE = CAP;                                 // positions per row, second half
-  static_assert(CAP <= 65536 && Q * CAP / 2 <= P_WORDS, "candidate positions fit the second half");
+  static_assert(CAP <= 65536 && (Q > 1 || CAP / 2 <= P_WORDS), "candidate positions fit the second half");
 };
 
 
@@ -1395,14 +1401,14 @@ __global__ void __launch_bounds__(DecodeCfg<H, Q>::THREADS, 1) decode_kernel(con
   // epilogue warps read them out; then every warp, in two selection groups, selects the round's
   // units. Register budgets are re-split for the stream and evened out for the selection.
   const int rounds = ks->h.rounds;
-  const bool stage_role = warp < C::STAGES;
+  const bool stage_role = warp < C::STAGE_WARPS;
   int tiles = 0, units = 0;  // streamed in earlier rounds (kept by every epilogue thread alike)
   for (int r = 0; r < rounds; ++r) {
     const int slot = r & 1;
     if (stage_role) {
       warpgroup_regs_dec<C::STAGE_REGS>();
       named_barrier_sync(kAllBarrier, C::THREADS);
-      if (ks->round[slot].uf < ks->round[slot].ul) stream_stage_warp<H, Q>(p, smem, slot, warp, lane);
+      if (warp < C::STAGES && ks->round[slot].uf < ks->round[slot].ul) stream_stage_warp<H, Q>(p, smem, slot, warp, lane);
       warpgroup_regs_inc<C::LAUNCH_REGS>();
     } else {
       warpgroup_regs_inc<C::EPI_REGS>();

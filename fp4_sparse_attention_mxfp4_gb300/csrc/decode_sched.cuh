@@ -24,7 +24,7 @@ constexpr int kMinTilesPerRange = 32;  // a CTA's share is at least 4096 keys: a
 
 // Tiles of one CTA range: its logits (4 bytes per key and row) fill the row buffer.
 __host__ __device__ constexpr int decode_cap_tiles(int next_n) {
-  return next_n <= 1 ? 128 : (next_n == 2 ? 96 : 48);
+  return next_n <= 2 ? 128 : 64;
 }
 
 struct DecodeUnit {  // 32 bytes

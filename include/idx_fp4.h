@@ -184,7 +184,7 @@ int idx_fp4_decode_logits_topk(const uint8_t *q_packed, const uint8_t *q_scale, 
  * next_n is 1, 2 or 4 with next_n * num_heads <= 128 (else IDX_FP4_ERR_SHAPE; larger shapes go
  * through idx_fp4_prefill_logits_topk, one request per sequence).
  *   Schedule: idx_fp4_build_decode_schedule_mtp with the same next_n (a range holds at most
- *   12288 keys for next_n 2, 6144 for 4), into a buffer of idx_fp4_decode_schedule_bytes.
+ *   16384 keys for next_n 2, 8192 for 4), into a buffer of idx_fp4_decode_schedule_bytes.
  *   Workspace: idx_fp4_decode_mtp_workspace_bytes, zero-filled before first use.
  *   q_packed [batch * next_n][H][64], q_scale [batch * next_n][H][4], weights [batch * next_n][H];
  *   topk_idx / topk_val [batch * next_n][topk]; logits_debug [batch * next_n][logits_stride].

@@ -127,11 +127,11 @@ def test_decode_mtp_full_size_sampled():
 
 
 def test_decode_mtp_several_rounds():
-    """More keys than one pass of the grid holds at next_n 4 (a range is at most 6144 keys), so
+    """More keys than one pass of the grid holds at next_n 4 (a range is at most 8192 keys), so
     the sequences' segments from different rounds are merged: rows of the first and last
     sequences against the oracle."""
     sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 256)
-    per_round = sms * 48 * 128
+    per_round = sms * 64 * 128
     nseq = 8
     L = -(-(per_round * 5 // 4) // nseq) + 1
     case = synth.mtp_case("dmtp_rounds", 95, [L] * (nseq - 1) + [L - 333], 32, 2048, 4)
