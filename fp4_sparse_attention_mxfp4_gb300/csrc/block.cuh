@@ -70,9 +70,10 @@ __device__ __forceinline__ void blk_zero(const Blk& B, uint32_t* p, int n) {
   for (int i = B.tid; i < n; i += B.nt) p[i] = 0u;
 }
 
-// The contiguous run of [0, n) that thread tid owns in run-based passes (runs in thread order).
+// The contiguous run of [0, n) that thread tid owns in run-based passes (runs in thread order). An
+// odd run length puts the lanes of a warp on distinct shared-memory banks in word-wise passes.
 __device__ __forceinline__ int2 blk_run(const Blk& B, int n) {
-  const int per = (n + B.nt - 1) / B.nt;
+  const int per = ((n + B.nt - 1) / B.nt) | 1;
   const int r0 = min(n, B.tid * per);
   return make_int2(r0, min(n, r0 + per));
 }
@@ -258,9 +259,11 @@ __device__ __forceinline__ uint2 warp_find_bin2(const uint32_t* fine, const uint
 }
 
 // The run of [0, n) that thread tid owns in run-based passes over 16-byte aligned keys: a multiple
-// of 4 long (except the last), runs in thread order.
+// of 4 long (except the last), runs in thread order. A run length of 4 mod 8 words spreads the 16-byte
+// loads of a warp's lanes over every bank.
 __device__ __forceinline__ int2 blk_run4(const Blk& B, int n) {
-  const int per = (((n + B.nt - 1) / B.nt) + 3) & ~3;
+  int per = (((n + B.nt - 1) / B.nt) + 3) & ~3;
+  if ((per & 7) == 0) per += 4;
   const int r0 = min(n, B.tid * per);
   return make_int2(r0, min(n, r0 + per));
 }

@@ -139,19 +139,19 @@ struct DecodeCfg {
   static constexpr int P_HIST = 0;                    // [kL1Bins + 64] histogram, fine and coarse
   static constexpr int P_LIST = P_HIST + kL1Bins + 64;  // [LIST_CAP] keys of the threshold bin
   static constexpr int LIST_CAP = 2048;
-  static constexpr int P_LVL = P_LIST + LIST_CAP;     // [1024 + 32] lower radix levels, fine and coarse
-  static constexpr int P_EQPRE = P_LVL + 1056;       // [Q][kDecodeMaxCtas + 4] prefix of the units' bin keys
-  static constexpr int P_SOFF = P_WORDS - 1040;       // [1024 + 1] segment offsets of a sequence merge
-  static constexpr int P_CAND = P_LVL;                // a sequence merge's staged candidate keys
-  static constexpr int CCAP = (P_SOFF - P_CAND) / 128 * 128;
-  // (a merge whose lists exceed CCAP keys reads them from the workspace instead of staging them)
-  static_assert(P_EQPRE + Q * (kDecodeMaxCtas + 4) <= P_SOFF && CCAP >= 2048, "selection areas fit");
-  static_assert(P_HIST % 4 == 0 && P_LVL % 4 == 0, "16-byte aligned histograms");
-  // Row-buffer positions (16 bits) of the keys that can still be selected, per row: in the words
-  // between the exchange's areas and the merge offsets, or, when the whole CTA selects one unit, in
-  // the second group's half.
+  static constexpr int P_EQPRE = P_LIST + LIST_CAP;  // [Q][kDecodeMaxCtas + 4] prefix of the units' bin keys
+  // Row-buffer positions (16 bits) of the keys that can still be selected, per row: in the rest of
+  // the group's area, or, when the whole CTA selects one unit, in the second group's half.
   static constexpr int P_CIDX = P_EQPRE + Q * (kDecodeMaxCtas + 4);
-  static constexpr int CIDX_GROUP = (P_SOFF - P_CIDX) * 2 / Q / 8 * 8;  // positions per row, own area
+  static constexpr int CIDX_GROUP = (P_WORDS - P_CIDX) * 2 / Q / 8 * 8;  // positions per row, own area
+  // A sequence merge (after the round's exchanges: the bin-key prefixes and positions are dead)
+  // stages candidate keys over them and keeps its segment offsets in the area's last words; a merge
+  // whose lists exceed CCAP keys reads them from the workspace instead.
+  static constexpr int P_CAND = P_EQPRE;
+  static constexpr int P_SOFF = P_WORDS - 1040;       // [1024 + 1] segment offsets of a sequence merge
+  static constexpr int CCAP = (P_SOFF - P_CAND) / 128 * 128;
+  static_assert(P_CIDX < P_WORDS && CCAP >= 2048, "selection areas fit");
+  static_assert(P_HIST % 4 == 0 && P_LIST % 4 == 0, "16-byte aligned histograms");
   static constexpr int CIDX_WHOLE = CAP;                                 // positions per row, second half
   static_assert(CAP <= 65536 && (Q > 1 || CAP / 2 <= P_WORDS), "candidate positions fit the second half");
 };
@@ -840,7 +840,6 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   const int uf = ks->round[slot].uf, ul = ks->round[slot].ul;
   uint32_t* P = reinterpret_cast<uint32_t*>(smem) + g * C::P_WORDS;
   uint32_t* hist = P + C::P_HIST;
-  uint32_t* lvl = P + C::P_LVL;
   uint32_t* cnt = ks->counter[g];
   const uint32_t* lg = reinterpret_cast<const uint32_t*>(smem + C::OFF_LG);
   const int topk = p.topk;
