@@ -878,10 +878,14 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   auto seg_keys = [&](const SegCtx& s) { return clampi(s.row_end - s.sg.kb, 0, s.sg.ke - s.sg.kb); };
   auto sync_word = [&](const SegCtx& s, int k) { return &ws.sync[(static_cast<int64_t>(s.seg_id) * Q + s.q) * 4 + k]; };
   // Unit j of a segment: its first tile and tile count follow from the segment's first tile and the
-  // range length (unit 0 starts the segment, unit j > 0 starts range seg.tile0 / per + j), so the
-  // other units' areas are found without reading the unit table.
+  // range length (unit 0 starts the segment; unit j > 0 starts range seg.tile0 / per + j, or, with
+  // ranges aligned to the sequences, j ranges after the segment's first tile), so the other units'
+  // areas are found without reading the unit table.
   const int per = ks->h.per;
-  auto unit_tile0 = [&](const DecodeSeg& sg, int j) { return j == 0 ? sg.tile0 : (sg.tile0 / per + j) * per; };
+  const bool aligned = ks->h.aligned != 0;
+  auto unit_tile0 = [&](const DecodeSeg& sg, int j) {
+    return j == 0 ? sg.tile0 : (aligned ? sg.tile0 + j * per : (sg.tile0 / per + j) * per);
+  };
   auto unit_tiles = [&](const DecodeSeg& sg, int j) {
     const int seg_end = sg.tile0 + (sg.ke - sg.kb + kTileKeys - 1) / kTileKeys;
     const int t1 = j + 1 < sg.nunits ? unit_tile0(sg, j + 1) : seg_end;

@@ -9,6 +9,9 @@
 // range is a unit; the units of one sequence inside one round form a segment. A segment of one unit
 // is selected inside its CTA; the units of a longer segment agree on the segment's threshold through
 // an exchange in the workspace. A sequence spanning several rounds merges its segments' lists.
+// With several query rows the ranges may instead be cut from the tiles with every sequence padded
+// to whole ranges (header flag `aligned`), so that each sequence starts a range; a unit's tile0
+// stays its position in the unpadded layout, which sizes the workspace.
 #pragma once
 #include <cstdint>
 
@@ -64,7 +67,7 @@ struct DecodeSchedHeader {  // 64 bytes
   int32_t total_tiles;
   int32_t tiles_cap;   // max_batch * tiles(max_ctx): fixes the workspace's per-row strides
   int32_t ok;          // 0: the schedule could not be built (every row comes out empty)
-  int32_t pad;
+  int32_t aligned;     // 1: every sequence starts a range (ranges cut from tiles padded per sequence)
 };
 static_assert(sizeof(DecodeSchedHeader) == 64, "64-byte header");
 

@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
   int* s_start = s_dyn;                   // [kMaxBatch + 1] first tile of each sequence
   int* s_ne = s_start + kMaxBatch + 1;    // [kMaxBatch + 1] non-empty sequences before each
   int* s_seg0 = s_ne + kMaxBatch + 1;     // [kMaxBatch + 1] segments before each
-  int* s_kb0 = s_seg0 + kMaxBatch + 1;    // [kMaxBatch] first key of each sequence's range
+  int* s_kb0 = s_seg0 + kMaxBatch + 1;    // [kMaxBatch + 1] first key of each sequence's range
+  int* s_astart = s_kb0 + kMaxBatch + 1;  // [kMaxBatch + 1] first tile of each sequence, tiles end to end
   __shared__ int warp_sums[32];
   __shared__ int s_total, s_nonempty, s_segs, s_chunk;
   pdl_wait();
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
   }
   __syncthreads();
   const int total = s_total;
+  for (int b = tid; b <= kMaxBatch; b += kThreads) s_astart[b] = s_start[b];
 
   // 2. rounds and range length
   const int cap = decode_cap_tiles(next_n);
@@ -125,6 +127,52 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
   if (rounds == 1 && per < kMinTilesPerRange) per = kMinTilesPerRange;
   if (per > cap) per = cap;
   if (per < 1) per = 1;
+
+  // 2b. With several query rows, ranges aligned to the sequences when that keeps the rounds: every
+  // sequence then starts a range, so no CTA holds the ends of two sequences (whose units each
+  // selection group would settle row after row). The ranges are cut from the sequences' tiles
+  // padded to whole ranges ("virtual" tiles, s_start); units keep their tile numbers (s_astart).
+  // Each warp tries one range length from `per` up and the smallest that fits the ranges wins.
+  int aligned = 0;
+  if (next_n > 1 && total > 0) {
+    const int w = tid >> 5, lane = tid & 31;
+    const int step = max(1, (cap - per + 31) / 32);
+    const int cand = per + w * step;
+    int need = 0;
+    if (cand <= cap)
+      for (int b = lane; b < batch; b += 32) need += (s_astart[b + 1] - s_astart[b] + cand - 1) / cand;
+    need = __reduce_add_sync(0xFFFFFFFFu, need);
+    if (lane == 0) warp_sums[w] = cand <= cap && need <= rounds * ctas ? cand : 0x7FFFFFFF;
+    __syncthreads();
+    if (w == 0) {
+      const int best = __reduce_min_sync(0xFFFFFFFFu, warp_sums[lane]);
+      if (lane == 0) s_chunk = best;
+    }
+    __syncthreads();
+    if (s_chunk != 0x7FFFFFFF) {
+      per = s_chunk;
+      aligned = 1;
+    }
+    __syncthreads();
+  }
+  int total_v = total;  // tiles of the layout the ranges are cut from
+  if (aligned) {
+    int vt[kPer], my_v = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      vt[j] = (tiles[j] + per - 1) / per * per;
+      my_v += vt[j];
+    }
+    int offv = scan_excl(my_v, warp_sums, &s_total);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      s_start[tid * kPer + j] = offv;
+      offv += vt[j];
+    }
+    if (tid == 0) s_start[kMaxBatch] = s_total;
+    __syncthreads();
+    total_v = s_total;
+  }
   const int ranges = rounds * ctas;
   const int64_t round_tiles = static_cast<int64_t>(ctas) * per;
   bool ok = ranges <= caps.ranges_cap && total <= caps.tiles_cap;
@@ -138,7 +186,11 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
     }
     return lo;
   };
-  auto seq_end = [&](int b) { return s_start[b + 1 <= kMaxBatch ? b + 1 : kMaxBatch]; };
+  // the end of sequence b's tiles in the layout (before any padding)
+  auto seq_end = [&](int b) {
+    const int n = b + 1 <= kMaxBatch ? b + 1 : kMaxBatch;
+    return s_start[b] + (s_astart[n] - s_astart[b]);
+  };
 
   // 3. segments per sequence: one per round the sequence's tiles touch
   int nseg[kPer], my_segs = 0;
@@ -169,8 +221,8 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
     int cnt = 0;
     if (i < ranges) {
       const int64_t lo = static_cast<int64_t>(i) * per;
-      if (lo < total) {
-        const int hi = static_cast<int>(lo + per < total ? lo + per : total);
+      if (lo < total_v) {
+        const int hi = static_cast<int>(lo + per < total_v ? lo + per : total_v);
         cnt = s_ne[seq_of(hi - 1) + 1] - s_ne[seq_of(static_cast<int>(lo))];
       }
     }
@@ -186,9 +238,9 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
   if (ok) {
     for (int i = tid; i < ranges; i += kThreads) {
       const int64_t lo64 = static_cast<int64_t>(i) * per;
-      if (lo64 >= total) continue;
+      if (lo64 >= total_v) continue;
       const int lo = static_cast<int>(lo64);
-      const int hi = lo + per < total ? lo + per : total;
+      const int hi = lo + per < total_v ? lo + per : total_v;
       const int b0 = seq_of(lo), b1 = seq_of(hi - 1);
       const int r = i / ctas;
       int idx = v.range_first[i];
@@ -205,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
         u.buf = (ulo - lo) * kTileKeys;
         u.seg = s_seg0[b] + (r - r0);
         u.uidx = i - static_cast<int>(seg_lo / per);
-        u.tile0 = ulo;
+        u.tile0 = s_astart[b] + (ulo - sb);
         u.pad = 0;
         v.units[idx++] = u;
       }
@@ -233,7 +285,7 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
       s.kb = s_kb0[b] + (slo - sb) * kTileKeys;
       s.ke = min(s_kb0[b] + (shi - sb) * kTileKeys, v.seq_ctx[b]);
       s.rank = k;
-      s.tile0 = slo;
+      s.tile0 = s_astart[b] + (slo - sb);
       s.pad = 0;
       v.segs[s_seg0[b] + k] = s;
     }
@@ -256,6 +308,7 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
     h.total_tiles = total;
     h.tiles_cap = static_cast<int32_t>(caps.tiles_cap);
     h.ok = ok ? 1 : 0;
+    h.aligned = aligned;
     *v.hdr = h;
   }
 }
@@ -265,7 +318,7 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
 cudaError_t launch_build_decode_schedule(const int32_t* ctx_lens, const int32_t* key_begin, int batch, int next_n,
                                          int max_batch, int64_t max_ctx, int ctas, const DecodeCaps& caps,
                                          void* sched, int32_t* status, cudaStream_t stream) {
-  constexpr size_t smem = sizeof(int) * (4 * (kMaxBatch + 1));
+  constexpr size_t smem = sizeof(int) * (5 * (kMaxBatch + 1));
   cudaError_t e = set_smem_once<build_decode_schedule_kernel>(smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(build_decode_schedule_kernel, dim3(1), dim3(kThreads), smem, stream, 1, false, ctx_lens,

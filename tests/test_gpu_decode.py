@@ -236,7 +236,7 @@ def parse_decode_schedule(buf, max_batch):
     context / first segment / segment count, units, segments)."""
     s = buf.cpu().numpy().view(np.int32)
     keys = ["magic", "ctas", "batch", "max_batch", "next_n", "rounds", "per", "num_units", "num_segs", "units_cap",
-            "segs_cap", "ranges_cap", "total_tiles", "tiles_cap", "ok", "pad"]
+            "segs_cap", "ranges_cap", "total_tiles", "tiles_cap", "ok", "aligned"]
     h = dict(zip(keys, (int(x) for x in s[:16])))
     o = 16
     range_first = s[o:o + h["ranges_cap"] + 1]
@@ -248,17 +248,21 @@ def parse_decode_schedule(buf, max_batch):
     return h, range_first, seq_ctx, seq_seg0, seq_nseg, units, segs
 
 
-@pytest.mark.parametrize("nseq", [8, 40])
-def test_decode_schedule_invariants(nseq):
+@pytest.mark.parametrize("nseq,next_n", [(8, 1), (40, 1), (8, 2), (40, 2), (40, 4)])
+def test_decode_schedule_invariants(nseq, next_n):
     """Units of every sequence partition [0, ctx) exactly in token order; each CTA range holds at
     most one row buffer of tiles; segments group a sequence's units per round with consecutive unit
-    indices; sequences without keys have no segment."""
+    indices; sequences without keys have no segment. With verify rows the ranges may be cut from
+    the tiles padded to whole ranges per sequence (every sequence then starts a range)."""
     base = np.array([131072, 5, 0, 70000, 128, 129, 1, 262144], np.int32)
     extra = synth.Rng(77).integers(0, 9000, max(nseq - len(base), 0)).astype(np.int32)
     ctx = np.concatenate([base, extra])[:nseq]
     max_batch = 16 if nseq <= 16 else 64
     sched = torch.zeros(fx.idx_fp4_decode_schedule_bytes(max_batch, 262144), dtype=torch.uint8, device="cuda")
-    fx.idx_fp4_build_decode_schedule(dev(ctx), max_batch, 262144, sched)
+    if next_n == 1:
+        fx.idx_fp4_build_decode_schedule(dev(ctx), max_batch, 262144, sched)
+    else:
+        fx.idx_fp4_build_decode_schedule_mtp(dev(ctx), next_n, max_batch, 262144, sched)
     torch.cuda.synchronize()
     h, range_first, seq_ctx, seq_seg0, seq_nseg, units, segs = parse_decode_schedule(sched, max_batch)
     assert h["magic"] == 0x44534333 and h["ok"] == 1 and h["batch"] == nseq and h["max_batch"] == max_batch
@@ -267,8 +271,13 @@ def test_decode_schedule_invariants(nseq):
     assert h["total_tiles"] == sum(tiles)
     assert np.array_equal(seq_ctx[:nseq], ctx)
     per, ctas, rounds = h["per"], h["ctas"], h["rounds"]
-    assert 1 <= per <= 128 and rounds * ctas * per >= h["total_tiles"]
+    assert 1 <= per <= (128 if next_n <= 2 else 64) and rounds * ctas * per >= h["total_tiles"]
+    assert h["aligned"] in ((0,) if next_n == 1 else (0, 1))
     starts = np.concatenate([[0], np.cumsum(tiles)])
+    # the layout the ranges are cut from: tiles end to end, or padded to whole ranges
+    padded = [-(-t // per) * per for t in tiles] if h["aligned"] else tiles
+    vstarts = np.concatenate([[0], np.cumsum(padded)])
+    assert vstarts[-1] <= rounds * ctas * per
     covered = {b: [] for b in range(nseq)}
     for i in range(rounds * ctas):
         lo = i * per
@@ -276,8 +285,11 @@ def test_decode_schedule_invariants(nseq):
             seq, kb, ke, buf, seg, uidx, tile0 = units[ui][:7]
             covered[seq].append((kb, ke, ui, seg, uidx))
             assert tile0 == starts[seq] + kb // 128 and kb % 128 == 0
-            assert lo <= tile0 and tile0 + -(-(ke - kb) // 128) <= lo + per
-            assert buf == (tile0 - lo) * 128 and buf + (ke - kb) <= per * 128
+            vt0 = vstarts[seq] + kb // 128
+            assert lo <= vt0 and vt0 + -(-(ke - kb) // 128) <= lo + per
+            assert buf == (vt0 - lo) * 128 and buf + (ke - kb) <= per * 128
+            if h["aligned"]:
+                assert range_first[i + 1] - range_first[i] == 1 and buf == 0
     assert range_first[rounds * ctas] == h["num_units"]
     nsegs = 0
     for b in range(nseq):
