@@ -128,7 +128,10 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
 // then does it touch global memory, and only then pdl_trigger() lets the next kernel begin
 // launching. Since every kernel waits before it can complete, each completion implies its
 // predecessor's, and stream order holds as without the attribute; what is saved is the next
-// kernel's launch latency.
+// kernel's launch latency. The schedule builders are the exception: they read only the caller's
+// inputs, so they run beside the kernel before them and call pdl_wait() only before their first
+// write to global memory other than the status word (their completion still implies their
+// predecessor's).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -54,11 +54,10 @@ __device__ int scan_excl(int v, int* warp_sums, int* total) {
   return r;
 }
 
-__global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const int32_t* __restrict__ ctx_lens,
-                                                                        const int32_t* __restrict__ key_begin,
-                                                                        int batch, int next_n, int max_batch,
-                                                                        int64_t max_ctx, int ctas, DecodeCaps caps,
-                                                                        void* sched, int32_t* status) {
+__device__ __forceinline__ void build_decode_schedule_body(const int32_t* __restrict__ ctx_lens,
+                                                           const int32_t* __restrict__ key_begin, int batch,
+                                                           int next_n, int max_batch, int64_t max_ctx, int ctas,
+                                                           DecodeCaps caps, void* sched, int32_t* status) {
   extern __shared__ int s_dyn[];
   int* s_start = s_dyn;                   // [kMaxBatch + 1] first tile of each sequence
   int* s_ne = s_start + kMaxBatch + 1;    // [kMaxBatch + 1] non-empty sequences before each
@@ -67,8 +66,6 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
   int* s_astart = s_kb0 + kMaxBatch + 1;  // [kMaxBatch + 1] first tile of each sequence, tiles end to end
   __shared__ int warp_sums[32];
   __shared__ int s_total, s_nonempty, s_segs, s_chunk;
-  pdl_wait();
-  pdl_trigger();
   const int tid = threadIdx.x;
   DecodeSchedView v = decode_sched_view(sched, max_batch, caps.ranges_cap, caps.units_cap);
 
@@ -83,7 +80,6 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
       const int64_t raw = ctx_lens[b];
       if (raw < 0 || raw > max_ctx) set_status(status, IDX_FP4_DEV_BAD_CTX);
       else c = static_cast<int>(raw);
-      v.seq_ctx[b] = c;
       if (key_begin != nullptr) {
         const int64_t kb = key_begin[b];
         if (kb < 0 || kb > c || kb % kTileKeys != 0) {
@@ -214,6 +210,15 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
   __syncthreads();
   ok = ok && s_segs <= caps.segs_cap;
 
+  // Everything above read only the caller's inputs; the tables below overwrite the schedule that
+  // the kernel before this one may still be reading.
+  pdl_wait();
+  // the validated context of sequence b
+  auto ctx_of = [&](int b) {
+    const int64_t raw = ctx_lens[b];
+    return raw < 0 || raw > max_ctx ? 0 : static_cast<int>(raw);
+  };
+
   // 4. units per range, and each range's first unit
   int running = 0;
   for (int base = 0; base < ranges; base += kThreads) {
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
         DecodeUnit u;
         u.seq = b;
         u.kb = s_kb0[b] + (ulo - sb) * kTileKeys;
-        u.ke = min(s_kb0[b] + (uhi - sb) * kTileKeys, v.seq_ctx[b]);
+        u.ke = min(s_kb0[b] + (uhi - sb) * kTileKeys, ctx_of(b));
         u.buf = (ulo - lo) * kTileKeys;
         u.seg = s_seg0[b] + (r - r0);
         u.uidx = i - static_cast<int>(seg_lo / per);
@@ -269,6 +274,7 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
   for (int b = tid; b < batch; b += kThreads) {
     const int sb = s_start[b], eb = seq_end(b);
     const int n = ok ? s_seg0[b + 1 <= kMaxBatch ? b + 1 : kMaxBatch] - s_seg0[b] : 0;
+    v.seq_ctx[b] = ctx_of(b);
     v.seq_seg0[b] = s_seg0[b];
     v.seq_nseg[b] = eb > sb ? n : 0;
     if (!ok || eb == sb) continue;
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
       s.first_unit = v.range_first[i0] + (s_ne[b] - s_ne[seq_of(i0 * per)]);
       s.nunits = i1 - i0 + 1;
       s.kb = s_kb0[b] + (slo - sb) * kTileKeys;
-      s.ke = min(s_kb0[b] + (shi - sb) * kTileKeys, v.seq_ctx[b]);
+      s.ke = min(s_kb0[b] + (shi - sb) * kTileKeys, ctx_of(b));
       s.rank = k;
       s.tile0 = s_astart[b] + (slo - sb);
       s.pad = 0;
@@ -311,6 +317,20 @@ __global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const i
     h.aligned = aligned;
     *v.hdr = h;
   }
+}
+
+// The builder reads only its caller's inputs (never what a kernel of this library writes), so it
+// starts at once, beside the kernel before it (the writer, when a step runs writer, schedule and
+// decode), and waits for that kernel only before its first write to the schedule: its completion
+// still implies its predecessor's, which the decode kernel launched after it relies on.
+__global__ void __launch_bounds__(kThreads) build_decode_schedule_kernel(const int32_t* __restrict__ ctx_lens,
+                                                                        const int32_t* __restrict__ key_begin,
+                                                                        int batch, int next_n, int max_batch,
+                                                                        int64_t max_ctx, int ctas, DecodeCaps caps,
+                                                                        void* sched, int32_t* status) {
+  pdl_trigger();
+  build_decode_schedule_body(ctx_lens, key_begin, batch, next_n, max_batch, max_ctx, ctas, caps, sched, status);
+  pdl_wait();
 }
 
 }  // namespace

@@ -47,12 +47,10 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 
 constexpr int kMaxPrefillGroups = kMaxPrefillRows + kMaxBatch;
 
-__global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
+__device__ __forceinline__ void build_prefill_schedule_body(
     const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ row_ends,
     const int32_t* __restrict__ ctx_lens, int num_requests, int num_rows, int rows_per_unit, int table_width,
     int64_t units_cap, int64_t slots_cap, void* workspace, int32_t* status) {
-  pdl_wait();
-  pdl_trigger();
   extern __shared__ int s_dyn[];
   int* s_off = s_dyn;                   // [kMaxBatch + 1] groups before each request
   int* s_n = s_dyn + kMaxBatch + 1;     // [kMaxPrefillGroups] chunks per group, then unit offsets
@@ -74,6 +72,7 @@ __global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
   if (s_bad) {
     // Rows cannot be mapped to requests: emit empty units over all rows so every row's output is
     // written as "no key", and flag the call.
+    pdl_wait();
     if (tid == 0) set_status(status, IDX_FP4_DEV_BAD_ROWS);
     const int n = (num_rows + Q - 1) / Q;
     for (int j = tid; j < n; j += kSchedThreads) {
@@ -159,6 +158,9 @@ __global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
   }
   const int total_units = running;
   const bool fits = total_units <= units_cap;
+  // Everything above read only the caller's inputs; the tables below overwrite the workspace that
+  // the kernel before this one may still be reading.
+  pdl_wait();
   // pass 3: units and the per-row merge table
   for (int idx = tid; idx < ngroups; idx += kSchedThreads) {
     int g, r0, nq, kcap;
@@ -198,6 +200,20 @@ __global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
     h.slots_cap = static_cast<int32_t>(slots_cap);
     *hdr = h;
   }
+}
+
+// The builder reads only its caller's inputs (never what a kernel of this library writes), so it
+// starts at once, beside the kernel before it (the writer, when a step runs writer, schedule and
+// scorer), and waits for that kernel only before its first write to the workspace: its completion
+// still implies its predecessor's, which the scorer launched after it relies on.
+__global__ void __launch_bounds__(kSchedThreads) build_prefill_schedule_kernel(
+    const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ row_ends,
+    const int32_t* __restrict__ ctx_lens, int num_requests, int num_rows, int rows_per_unit, int table_width,
+    int64_t units_cap, int64_t slots_cap, void* workspace, int32_t* status) {
+  pdl_trigger();
+  build_prefill_schedule_body(cu_seqlens, row_ends, ctx_lens, num_requests, num_rows, rows_per_unit, table_width,
+                              units_cap, slots_cap, workspace, status);
+  pdl_wait();
 }
 
 }  // namespace
