@@ -4,8 +4,10 @@
 // fused writer stores packed E2M1 plus e8m0 scales in the index region; sub-commit
 // "Schedule, refuse and document ...": rows with slot < 0 are skipped). One warp encodes one
 // 128-dim vector: lane l owns dims 4l..4l+3, the 8 lanes of a 32-dim group reduce the
-// group's max magnitude with shuffles, and each lane stores its two packed bytes. A warp takes four
-// consecutive vectors at a time and issues their loads together.
+// group's max magnitude with shuffles, and each lane stores its two packed bytes. With enough
+// vectors to fill the GPU a warp takes four consecutive vectors at a time and issues their loads
+// together; a small input (a decode step's few keys and queries) keeps one vector per warp and
+// spreads over more SMs.
 // HBM-bound: 256 B read and 68 B written per vector.
 #include <cuda_runtime.h>
 
@@ -37,8 +39,6 @@ __device__ __forceinline__ uint32_t e2m1_code(float a) {
 __device__ __forceinline__ float bf16_lo(uint32_t two) { return __uint_as_float(two << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t two) { return __uint_as_float(two & 0xFFFF0000u); }
 
-constexpr int kVecPerWarp = 4;
-
 // Encode the warp's vector from this lane's dims 4l..4l+3 (raw bf16 pairs). Returns this lane's 2
 // packed bytes and the group's scale byte (valid in every lane).
 __device__ __forceinline__ void encode_lane(uint2 raw, uint32_t& packed2, uint32_t& scale_byte) {
@@ -61,6 +61,7 @@ __device__ __forceinline__ void encode_lane(uint2 raw, uint32_t& packed2, uint32
   scale_byte = static_cast<uint32_t>(e + 127);
 }
 
+template <int kVecPerWarp>
 __global__ void __launch_bounds__(256) quant_and_cache_kernel(const uint16_t* __restrict__ k, int64_t num_tokens,
                                                               const int32_t* __restrict__ slots, uint8_t* kv_packed,
                                                               uint8_t* kv_scale, int64_t num_pages,
@@ -123,11 +124,17 @@ cudaError_t launch_quant_and_cache(const uint16_t* k, int64_t num_tokens, const 
                                    cudaStream_t stream) {
   const int64_t vecs = num_tokens + num_q_vec;
   if (vecs == 0) return cudaSuccess;
-  const int64_t blocks_needed = (vecs + 8 * kVecPerWarp - 1) / (8 * kVecPerWarp);  // 8 warps per block
+  // four vectors per warp once that still gives every SM four blocks of 8 warps
+  const bool wide = vecs >= static_cast<int64_t>(num_sms) * 4 * 8 * 4;
+  const int per_block = wide ? 8 * 4 : 8;
+  const int64_t blocks_needed = (vecs + per_block - 1) / per_block;
   const int blocks = static_cast<int>(blocks_needed < static_cast<int64_t>(num_sms) * 16 ? blocks_needed
                                                                                           : static_cast<int64_t>(num_sms) * 16);
-  return launch_pdl(quant_and_cache_kernel, dim3(blocks), dim3(256), 0, stream, 1, false, k, num_tokens, slots, kv_packed,
-                    kv_scale, num_pages, q, num_q_vec, q_packed, q_scale, status);
+  if (wide)
+    return launch_pdl(quant_and_cache_kernel<4>, dim3(blocks), dim3(256), 0, stream, 1, false, k, num_tokens, slots,
+                      kv_packed, kv_scale, num_pages, q, num_q_vec, q_packed, q_scale, status);
+  return launch_pdl(quant_and_cache_kernel<1>, dim3(blocks), dim3(256), 0, stream, 1, false, k, num_tokens, slots,
+                    kv_packed, kv_scale, num_pages, q, num_q_vec, q_packed, q_scale, status);
 }
 
 }  // namespace idxfp4

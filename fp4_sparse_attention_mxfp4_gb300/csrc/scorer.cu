@@ -9,7 +9,8 @@
 //   * A 128-key tile (two pages) is the MMA M dimension, query rows x heads the N dimension:
 //     D[128 x N] = K[128 x 128] . Q^T, as two K=64 tcgen05.mma kind::mxf4 block-scaled MMAs
 //     accumulating fp32 in TMEM. TMEM lane = key, so the head sum is thread-local.
-//   * Twelve stage warps each own one stage of a 12-stage ring and fill it with 1-D bulk copies
+//   * Stage warps each own one stage of the ring (twelve; eight when the epilogue is two groups wide,
+//     which leaves room for the second row's selection areas) and fill it with 1-D bulk copies
 //     (cp.async.bulk): a page's four 1 KB group chunks land interleaved with the tile's other page,
 //     which makes the stage a canonical no-swizzle K-major operand (LBO 2048 B between 32-dim
 //     chunks, SBO 128 B between 8-key groups). The same warp rebuilds the tile's scale bytes from
@@ -37,7 +38,7 @@ namespace idxfp4 {
 namespace {
 
 constexpr uint32_t kEpiBarrier = 1;  // all epilogue warps
-constexpr uint32_t kSelBarrier = 2;  // the warps that run the unit-end selection
+constexpr uint32_t kSelBarrier = 2;  // the warps that run the unit-end selection (+1: the second row group)
 
 template <int H, int Q>
 struct ScorerCfg {
@@ -47,11 +48,15 @@ struct ScorerCfg {
   // with the stream at up to 64 columns per tile; wider tiles use two, with paired TMEM loads.
   static constexpr int GROUPS = N <= 64 ? 3 : 2;
   static constexpr int ACC = N <= 64 ? 6 : 2;  // TMEM accumulators
-  static constexpr int STAGES = 12;            // tiles in flight; one stage warp per stage
+  static constexpr int STAGES = GROUPS == 3 ? 12 : 8;  // tiles in flight; one stage warp per stage
   static constexpr int EPI_WARP0 = STAGES;
   static constexpr int EPI_WARPS = 4 * GROUPS;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int SEL_THREADS = 256;      // the unit-end selection runs on the first two groups
+  // Two rows on two epilogue groups (N = 128): each group selects one of the unit's rows, side by
+  // side, with its own histogram, scratch and barrier.
+  static constexpr int ROW_GROUPS = Q == 2 && EPI_WARPS == 8 ? 2 : 1;
+  static constexpr int SEL_NT = SEL_THREADS / ROW_GROUPS;  // threads selecting one row
   static constexpr int THREADS = (STAGES + EPI_WARPS) * 32;
   // Registers per thread: the launch gets 65536 / THREADS (rounded down to 8); the stage
   // warpgroups give registers back and the epilogue warpgroups take them, enough to hold a
@@ -79,15 +84,15 @@ struct ScorerCfg {
   static constexpr uint32_t OFF_W = OFF_SFB + 2 * 512;                   // [2][N] head weights
   static constexpr uint32_t OFF_LG = OFF_W + 2 * N * 4;                  // [Q][UCAP] ordered keys
   static constexpr uint32_t OFF_HW = OFF_LG + Q * UCAP * 4;              // [Q][4 quarters][1024] packed counts
-  static constexpr uint32_t OFF_HIST = OFF_HW + Q * 4 * kHistWords * 4;  // [2048]
-  static constexpr uint32_t OFF_SCR = OFF_HIST + 2048 * 4;               // [64]
+  static constexpr uint32_t OFF_HIST = OFF_HW + Q * 4 * kHistWords * 4;  // [ROW_GROUPS][2048]
+  static constexpr uint32_t OFF_SCR = OFF_HIST + ROW_GROUPS * 2048 * 4;  // [ROW_GROUPS][64]
   // Release barriers per accumulator, used in turn. A stage warp's tiles all use one accumulator,
   // STAGES / ACC of its tiles apart; with this many barriers the one it waits on has always seen
   // the completion before the awaited one.
   static constexpr int REL_RING = STAGES / ACC + 2;
   static_assert(STAGES % ACC == 0, "a stage warp keeps to one accumulator");
   static constexpr uint32_t NUM_BARS = 2 * STAGES + ACC + ACC * REL_RING + 2;
-  static constexpr uint32_t OFF_BAR = OFF_SCR + 64 * 4;
+  static constexpr uint32_t OFF_BAR = OFF_SCR + ROW_GROUPS * 64 * 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
   static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM");
@@ -248,8 +253,8 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
 
   if (warp < STAGES) {
     if constexpr (C::RESPLIT) warpgroup_regs_dec<C::STAGE_REGS>();
-    // ---------------- stage warps: warp w streams tiles w, w+12, ... through stage w and issues
-    // their MMAs. Issue work is spread over twelve warps because a bulk copy or a tcgen05
+    // ---------------- stage warps: warp w streams tiles w, w+STAGES, ... through stage w and issues
+    // their MMAs. Issue work is spread over many warps because a bulk copy or a tcgen05
     // instruction occupies its issuing warp or thread for a long time; one stage per warp also
     // keeps every wait on a barrier this warp alone advances.
     const int ps = warp;
@@ -507,8 +512,13 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
       }
       t0 += ntiles;
       named_barrier_sync(kEpiBarrier, C::EPI_THREADS);
-      // select each row: exactly min(k, valid keys) keys, in token order (first SEL_THREADS)
-      for (int r = 0; etid < C::SEL_THREADS && r < u.nq && r < Q; ++r) {
+      // select each row: exactly min(k, valid keys) keys, in token order (first SEL_THREADS; with
+      // two row groups each takes every other row)
+      const int rg = C::ROW_GROUPS == 1 ? 0 : etid / C::SEL_NT, stid = etid - rg * C::SEL_NT;
+      const uint32_t sbar = kSelBarrier + static_cast<uint32_t>(rg);
+      uint32_t* hist_g = hist + rg * 2048;
+      uint32_t* scr_g = scr + rg * 64;
+      for (int r = rg; etid < C::SEL_THREADS && r < u.nq && r < Q; r += C::ROW_GROUPS) {
         const uint32_t* keys = lg_base + r * C::UCAP;
         const int nvalid = max(0, end[r] - u.kb);
         const int kk = min(p.topk, nvalid);
@@ -516,14 +526,14 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
         const int kb = u.kb;
         const bool to_slot = u.slot >= 0;
         if (to_slot && u.slot + r >= p.cand_slots) {
-          if (etid == 0) set_status(p.status, IDX_FP4_DEV_CAPACITY);
+          if (stid == 0) set_status(p.status, IDX_FP4_DEV_CAPACITY);
           continue;
         }
         // The selection is emitted into this row's level-1 histogram area (free by then: 2048
         // (key, index) pairs fit its 16 KB) and then copied out with coalesced stores.
         uint2* sel = reinterpret_cast<uint2*>(hw_r);
-        uint2* spare = reinterpret_cast<uint2*>(hist) + lane;  // where keys not kept are written
-        select_topk<C::SEL_THREADS, 4>(keys, nvalid, kk, hw_r, hist, scr, etid, kSelBarrier,
+        uint2* spare = reinterpret_cast<uint2*>(hist_g) + lane;  // where keys not kept are written
+        select_topk<C::SEL_NT, 4>(keys, nvalid, kk, hw_r, hist_g, scr_g, stid, sbar,
                                        [=](bool keep, int pos, int x, uint32_t kv) {
                                          *(keep ? sel + pos : spare) = make_uint2(kv, static_cast<uint32_t>(x));
                                        });
@@ -531,7 +541,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
           const int64_t rowoff = static_cast<int64_t>(u.row + r) * p.topk;
           int32_t* oi = p.topk_idx + rowoff;
           float* ov = p.topk_val != nullptr ? p.topk_val + rowoff : nullptr;
-          for (int x = etid; x < p.topk; x += C::SEL_THREADS) {
+          for (int x = stid; x < p.topk; x += C::SEL_NT) {
             const uint2 e = x < kk ? sel[x] : make_uint2(0u, 0u);
             oi[x] = x < kk ? kb + static_cast<int>(e.y) : -1;
             if (ov != nullptr) ov[x] = x < kk ? key_to_float(e.x) : -__int_as_float(0x7f800000);
@@ -540,7 +550,7 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
           uint2* slot = p.cand + static_cast<int64_t>(u.slot + r) * static_cast<int64_t>(cand_slot_entries(p.topk));
           uint2* oc = slot + 2;
           uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-          for (int x = etid; x < kk; x += C::SEL_THREADS) {
+          for (int x = stid; x < kk; x += C::SEL_NT) {
             const uint2 e = sel[x];
             oc[x] = make_uint2(e.x, static_cast<uint32_t>(kb) + e.y);
             kmin = min(kmin, e.x);
@@ -552,23 +562,23 @@ __global__ void __launch_bounds__(ScorerCfg<H, Q>::THREADS, 1) scorer_kernel(con
           kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
           kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
           if (lane == 0) {
-            scr[32 + 2 * (etid >> 5)] = kmin;
-            scr[33 + 2 * (etid >> 5)] = kmax;
+            scr_g[32 + 2 * (stid >> 5)] = kmin;
+            scr_g[33 + 2 * (stid >> 5)] = kmax;
           }
-          named_barrier_sync(kSelBarrier, C::SEL_THREADS);
+          named_barrier_sync(sbar, C::SEL_NT);
           // odd counts get one pad entry so every list is a whole number of 16-byte pairs; key 0 is
           // below every logit and never selected
-          if (etid == 0) {
+          if (stid == 0) {
 #pragma unroll
-            for (int w2 = 0; w2 < C::SEL_THREADS / 32; ++w2) {
-              kmin = min(kmin, scr[32 + 2 * w2]);
-              kmax = max(kmax, scr[33 + 2 * w2]);
+            for (int w2 = 0; w2 < C::SEL_NT / 32; ++w2) {
+              kmin = min(kmin, scr_g[32 + 2 * w2]);
+              kmax = max(kmax, scr_g[33 + 2 * w2]);
             }
             if (kk & 1) oc[kk] = make_uint2(0u, 0xFFFFFFFFu);
             *reinterpret_cast<uint4*>(slot) = make_uint4(static_cast<uint32_t>(kk), kmin, kmax, 0u);
           }
         }
-        named_barrier_sync(kSelBarrier, C::SEL_THREADS);  // the area is reused by the next row
+        named_barrier_sync(sbar, C::SEL_NT);  // the area is reused by the next row
       }
       named_barrier_sync(kEpiBarrier, C::EPI_THREADS);  // selection done before the areas are cleared
       // the next unit counts into cleared histograms
