@@ -225,7 +225,7 @@ __device__ __forceinline__ uint2 warp_find_bin2(const uint32_t* fine, const uint
   static_assert((CB == 32 || CB == 64) && (FPER == 32 || FPER == 64), "one or two bins per lane");
   // One level: lane l holds bins PER*l .. PER*l + PER - 1 of h; returns the bin holding the need-th
   // largest element and the elements above it (above0: elements above h's first bin... last bin).
-  auto search = [&](const uint32_t* h, auto per_c, uint32_t above0, uint32_t& at_above) {
+  auto search = [lane, need](const uint32_t* h, auto per_c, uint32_t above0) {
     constexpr int PER = decltype(per_c)::value;
     uint32_t c0, c1 = 0u;
     if constexpr (PER == 2) {
@@ -247,15 +247,13 @@ __device__ __forceinline__ uint2 warp_find_bin2(const uint32_t* fine, const uint
     const int L = m != 0u ? 31 - __clz(m) : 0;
     // inside lane L: the upper bin first
     const bool hi = PER == 2 && a < need && need <= a + c1;
-    const int bin = lane * PER + (PER == 2 && !hi ? 0 : PER - 1);
+    const uint32_t bin = static_cast<uint32_t>(lane * PER + (PER == 2 && !hi ? 0 : PER - 1));
     const uint32_t ab = PER == 2 && !hi ? a + c1 : a;
-    at_above = __shfl_sync(0xFFFFFFFFu, ab, L);
-    return __shfl_sync(0xFFFFFFFFu, bin, L);
+    return make_uint2(__shfl_sync(0xFFFFFFFFu, bin, L), __shfl_sync(0xFFFFFFFFu, ab, L));
   };
-  uint32_t a1 = 0, a2 = 0;
-  const int cb = search(coarse, std::integral_constant<int, CB / 32>{}, 0u, a1);
-  const int fb = search(fine + cb * FPER, std::integral_constant<int, FPER / 32>{}, a1, a2);
-  return make_uint2(static_cast<uint32_t>(cb * FPER + fb), a2);
+  const uint2 c = search(coarse, std::integral_constant<int, CB / 32>{}, 0u);
+  const uint2 f = search(fine + c.x * FPER, std::integral_constant<int, FPER / 32>{}, c.y);
+  return make_uint2(c.x * FPER + f.x, f.y);
 }
 
 // The run of [0, n) that thread tid owns in run-based passes over 16-byte aligned keys: a multiple

@@ -136,8 +136,13 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Barrier over `threads` threads (whole warps, each executing it with all its lanes). The barrier
+// does not reconverge a warp whose lanes took different paths before it; warp-collective work after
+// it (shuffles, votes, reductions) would then run with the lanes apart, several times slower. The
+// __syncwarp() that follows reconverges every participating warp.
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+  __syncwarp();
 }
 
 // ---- tensor memory --------------------------------------------------------------------------
