@@ -334,6 +334,10 @@ class DecodeBench:
         torch.cuda.synchronize()
         self.g_prep, self.g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         self.g_write, self.g_sched = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        self.g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_step):
+            self.prep()
+            self.decode()
         with torch.cuda.graph(self.g_prep):
             self.prep()
         with torch.cuda.graph(self.g_dec):
@@ -349,33 +353,40 @@ class DecodeBench:
 
 
 def time_decode(bench: DecodeBench, steps: int, warmup: int, flush: L2Flush, dist=None, clock=None):
-    """Replays writer + schedule and the decode call `steps` times (after `warmup` untimed steps),
-    with events around each graph on the launching stream and an L2 flush between steps. Returns
-    per-step milliseconds of the whole step and of the decode call, and the clock record."""
+    """Replays the whole step (writer, schedule and decode call, one graph: each kernel may begin
+    while the one before it finishes) `steps` times after `warmup` untimed steps, with events around
+    each replay on the launching stream and an L2 flush between steps; then, as many times, the
+    writer and schedule graph followed by the decode call's own graph, with events around the
+    decode call alone. Returns per-step milliseconds of the whole step and of the decode call, and
+    the clock record (sampled over both passes)."""
     torch = bench.torch
     for _ in range(warmup):
-        bench.g_prep.replay()
-        bench.g_dec.replay()
+        bench.g_step.replay()
         flush()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize()
     barrier(dist)
     if clock is not None:
         clock.start()
     torch.cuda.synchronize()
-    for e0, e1, e2 in ev:
+    for e0, e1 in ev:
         e0.record()
-        bench.g_prep.replay()
+        bench.g_step.replay()
         e1.record()
-        bench.g_dec.replay()
-        e2.record()
         flush()
     torch.cuda.synchronize()
     barrier(dist)
+    for e0, e1 in ev_dec:
+        bench.g_prep.replay()
+        e0.record()
+        bench.g_dec.replay()
+        e1.record()
+        flush()
+    torch.cuda.synchronize()
     clocks = clock.stop() if clock is not None else None
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
     return step_ms, dec_ms, clocks
 
 
