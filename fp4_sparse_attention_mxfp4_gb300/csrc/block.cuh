@@ -81,6 +81,18 @@ __device__ __forceinline__ int2 blk_run(const Blk& B, int n) {
 template <int CB, int FPER>
 __device__ __forceinline__ uint2 warp_find_bin2(const uint32_t* fine, const uint32_t* coarse, uint32_t need, int lane);
 
+// The 64 coarse bins of a first-level histogram (coarse c sums fine bins 64c .. 64c + 63), written
+// to hist[kL1Bins + c] by warps from the fine bins: one pass over shared memory instead of a second
+// atomic per counted key (the keys crowd a few coarse bins, whose atomics would conflict). The
+// caller synchronises before and after.
+__device__ __forceinline__ void blk_coarse64(const Blk& B, uint32_t* hist) {
+  for (int c = B.warp(); c < 64; c += B.nw()) {
+    const uint2 v = reinterpret_cast<const uint2*>(hist + c * 64)[B.lane()];
+    const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, v.x + v.y);
+    if (B.lane() == 0) hist[kL1Bins + c] = sum;
+  }
+}
+
 // Threshold of an exact top-kk over n candidates whose first-level bin is known: `bin` holds the
 // kk-th largest key, and `need` (>= 1) of its keys are among the kk. Finds the low 20 bits of T from
 // the keys in `bin`, listed into `list` when they fit list_cap, else counted straight from the

@@ -116,8 +116,9 @@ struct DecodeCfg {
   static constexpr uint32_t OFF_SFB = OFF_QB + 2 * N * 64;          // [2][512]
   static constexpr uint32_t OFF_W = OFF_SFB + 2 * 512;              // [2][N]
   static constexpr uint32_t OFF_LG = OFF_W + 2 * N * 4;             // [Q][CAP] ordered keys
-  // Histograms of the range's first and last units (4096 fine bins and 64 coarse bins of 64),
-  // counted while streaming (one query row; with several rows they are counted after the stream).
+  // Histograms of the range's first and last units (4096 fine bins and 64 coarse bins of 64): the
+  // fine bins counted while streaming, the coarse ones summed from them when the selection starts
+  // (one query row; with several rows they are counted after the stream).
   static constexpr bool HIST_IN_STREAM = Q == 1;
   static constexpr int HST_WORDS = kL1Bins + 64;
   static constexpr uint32_t OFF_HST = OFF_LG + Q * CAP * 4;         // [2][HST_WORDS]
@@ -594,10 +595,7 @@ __device__ __forceinline__ void stream_epilogue_warp(const DecodeParams& p, uint
         const bool valid = key < ctx - Q + 1 + r;
         const uint32_t ok = ordered_key(logit[r]);
         if (at < C::CAP) lg[r * C::CAP + at] = valid ? ok : 0u;
-        if (C::HIST_IN_STREAM && valid && uh != nullptr) {
-          smem_red_add(&uh[ok >> kL1Shift], 1u);
-          smem_red_add(&uh[kL1Bins + (ok >> (kL1Shift + 6))], 1u);
-        }
+        if (C::HIST_IN_STREAM && valid && uh != nullptr) smem_red_add(&uh[ok >> kL1Shift], 1u);
         if (valid && p.logits_debug != nullptr && key < p.logits_stride)
           p.logits_debug[(static_cast<int64_t>(u.seq) * Q + r) * p.logits_stride + key] = logit[r];
       }
@@ -656,14 +654,12 @@ __device__ __forceinline__ void blk_select(const Blk& B, KeyAt key, TokAt tok, i
   // the first-level histogram (4096 fine bins, then 64 coarse): counted in the stream, or here
   const uint32_t* h = pre;
   if (h == nullptr) {
-    blk_zero(B, hist, kL1Bins + 64);
+    blk_zero(B, hist, kL1Bins);
     B.sync();
 #pragma unroll 1
-    for (int x = B.tid; x < n; x += B.nt) {
-      const uint32_t b = key(x) >> kL1Shift;
-      smem_red_add(&hist[b], 1u);
-      smem_red_add(&hist[kL1Bins + (b >> 6)], 1u);
-    }
+    for (int x = B.tid; x < n; x += B.nt) smem_red_add(&hist[key(x) >> kL1Shift], 1u);
+    B.sync();
+    blk_coarse64(B, hist);
     h = hist;
   }
   B.sync();
@@ -901,6 +897,8 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
   };
   auto exchanged = [&](const SegCtx& s) { return s.sg.nunits > 1 && s.kk < seg_keys(s); };
   if (B.tid == 0) ks->pending[g] = 0;
+  // the stream counted this group's range-end unit (area g) into the fine bins only
+  if constexpr (C::HIST_IN_STREAM) blk_coarse64(B, reinterpret_cast<uint32_t*>(smem + C::OFF_HST) + g * C::HST_WORDS);
   // A completed segment row: pad its final row, or count it for its sequence; the last segment of a
   // longer sequence merges the lists at the end of this group's selection (a merge reuses the areas
   // the group's exchanges hold). Only a range-end unit can belong to a sequence spanning rounds, so a
@@ -970,12 +968,11 @@ __device__ void select_round(const DecodeParams& p, uint8_t* smem, int slot, int
         if constexpr (C::HIST_IN_STREAM) {
           uh = reinterpret_cast<const uint32_t*>(smem + C::OFF_HST) + (ex == uf ? 0 : C::HST_WORDS);
         } else {
-          blk_zero(B, hist, kL1Bins + 64);
+          blk_zero(B, hist, kL1Bins);
           B.sync();
-          for (int x = B.tid; x < un; x += B.nt) {
-            smem_red_add(&hist[keys[x] >> kL1Shift], 1u);
-            smem_red_add(&hist[kL1Bins + (keys[x] >> (kL1Shift + 6))], 1u);
-          }
+          for (int x = B.tid; x < un; x += B.nt) smem_red_add(&hist[keys[x] >> kL1Shift], 1u);
+          B.sync();
+          blk_coarse64(B, hist);
           uh = hist;
         }
         B.sync();
